@@ -1,0 +1,244 @@
+"""GB300 (sm_103a) FP4 block-scaled quantized linear layer.
+
+Python face of libfp4bs.so (include/fp4bs.h). The functions below have the
+C-ABI names and only marshal arguments: PyTorch tensors supply device memory,
+PyTorch streams the CUDA stream, and every step of the quantizer and the GEMMs
+runs in the library's kernels. Nothing here falls back to another
+implementation: if the library is missing, calls raise.
+
+Method: "Pretraining Large Language Models with NVFP4" (arXiv 2509.25149),
+sections 4.1-4.4 and App. B-C, and the UE5M3 block-scale paper (arXiv
+2609.02846). See include/fp4bs.h for the operation each entry point performs.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+
+import torch
+
+from . import _lib
+from ._lib import (FP4_BLOCK_1x16, FP4_BLOCK_1x32, FP4_BLOCK_16x16, FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05,
+                   FP4_ORIENT_COLWISE, FP4_ORIENT_ROWWISE, FP4_ROUND_RNE, FP4_ROUND_SR, FP4_SCALE_E4M3,
+                   FP4_SCALE_UE5M3, FP4_SCALE_UE8M0, FP4_TSCALE_CURRENT, FP4_TSCALE_HELD, Fp4Error)
+
+__all__ = ["QTensor", "QuantConfig", "AmaxState", "fp4_quantize", "fp4_dequantize", "fp4_gemm",
+           "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
+           "fp4_workspace_bytes", "fp4_quantized_sizes", "Fp4Error", "Fp4Linear"]
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclass
+class QTensor:
+    """A quantized operand: rows x cols E2M1 codes (cols = dot dimension),
+    block scales, and the FP32 decode tensor scale."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    s_dec: torch.Tensor
+    rows: int
+    cols: int
+    scale_fmt: int = FP4_SCALE_E4M3
+    block_k: int = 16
+    layout: int = FP4_LAYOUT_TCGEN05
+
+    @staticmethod
+    def empty(rows: int, cols: int, scale_fmt: int = FP4_SCALE_E4M3, layout: int = FP4_LAYOUT_TCGEN05,
+              device="cuda") -> "QTensor":
+        bk = 32 if scale_fmt == FP4_SCALE_UE8M0 else 16
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty((rows * (cols // bk),), dtype=torch.uint8, device=device)
+        s_dec = torch.empty((4,), dtype=torch.float32, device=device)  # 16 bytes keeps later buffers aligned
+        return QTensor(codes, scales, s_dec, rows, cols, scale_fmt, bk, layout)
+
+    def desc(self) -> _lib.fp4_tensor_t:
+        return _lib.fp4_tensor_t(self.codes.data_ptr(), self.scales.data_ptr(), self.s_dec.data_ptr(),
+                                 self.rows, self.cols, self.scale_fmt, self.block_k, self.layout, 0)
+
+
+@dataclass
+class QuantConfig:
+    """Quantizer options (fp4_quant_params_t)."""
+    scale_fmt: int = FP4_SCALE_E4M3
+    block: int = FP4_BLOCK_1x16
+    round: int = FP4_ROUND_RNE
+    orient: int = FP4_ORIENT_ROWWISE
+    rht: bool = False
+    tscale: int = FP4_TSCALE_CURRENT
+    target_T: float = 448.0
+    refresh_every: int = 50
+    tensor_id: int = 0
+    layout: int = FP4_LAYOUT_TCGEN05
+    emit_transpose: bool = False
+    seed: int = 0
+    step: int = 0
+
+    def params(self) -> _lib.fp4_quant_params_t:
+        return _lib.fp4_quant_params_t(self.scale_fmt, self.block, self.round, self.orient, int(self.rht),
+                                       self.tscale, self.target_T, self.refresh_every, self.tensor_id,
+                                       self.layout, int(self.emit_transpose), 0, self.seed, self.step)
+
+
+class AmaxState:
+    """Device-resident held-amax record (fp4_amax_state_t, 16 bytes)."""
+
+    def __init__(self, device="cuda"):
+        self.buf = torch.zeros(4, dtype=torch.int32, device=device)
+
+    @property
+    def amax(self) -> float:
+        return float(self.buf[0:1].view(torch.float32).item())
+
+    @property
+    def valid(self) -> int:
+        return int(self.buf[1].item())
+
+    @property
+    def last_refresh_step(self) -> int:
+        return int(self.buf[2:4].view(torch.int64).item())
+
+
+def fp4_quantized_sizes(cfg: QuantConfig, rows: int, cols: int) -> tuple[int, int]:
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    p = cfg.params()
+    _lib.check(_lib.load().fp4_quantized_sizes(ctypes.byref(p), rows, cols, ctypes.byref(c), ctypes.byref(s)),
+               "fp4_quantized_sizes")
+    return c.value, s.value
+
+
+def fp4_workspace_bytes(cfg: QuantConfig, rows: int, cols: int) -> int:
+    p = cfg.params()
+    return _lib.load().fp4_workspace_bytes(ctypes.byref(p), rows, cols)
+
+
+def fp4_quantize(cfg: QuantConfig, x: torch.Tensor, out: QTensor, out_t: QTensor | None = None,
+                 state: AmaxState | None = None, counters: torch.Tensor | None = None,
+                 ws: torch.Tensor | None = None, stream=None) -> None:
+    """Quantize the row-major BF16 matrix `x` into `out` (see fp4_quantize in fp4bs.h)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    p = cfg.params()
+    d = out.desc()
+    dt = out_t.desc() if out_t is not None else None
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    st = _lib.load().fp4_quantize(ctypes.byref(p), _ptr(x), x.shape[0], x.shape[1], ctypes.byref(d),
+                                  ctypes.byref(dt) if dt is not None else None,
+                                  _ptr(state.buf) if state is not None else None, _ptr(counters), _ptr(ws),
+                                  ws_bytes, _stream(stream))
+    _lib.check(st, "fp4_quantize")
+
+
+def fp4_dequantize(t: QTensor, out: torch.Tensor, stream=None) -> None:
+    assert out.is_contiguous() and out.dtype in (torch.float32, torch.bfloat16)
+    d = t.desc()
+    _lib.check(_lib.load().fp4_dequantize(ctypes.byref(d), _ptr(out), int(out.dtype == torch.float32),
+                                          _stream(stream)), "fp4_dequantize")
+
+
+def fp4_gemm(a: QTensor, b: QTensor, d: torch.Tensor, accumulate: bool = False, stream=None) -> None:
+    assert d.is_contiguous() and d.dtype in (torch.float32, torch.bfloat16)
+    da, db = a.desc(), b.desc()
+    _lib.check(_lib.load().fp4_gemm(ctypes.byref(da), ctypes.byref(db), _ptr(d), int(d.dtype == torch.float32),
+                                    int(accumulate), _stream(stream)), "fp4_gemm")
+
+
+def fp4_linear_fprop(x: QTensor, w: QTensor, y: torch.Tensor, stream=None) -> None:
+    dx, dw = x.desc(), w.desc()
+    _lib.check(_lib.load().fp4_linear_fprop(ctypes.byref(dx), ctypes.byref(dw), _ptr(y), _stream(stream)),
+               "fp4_linear_fprop")
+
+
+def fp4_linear_dgrad(dy: QTensor, wt: QTensor, dx: torch.Tensor, stream=None) -> None:
+    a, b = dy.desc(), wt.desc()
+    _lib.check(_lib.load().fp4_linear_dgrad(ctypes.byref(a), ctypes.byref(b), _ptr(dx), _stream(stream)),
+               "fp4_linear_dgrad")
+
+
+def fp4_linear_wgrad(dyt: QTensor, xt: QTensor, dw: torch.Tensor, accumulate: bool = False, stream=None) -> None:
+    a, b = dyt.desc(), xt.desc()
+    _lib.check(_lib.load().fp4_linear_wgrad(ctypes.byref(a), ctypes.byref(b), _ptr(dw), int(accumulate),
+                                            _stream(stream)), "fp4_linear_wgrad")
+
+
+def fp4_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word."""
+    return _lib.load().fp4_device_status(_stream(stream))
+
+
+# --------------------------------------------------------------------------- linear layer
+@dataclass
+class Fp4Linear:
+    """One FP4 quantized linear layer Y = X W^T with its backward GEMMs
+    ("Pretraining LLMs with NVFP4", section 4.1, Fig. 5 and the recipe of
+    section 4: 16x16 weight scales, 1x16 activation/gradient scales, SR on
+    gradients, RHT16 on the Wgrad inputs). Owns the quantized buffers; each call
+    of `step` runs five quantizations and three GEMMs through the C ABI.
+
+    scale_fmt E4M3 gives NVFP4 with current tensor scaling; UE5M3 gives the
+    UE5M3 recipe (held amax refreshed every `refresh_every` steps with target T,
+    no RHT) on the emulated GEMM path."""
+    tokens: int
+    k_in: int
+    n_out: int
+    scale_fmt: int = FP4_SCALE_E4M3
+    rht: bool = True
+    seed: int = 0
+    layer: int = 0
+    target_T: float = 448.0
+    held: bool = False
+    refresh_every: int = 50
+    device: str = "cuda"
+    bufs: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        T, K, N, f, dev = self.tokens, self.k_in, self.n_out, self.scale_fmt, self.device
+        self.bufs = {
+            "x": QTensor.empty(T, K, f, device=dev),        # X rowwise      (Fprop A)
+            "w": QTensor.empty(N, K, f, device=dev),        # W 16x16        (Fprop B)
+            "wt": QTensor.empty(K, N, f, device=dev),       # W^T 16x16      (Dgrad B)
+            "dy": QTensor.empty(T, N, f, device=dev),       # dY rowwise SR  (Dgrad A)
+            "dyt": QTensor.empty(N, T, f, device=dev),      # dY^T colwise   (Wgrad A)
+            "xt": QTensor.empty(K, T, f, device=dev),       # X^T colwise    (Wgrad B)
+        }
+        self.ws = torch.empty(fp4_workspace_bytes(QuantConfig(), 1, 1) // 4 + 4, dtype=torch.float32,
+                              device=dev)
+        self.counters = torch.zeros((5, 4), dtype=torch.int64, device=dev)
+        self.states = [AmaxState(dev) for _ in range(5)] if self.held else [None] * 5
+
+    def _cfg(self, idx: int, step: int, **kw) -> QuantConfig:
+        base = dict(scale_fmt=self.scale_fmt, target_T=self.target_T, seed=self.seed,
+                    tensor_id=8 * self.layer + idx, step=step, refresh_every=self.refresh_every,
+                    tscale=FP4_TSCALE_HELD if self.held else FP4_TSCALE_CURRENT)
+        base.update(kw)
+        return QuantConfig(**base)
+
+    def quantize_all(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor, step: int = 0, stream=None):
+        b, c = self.bufs, self.counters
+        rht = self.rht
+        fp4_quantize(self._cfg(0, step), x, b["x"], state=self.states[0], counters=c[0], ws=self.ws,
+                     stream=stream)
+        fp4_quantize(self._cfg(2, step, block=FP4_BLOCK_16x16, emit_transpose=True), w, b["w"], b["wt"],
+                     state=self.states[2], counters=c[2], ws=self.ws, stream=stream)
+        fp4_quantize(self._cfg(3, step, round=FP4_ROUND_SR), dy, b["dy"], state=self.states[3], counters=c[3],
+                     ws=self.ws, stream=stream)
+        fp4_quantize(self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x, b["xt"], state=self.states[1],
+                     counters=c[1], ws=self.ws, stream=stream)
+        fp4_quantize(self._cfg(4, step, orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR), dy, b["dyt"],
+                     state=self.states[4], counters=c[4], ws=self.ws, stream=stream)
+
+    def gemms(self, y: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor, stream=None):
+        b = self.bufs
+        fp4_linear_fprop(b["x"], b["w"], y, stream=stream)
+        fp4_linear_dgrad(b["dy"], b["wt"], dx, stream=stream)
+        fp4_linear_wgrad(b["dyt"], b["xt"], dw, stream=stream)
+
+    def step(self, x, w, dy, y, dx, dw, step: int = 0, stream=None):
+        self.quantize_all(x, w, dy, step=step, stream=stream)
+        self.gemms(y, dx, dw, stream=stream)

@@ -1,0 +1,294 @@
+// api.cu -- the extern "C" entry points of libfp4bs.so: synchronous argument
+// checks, then kernel launches on the caller's stream. No entry point
+// allocates device memory.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "fp4_device.cuh"
+#include "internal.h"
+
+namespace fp4bs {
+
+// Per-device status word: bounded waits that time out and held-amax states
+// used before their first refresh record a code here (first error wins).
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+int* g_status_ptr[kMaxDevices];
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fp4_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4_OK : FP4_ERR_CUDA; }
+
+}  // namespace
+
+int num_sms() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+int* device_status_ptr() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+}  // namespace fp4bs
+
+using namespace fp4bs;
+
+namespace {
+
+int block_len(int block) { return block == FP4_BLOCK_1x32 ? 32 : 16; }
+
+// Checks shared by the quantizer entry points. Fills `job` on success.
+fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t rows, int64_t cols,
+                            const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
+                            uint64_t* counters, void* ws, size_t ws_bytes, QuantJob& job) {
+    if (p == nullptr || out == nullptr) return FP4_ERR_INVALID_ARG;
+    if (p->reserved != 0 || out->reserved != 0) return FP4_ERR_INVALID_ARG;
+    if (p->scale_fmt < 0 || p->scale_fmt > 2 || p->block < 0 || p->block > 2) return FP4_ERR_INVALID_ARG;
+    if (p->round < 0 || p->round > 1 || p->orient < 0 || p->orient > 1) return FP4_ERR_INVALID_ARG;
+    if (p->tscale < 0 || p->tscale > 1 || p->scale_layout < 0 || p->scale_layout > 1) return FP4_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return FP4_ERR_SHAPE;
+    if (p->tensor_id == 0xFFFFFFFFu) return FP4_ERR_INVALID_ARG;
+    const bool mx = p->scale_fmt == FP4_SCALE_UE8M0;
+    if (mx != (p->block == FP4_BLOCK_1x32)) return FP4_ERR_INVALID_ARG;
+    if (p->rht && (p->block != FP4_BLOCK_1x16 || p->orient != FP4_ORIENT_COLWISE)) return FP4_ERR_INVALID_ARG;
+    if (mx && (p->round != FP4_ROUND_RNE || p->orient != FP4_ORIENT_ROWWISE)) return FP4_ERR_UNSUPPORTED;
+    if (p->block == FP4_BLOCK_16x16 && p->round != FP4_ROUND_RNE) return FP4_ERR_UNSUPPORTED;
+    if (p->emit_transpose && p->block != FP4_BLOCK_16x16) return FP4_ERR_INVALID_ARG;
+    if (p->emit_transpose && out_t == nullptr) return FP4_ERR_INVALID_ARG;
+    const bool held = !mx && p->tscale == FP4_TSCALE_HELD;
+    if (held && (state == nullptr || p->refresh_every == 0)) return FP4_ERR_INVALID_ARG;
+    if (!mx && !(p->target_T > 0.0f && p->target_T <= 3.0e38f)) return FP4_ERR_INVALID_ARG;
+
+    const int bs = block_len(p->block);
+    const bool colwise = p->orient == FP4_ORIENT_COLWISE;
+    const int64_t R = colwise ? cols : rows, C = colwise ? rows : cols;
+    if (out->rows != R || out->cols != C) return FP4_ERR_SHAPE;
+    if (out->scale_fmt != p->scale_fmt || out->block_k != bs || out->scale_layout != p->scale_layout)
+        return FP4_ERR_INVALID_ARG;
+    if (C % bs != 0) return FP4_ERR_SHAPE;
+    if (p->block == FP4_BLOCK_16x16 && (R % 16 != 0)) return FP4_ERR_SHAPE;
+    if (colwise && p->block == FP4_BLOCK_1x16 && (cols % 8 != 0)) return FP4_ERR_SHAPE;
+    if (p->scale_layout == FP4_LAYOUT_TCGEN05 && (R % 128 != 0 || (C / bs) % 4 != 0)) return FP4_ERR_SHAPE;
+    if (p->emit_transpose) {
+        if (out_t->reserved != 0) return FP4_ERR_INVALID_ARG;
+        if (out_t->rows != C || out_t->cols != R) return FP4_ERR_SHAPE;
+        if (out_t->scale_fmt != p->scale_fmt || out_t->block_k != 16) return FP4_ERR_INVALID_ARG;
+        if (out_t->scale_layout == FP4_LAYOUT_TCGEN05 && (C % 128 != 0 || (R / 16) % 4 != 0)) return FP4_ERR_SHAPE;
+    }
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty) {
+        if (in == nullptr || out->codes == nullptr || out->scales == nullptr) return FP4_ERR_INVALID_ARG;
+        if (!aligned16(in) || !aligned16(out->codes)) return FP4_ERR_ALIGNMENT;
+        if (p->scale_layout == FP4_LAYOUT_TCGEN05 && !aligned16(out->scales)) return FP4_ERR_ALIGNMENT;
+        if (p->emit_transpose) {
+            if (out_t->codes == nullptr || out_t->scales == nullptr) return FP4_ERR_INVALID_ARG;
+            if (!aligned16(out_t->codes)) return FP4_ERR_ALIGNMENT;
+        }
+    }
+    if (!mx && out->s_dec_global == nullptr) return FP4_ERR_INVALID_ARG;
+
+    job = QuantJob{};
+    job.scale_fmt = p->scale_fmt;
+    job.block = p->block;
+    job.sr = p->round == FP4_ROUND_SR;
+    job.colwise = colwise;
+    job.rht = p->rht != 0;
+    job.held = held;
+    job.refresh = held ? (p->step % p->refresh_every == 0) : 1;
+    job.target_T = p->target_T;
+    job.tensor_id = p->tensor_id;
+    job.seed = p->seed;
+    job.step = p->step;
+    job.in = static_cast<const uint16_t*>(in);
+    job.rows = rows;
+    job.cols = cols;
+    job.codes = out->codes;
+    job.scales = out->scales;
+    job.s_dec = out->s_dec_global;
+    job.layout = out->scale_layout;
+    if (p->emit_transpose) {
+        job.codes_t = out_t->codes;
+        job.scales_t = out_t->scales;
+        job.s_dec_t = out_t->s_dec_global;
+        job.layout_t = out_t->scale_layout;
+    }
+    job.state = state;
+    job.counters = counters;
+    job.partials = static_cast<float*>(ws);
+    const int np = amax_partials_needed(job);
+    if (np > 0 && (ws == nullptr || ws_bytes < (size_t)np * sizeof(float))) return FP4_ERR_WORKSPACE;
+    if (np > 0 && !aligned16(ws)) return FP4_ERR_ALIGNMENT;
+    return FP4_OK;
+}
+
+fp4_status_t check_operand(const fp4_tensor_t* t) {
+    if (t == nullptr || t->codes == nullptr || t->scales == nullptr || t->s_dec_global == nullptr)
+        return FP4_ERR_INVALID_ARG;
+    if (t->reserved != 0) return FP4_ERR_INVALID_ARG;
+    if (!aligned16(t->codes) || !aligned16(t->scales)) return FP4_ERR_ALIGNMENT;
+    return FP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp4_abi_version(void) { return 1; }
+
+const char* fp4_status_string(fp4_status_t s) {
+    switch (s) {
+        case FP4_OK: return "ok";
+        case FP4_ERR_INVALID_ARG: return "invalid argument";
+        case FP4_ERR_UNSUPPORTED: return "unsupported combination";
+        case FP4_ERR_SHAPE: return "unsupported shape";
+        case FP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case FP4_ERR_STATE: return "held-amax state invalid on a non-refresh step";
+        case FP4_ERR_CUDA: return "CUDA runtime error";
+        case FP4_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case FP4_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+fp4_status_t fp4_quantized_sizes(const fp4_quant_params_t* p, int64_t rows, int64_t cols, size_t* codes_bytes,
+                                 size_t* scales_bytes) {
+    if (p == nullptr || codes_bytes == nullptr || scales_bytes == nullptr) return FP4_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || p->block < 0 || p->block > 2) return FP4_ERR_INVALID_ARG;
+    const int bs = block_len(p->block);
+    const int64_t R = p->orient == FP4_ORIENT_COLWISE ? cols : rows;
+    const int64_t C = p->orient == FP4_ORIENT_COLWISE ? rows : cols;
+    if (C % bs != 0) return FP4_ERR_SHAPE;
+    *codes_bytes = (size_t)(R * C / 2);
+    *scales_bytes = (size_t)(R * (C / bs));
+    return FP4_OK;
+}
+
+size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols) {
+    (void)rows;
+    (void)cols;
+    if (p == nullptr || p->scale_fmt == FP4_SCALE_UE8M0) return 0;
+    return (size_t)kMaxAmaxPartials * sizeof(float);
+}
+
+fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+                          const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
+                          uint64_t* counters, void* ws, size_t ws_bytes, void* stream) {
+    QuantJob job;
+    fp4_status_t s = check_quantize(p, in_bf16, rows, cols, out, out_t, state, counters, ws, ws_bytes, job);
+    if (s != FP4_OK) return s;
+    if (rows == 0 || cols == 0) return FP4_OK;
+    job.status = device_status_ptr();
+    if (job.status == nullptr) return FP4_ERR_CUDA;
+    return from_cuda(launch_quantize(job, static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void* stream) {
+    if (t == nullptr || out == nullptr) return FP4_ERR_INVALID_ARG;
+    if (t->rows == 0 || t->cols == 0) return FP4_OK;
+    fp4_status_t s = check_operand(t);
+    if (s != FP4_OK && s != FP4_ERR_ALIGNMENT) return s;
+    if (!aligned16(t->codes) || !aligned16(out)) return FP4_ERR_ALIGNMENT;
+    if (t->scale_fmt < 0 || t->scale_fmt > 2) return FP4_ERR_INVALID_ARG;
+    const int bs = t->scale_fmt == FP4_SCALE_UE8M0 ? 32 : 16;
+    if (t->block_k != bs || t->rows < 0 || t->cols % bs != 0) return FP4_ERR_SHAPE;
+    if (t->scale_layout == FP4_LAYOUT_TCGEN05 && (t->rows % 128 != 0 || (t->cols / bs) % 4 != 0))
+        return FP4_ERR_SHAPE;
+    DequantJob j{t->codes, t->scales, t->s_dec_global, t->rows, t->cols, t->scale_fmt, bs,
+                 t->scale_layout, out, out_fp32 != 0};
+    return from_cuda(launch_dequantize(j, static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
+                      void* stream) {
+    fp4_status_t s = check_operand(a);
+    if (s != FP4_OK) return s;
+    s = check_operand(b);
+    if (s != FP4_OK) return s;
+    if (d == nullptr) return FP4_ERR_INVALID_ARG;
+    if (!aligned16(d)) return FP4_ERR_ALIGNMENT;
+    if (accumulate && !out_fp32) return FP4_ERR_INVALID_ARG;
+    if (a->scale_fmt != b->scale_fmt || a->block_k != 16 || b->block_k != 16) return FP4_ERR_UNSUPPORTED;
+    if (a->scale_fmt == FP4_SCALE_UE8M0) return FP4_ERR_UNSUPPORTED;
+    if (a->scale_layout != FP4_LAYOUT_TCGEN05 || b->scale_layout != FP4_LAYOUT_TCGEN05) return FP4_ERR_UNSUPPORTED;
+    if (a->cols != b->cols) return FP4_ERR_SHAPE;
+    if (a->rows % 128 != 0 || b->rows % 128 != 0 || a->cols % 256 != 0 || a->cols <= 0 || a->rows <= 0 ||
+        b->rows <= 0)
+        return FP4_ERR_SHAPE;
+    GemmJob j{};
+    j.a_codes = a->codes;
+    j.a_scales = a->scales;
+    j.a_sdec = a->s_dec_global;
+    j.b_codes = b->codes;
+    j.b_scales = b->scales;
+    j.b_sdec = b->s_dec_global;
+    j.M = a->rows;
+    j.N = b->rows;
+    j.K = a->cols;
+    j.scale_fmt = a->scale_fmt;
+    j.d = d;
+    j.out_fp32 = out_fp32 != 0;
+    j.accumulate = accumulate != 0;
+    j.status = device_status_ptr();
+    if (j.status == nullptr) return FP4_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (a->scale_fmt == FP4_SCALE_E4M3) return from_cuda(launch_gemm_nvfp4(j, st));
+    return from_cuda(launch_gemm_ue5m3(j, st));
+}
+
+fp4_status_t fp4_linear_fprop(const fp4_tensor_t* x, const fp4_tensor_t* w, void* y_bf16, void* stream) {
+    return fp4_gemm(x, w, y_bf16, 0, 0, stream);
+}
+
+fp4_status_t fp4_linear_dgrad(const fp4_tensor_t* dy, const fp4_tensor_t* wt, void* dx_bf16, void* stream) {
+    return fp4_gemm(dy, wt, dx_bf16, 0, 0, stream);
+}
+
+fp4_status_t fp4_linear_wgrad(const fp4_tensor_t* dyt, const fp4_tensor_t* xt, float* dw_fp32, int accumulate,
+                              void* stream) {
+    return fp4_gemm(dyt, xt, dw_fp32, 1, accumulate, stream);
+}
+
+fp4_status_t fp4_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP4_ERR_CUDA;
+    int* p = device_status_ptr();
+    if (p == nullptr) return FP4_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FP4_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FP4_ERR_CUDA;
+    }
+    return static_cast<fp4_status_t>(v);
+}
+
+}  // extern "C"

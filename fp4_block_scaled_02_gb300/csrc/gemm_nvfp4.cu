@@ -1,0 +1,328 @@
+// gemm_nvfp4.cu -- block-scaled NVFP4 GEMM on the sm_103a tensor cores.
+//
+// D[M x N] = s_dec,G,A * s_dec,G,B * sum_k (a_mk s_A)(b_nk s_B): "Pretraining
+// Large Language Models with NVFP4" (arXiv 2509.25149), App. B.3 ("Tensor Core
+// processing": the tensor core reads one 8-bit scale per 16-element block,
+// multiplies each block's partial dot product by both decode scales and
+// accumulates in FP32; the global decode scales are applied to the output) and
+// section A3 (hardware support). Both operands are K-major packed E2M1 with
+// UE4M3 scales in the tensor-core scale-factor layout.
+//
+// Design (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      : TMA producer -- A/B code tiles (128-byte swizzled rows of 256
+//                 FP4 values) and the tiles' scale chunks (1-D bulk copies) into
+//                 a STAGES-deep shared-memory ring guarded by mbarriers;
+//   warp 1      : allocates tensor memory and one lane issues, per stage, four
+//                 tcgen05.cp scale copies per operand into tensor memory and four
+//                 tcgen05.mma kind::mxf4nvf4 (K = 64 each), then commits the
+//                 stage back to the producer;
+//   warps 2-5   : epilogue -- tcgen05.ld the FP32 accumulator (each warp owns
+//                 its 32-lane quadrant), scale by alpha, store BF16 / FP32.
+// Two accumulators in tensor memory let the epilogue of tile t overlap the
+// main loop of tile t+1. Every mbarrier wait is bounded (see tcgen05.cuh).
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace fp4bs {
+
+namespace {
+
+struct GemmParams {
+    const uint8_t* a_scales;
+    const uint8_t* b_scales;
+    const float* a_sdec;
+    const float* b_sdec;
+    void* d;
+    int64_t M, N, K;
+    int accumulate;
+    int* status;
+};
+
+template <int BN_, int STAGES_>
+struct NvCfg {
+    static constexpr int BM = 128, BN = BN_, STAGES = STAGES_;
+    static constexpr int BK = 256;                 // FP4 values per stage = 128 bytes per row
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int SFA_BYTES = BM * 16;      // 16 scale blocks of 16 per row per stage
+    static constexpr int SFB_BYTES = BN * 16;
+    static constexpr uint32_t TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int NUM_ACC = (BN <= 128) ? 2 : 1;
+    static constexpr int SF_COLS_A = 16;           // 4 MMAs x 4 columns
+    static constexpr int SF_COLS_B = 4 * (BN / 32);  // 4 MMAs x (BN / 32) columns
+    static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
+    static constexpr int SF_TMEM_BASE = NUM_ACC * BN;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(SF_TMEM_BASE + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+    static constexpr int THREADS = 192;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+template <class Cfg, bool OUT32>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                      const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sb = tc::smem_u32(smem);
+    auto full_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (Cfg::STAGES + s); };
+    auto accf_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + a); };
+    auto acce_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + Cfg::NUM_ACC + a); };
+    const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + 2 * Cfg::NUM_ACC);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+
+    const int64_t num_m = p.M / Cfg::BM, num_n = p.N / Cfg::BN, tiles = num_m * num_n;
+    const int num_k = (int)(p.K / Cfg::BK);
+    const int64_t chunks_k = p.K / 64;  // scale chunks (128 rows x 64 values) along K
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            tc::mbar_init(full_bar(s), 1);
+            tc::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < Cfg::NUM_ACC; ++a) {
+            tc::mbar_init(accf_bar(a), 1);
+            tc::mbar_init(acce_bar(a), 4);
+        }
+        tc::mbar_init(drain_bar, 1);
+        tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmap_a);
+        tc::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                const int64_t mb = tile % num_m, nb = tile / num_m;
+                for (int kb = 0; kb < num_k; ++kb, ++it) {
+                    const int s = (int)(it % Cfg::STAGES);
+                    const uint32_t ph = (it / Cfg::STAGES) & 1u;
+                    if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(full_bar(s), Cfg::TX);
+                    tc::tma_load_2d(sb + Cfg::OFF_A + s * Cfg::A_BYTES, &tmap_a, kb * 128, (int32_t)(mb * Cfg::BM),
+                                    full_bar(s));
+                    tc::tma_load_2d(sb + Cfg::OFF_B + s * Cfg::B_BYTES, &tmap_b, kb * 128, (int32_t)(nb * Cfg::BN),
+                                    full_bar(s));
+                    tc::bulk_load(sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
+                                  p.a_scales + 512 * (mb * chunks_k + 4 * kb), Cfg::SFA_BYTES, full_bar(s));
+#pragma unroll
+                    for (int h = 0; h < Cfg::BN / 128; ++h)
+                        tc::bulk_load(sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + 2048 * h,
+                                      p.b_scales + 512 * ((nb * (Cfg::BN / 128) + h) * chunks_k + 4 * kb), 2048,
+                                      full_bar(s));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = tc::idesc_mxf4nvf4(Cfg::BM, Cfg::BN);
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
+                const int acc = local % Cfg::NUM_ACC;
+                const uint32_t aph = (uint32_t)(local / Cfg::NUM_ACC) & 1u;
+                if (!tc::mbar_wait(acce_bar(acc), aph ^ 1u, p.status)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * Cfg::BN);
+                for (int kb = 0; kb < num_k; ++kb, ++it) {
+                    const int s = (int)(it % Cfg::STAGES);
+                    const uint32_t ph = (it / Cfg::STAGES) & 1u;
+                    if (!tc::mbar_wait(full_bar(s), ph, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t sfa_t = tmem + (uint32_t)(Cfg::SF_TMEM_BASE + s * Cfg::SF_COLS_STAGE);
+                    const uint32_t sfb_t = sfa_t + Cfg::SF_COLS_A;
+                    const uint32_t a_s = sb + Cfg::OFF_A + s * Cfg::A_BYTES;
+                    const uint32_t b_s = sb + Cfg::OFF_B + s * Cfg::B_BYTES;
+                    const uint32_t sfa_s = sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
+                    const uint32_t sfb_s = sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        tc::cp_32x128b_warpx4(sfa_t + 4 * kk, tc::scale_chunk_desc(sfa_s + 512 * kk));
+#pragma unroll
+                        for (int h = 0; h < Cfg::BN / 128; ++h)
+                            tc::cp_32x128b_warpx4(sfb_t + (Cfg::BN / 32) * kk + 4 * h,
+                                                  tc::scale_chunk_desc(sfb_s + 2048 * h + 512 * kk));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        tc::mma_mxf4nvf4(d_tmem, tc::kmajor_sw128_desc(a_s + 32 * kk),
+                                         tc::kmajor_sw128_desc(b_s + 32 * kk), IDESC, sfa_t + 4 * kk,
+                                         sfb_t + (Cfg::BN / 32) * kk, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc::commit(empty_bar(s));
+                }
+                if (ok) tc::commit(accf_bar(acc));
+            }
+            // wait until every MMA this thread issued has retired before the
+            // tensor memory is released
+            tc::commit(drain_bar);
+            tc::mbar_wait(drain_bar, 0, p.status);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // the TMEM lane quadrant this warp may access
+        const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
+        int local = 0;
+        for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+            const int64_t mb = tile % num_m, nb = tile / num_m;
+            const int acc = local % Cfg::NUM_ACC;
+            const uint32_t aph = (uint32_t)(local / Cfg::NUM_ACC) & 1u;
+            if (!tc::mbar_wait(accf_bar(acc), aph, p.status)) break;
+            tc::fence_after_sync();
+            const int64_t m = mb * Cfg::BM + q * 32 + lane;
+            const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Cfg::BN);
+#pragma unroll 1
+            for (int c = 0; c < Cfg::BN; c += 32) {
+                uint32_t r[32];
+                tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
+                tc::tmem_ld_wait();
+                if (c + 32 == Cfg::BN) {
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(acce_bar(acc));
+                }
+                const int64_t n0 = nb * Cfg::BN + c;
+                if (OUT32) {
+                    float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        float4 o = make_float4(__fmul_rn(__uint_as_float(r[4 * v + 0]), alpha),
+                                               __fmul_rn(__uint_as_float(r[4 * v + 1]), alpha),
+                                               __fmul_rn(__uint_as_float(r[4 * v + 2]), alpha),
+                                               __fmul_rn(__uint_as_float(r[4 * v + 3]), alpha));
+                        if (p.accumulate) {
+                            const float4 old = reinterpret_cast<const float4*>(dst)[v];
+                            o.x = __fadd_rn(o.x, old.x);
+                            o.y = __fadd_rn(o.y, old.y);
+                            o.z = __fadd_rn(o.z, old.z);
+                            o.w = __fadd_rn(o.w, old.w);
+                        }
+                        reinterpret_cast<float4*>(dst)[v] = o;
+                    }
+                } else {
+                    uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const __nv_bfloat162 h =
+                                __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * v + 2 * k]), alpha),
+                                                      __fmul_rn(__uint_as_float(r[8 * v + 2 * k + 1]), alpha));
+                            w[k] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+// 2-D byte-matrix tensor map (rows x row_bytes, row-major) with a box of
+// box_rows x 128 bytes and 128-byte swizzling: each box row is one swizzle atom
+// row of a K-major tcgen05 operand.
+bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+template <class Cfg, bool OUT32>
+cudaError_t run_nvfp4(const GemmJob& j, cudaStream_t st) {
+    CUtensorMap ta, tb;
+    if (!make_tmap_u8_sw128(&ta, j.a_codes, j.M, j.K / 2, Cfg::BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8_sw128(&tb, j.b_codes, j.N, j.K / 2, Cfg::BN)) return cudaErrorInvalidValue;
+    GemmParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status};
+    auto kern = gemm_nvfp4_kernel<Cfg, OUT32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (j.M / Cfg::BM) * (j.N / Cfg::BN);
+    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+using NvDefault = NvCfg<128, 6>;
+
+}  // namespace
+
+cudaError_t launch_gemm_nvfp4(const GemmJob& j, cudaStream_t st) {
+    if (j.out_fp32) return run_nvfp4<NvDefault, true>(j, st);
+    return run_nvfp4<NvDefault, false>(j, st);
+}
+
+}  // namespace fp4bs

@@ -1,0 +1,352 @@
+// gemm_ue5m3.cu -- software-emulated UE5M3 block-scaled GEMM on sm_103a.
+//
+// The UE5M3 pretraining paper (arXiv 2609.02846, abstract and limitations)
+// runs its UE5M3-scaled FP4 GEMMs in software emulation because no tensor core
+// reads UE5M3 block scales. The product it needs is the same block-scaled sum
+// as NVFP4 ("Pretraining LLMs with NVFP4", App. B.3):
+//     D[m,n] = s_dec,G,A * s_dec,G,B * sum_k (a_mk s_A)(b_nk s_B).
+// Each decoded operand value a * s (an E2M1 value times a UE5M3 scale) has at
+// most 6 significant bits and an exponent inside the BF16 range, so it is EXACT
+// in BF16; a BF16 x BF16 tensor-core MMA with FP32 accumulation then computes
+// the same products the native path would.
+//
+// Design (one persistent CTA per SM, 128 x 128 output tiles, 320 threads):
+//   warp 0    : TMA producer -- raw FP4 code tiles (K = 256) and scale chunks;
+//   warps 2-5 : decode -- per K = 64 slice, each thread expands its row's
+//               16-byte code chunks into BF16 with byte-permute table lookups,
+//               multiplies by the block scale (packed BF16 multiply, exact) and
+//               writes the 128-byte-swizzled K-major layout the tensor core reads;
+//   warp 1    : one lane issues tcgen05.mma kind::f16 (K = 16) on each decoded
+//               slice and commits it back to the decoders;
+//   warps 6-9 : epilogue (tcgen05.ld, x alpha, BF16/FP32 store).
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace fp4bs {
+
+namespace {
+
+struct EmuParams {
+    const uint8_t* a_scales;
+    const uint8_t* b_scales;
+    const float* a_sdec;
+    const float* b_sdec;
+    void* d;
+    int64_t M, N, K;
+    int accumulate;
+    int* status;
+};
+
+struct EmuCfg {
+    static constexpr int BM = 128, BN = 128, BK = 256;
+    static constexpr int RAW_STAGES = 3, DEC_STAGES = 3;
+    static constexpr int RAW_A = BM * 128, RAW_B = BN * 128;     // FP4 codes, 128 B per row
+    static constexpr int RAW_SFA = BM * 16, RAW_SFB = BN * 16;   // 16 scale blocks per row
+    static constexpr uint32_t RAW_TX = RAW_A + RAW_B + RAW_SFA + RAW_SFB;
+    static constexpr int DEC_A = BM * 128, DEC_B = BN * 128;     // BF16, K = 64 -> 128 B per row
+    static constexpr int OFF_RAW_A = 0;
+    static constexpr int OFF_RAW_B = OFF_RAW_A + RAW_STAGES * RAW_A;
+    static constexpr int OFF_DEC_A = OFF_RAW_B + RAW_STAGES * RAW_B;
+    static constexpr int OFF_DEC_B = OFF_DEC_A + DEC_STAGES * DEC_A;
+    static constexpr int OFF_SFA = OFF_DEC_B + DEC_STAGES * DEC_B;
+    static constexpr int OFF_SFB = OFF_SFA + RAW_STAGES * RAW_SFA;
+    static constexpr int OFF_BAR = OFF_SFB + RAW_STAGES * RAW_SFB;
+    static constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * DEC_STAGES + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int THREADS = 320;
+    static constexpr int TMEM_COLS = 256;  // two 128-column FP32 accumulators
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// Eight E2M1 codes (one 32-bit word, element i in nibble i) -> eight BF16
+// values times the block scale. The E2M1 magnitudes {0,.5,1,1.5,2,3,4,6} have
+// BF16 patterns 0x0000, 0x3F00, 0x3F80, 0x3FC0, 0x4000, 0x4040, 0x4080, 0x40C0:
+// their high and low bytes are looked up with byte permutes indexed by the
+// 3-bit magnitude codes, the code's sign bit goes to bit 15, and the packed
+// BF16 multiply by the scale is exact (at most 6 significant bits).
+__device__ __forceinline__ uint4 decode8(uint32_t w, __nv_bfloat162 scale2) {
+    constexpr uint32_t HI_0123 = 0x3F3F3F00u, HI_4567 = 0x40404040u;
+    constexpr uint32_t LO_0123 = 0xC0800000u, LO_4567 = 0xC0804000u;
+    const uint32_t sel_a = w & 0x7777u, sel_b = (w >> 16) & 0x7777u;
+    uint32_t hi_a = __byte_perm(HI_0123, HI_4567, sel_a), lo_a = __byte_perm(LO_0123, LO_4567, sel_a);
+    uint32_t hi_b = __byte_perm(HI_0123, HI_4567, sel_b), lo_b = __byte_perm(LO_0123, LO_4567, sel_b);
+    const uint32_t u = w & 0x88888888u;
+    const uint32_t even = u << 4, odd = u;  // bit 7 of byte k: sign of element 2k / 2k+1
+    hi_a |= __byte_perm(even, odd, 0x5140) & 0x80808080u;
+    hi_b |= __byte_perm(even, odd, 0x7362) & 0x80808080u;
+    uint32_t p[4] = {__byte_perm(lo_a, hi_a, 0x5140), __byte_perm(lo_a, hi_a, 0x7362),
+                     __byte_perm(lo_b, hi_b, 0x5140), __byte_perm(lo_b, hi_b, 0x7362)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&p[k]);
+        v = __hmul2(v, scale2);
+        p[k] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+__device__ __forceinline__ __nv_bfloat162 ue5m3_bf16x2(uint32_t code) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(scale_decode_m3<15>(code));
+    return __nv_bfloat162(h, h);
+}
+
+// Decode one operand row's two 16-byte raw chunks (K = 64 values) of slice kk
+// into the swizzled BF16 row of the decoded tile.
+__device__ __forceinline__ void decode_row(const uint8_t* raw, const uint8_t* sf, uint8_t* dec, int r, int kk) {
+    const int sw = r & 7;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int cr = 2 * kk + h;  // raw 16-byte chunk: values 32 cr .. 32 cr + 31 of the 256
+        const uint4 codes = *reinterpret_cast<const uint4*>(raw + r * 128 + ((cr ^ sw) << 4));
+        const uint16_t s2 =
+            *reinterpret_cast<const uint16_t*>(sf + 512 * (cr >> 1) + 16 * (r & 31) + 4 * ((r >> 5) & 3) + 2 * (cr & 1));
+        const __nv_bfloat162 s_lo = ue5m3_bf16x2(s2 & 0xFFu), s_hi = ue5m3_bf16x2(s2 >> 8);
+        const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int oc = 4 * h + k;  // output 16-byte chunk (8 BF16 values) of the 128-byte row
+            *reinterpret_cast<uint4*>(dec + r * 128 + ((oc ^ sw) << 4)) = decode8(w[k], k < 2 ? s_lo : s_hi);
+        }
+    }
+}
+
+template <bool OUT32>
+__global__ void __launch_bounds__(EmuCfg::THREADS, 1)
+    gemm_ue5m3_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                      const EmuParams p) {
+    using C = EmuCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sb = tc::smem_u32(smem);
+    auto bar = [&](int i) { return sb + C::OFF_BAR + 8u * i; };
+    auto raw_full = [&](int s) { return bar(s); };
+    auto raw_empty = [&](int s) { return bar(C::RAW_STAGES + s); };
+    auto dec_full = [&](int s) { return bar(2 * C::RAW_STAGES + s); };
+    auto dec_empty = [&](int s) { return bar(2 * C::RAW_STAGES + C::DEC_STAGES + s); };
+    auto accf = [&](int a) { return bar(2 * C::RAW_STAGES + 2 * C::DEC_STAGES + a); };
+    auto acce = [&](int a) { return bar(2 * C::RAW_STAGES + 2 * C::DEC_STAGES + 2 + a); };
+    const uint32_t drain = bar(2 * C::RAW_STAGES + 2 * C::DEC_STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+
+    const int64_t num_m = p.M / C::BM, num_n = p.N / C::BN, tiles = num_m * num_n;
+    const int num_k = (int)(p.K / C::BK);
+    const int64_t chunks_k = p.K / 64;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < C::RAW_STAGES; ++s) {
+            tc::mbar_init(raw_full(s), 1);
+            tc::mbar_init(raw_empty(s), 4);
+        }
+        for (int s = 0; s < C::DEC_STAGES; ++s) {
+            tc::mbar_init(dec_full(s), 4);
+            tc::mbar_init(dec_empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(accf(a), 1);
+            tc::mbar_init(acce(a), 4);
+        }
+        tc::mbar_init(drain, 1);
+        tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmap_a);
+        tc::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                const int64_t mb = tile % num_m, nb = tile / num_m;
+                for (int kb = 0; kb < num_k; ++kb, ++it) {
+                    const int s = (int)(it % C::RAW_STAGES);
+                    const uint32_t ph = (it / C::RAW_STAGES) & 1u;
+                    if (!tc::mbar_wait(raw_empty(s), ph ^ 1u, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(raw_full(s), C::RAW_TX);
+                    tc::tma_load_2d(sb + C::OFF_RAW_A + s * C::RAW_A, &tmap_a, kb * 128, (int32_t)(mb * C::BM),
+                                    raw_full(s));
+                    tc::tma_load_2d(sb + C::OFF_RAW_B + s * C::RAW_B, &tmap_b, kb * 128, (int32_t)(nb * C::BN),
+                                    raw_full(s));
+                    tc::bulk_load(sb + C::OFF_SFA + s * C::RAW_SFA, p.a_scales + 512 * (mb * chunks_k + 4 * kb),
+                                  C::RAW_SFA, raw_full(s));
+                    tc::bulk_load(sb + C::OFF_SFB + s * C::RAW_SFB, p.b_scales + 512 * (nb * chunks_k + 4 * kb),
+                                  C::RAW_SFB, raw_full(s));
+                }
+            }
+        }
+    } else if (warp >= 2 && warp < 6) {
+        // ------------------------------------------------------------ decoders
+        const int r = threadIdx.x - 64;  // operand row 0..127 of the tile
+        uint32_t it_raw = 0, it_dec = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            for (int kb = 0; kb < num_k && ok; ++kb, ++it_raw) {
+                const int rs = (int)(it_raw % C::RAW_STAGES);
+                if (!tc::mbar_wait(raw_full(rs), (it_raw / C::RAW_STAGES) & 1u, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw_a = smem + C::OFF_RAW_A + rs * C::RAW_A;
+                const uint8_t* raw_b = smem + C::OFF_RAW_B + rs * C::RAW_B;
+                const uint8_t* sfa = smem + C::OFF_SFA + rs * C::RAW_SFA;
+                const uint8_t* sfb = smem + C::OFF_SFB + rs * C::RAW_SFB;
+                for (int kk = 0; kk < 4; ++kk, ++it_dec) {
+                    const int ds = (int)(it_dec % C::DEC_STAGES);
+                    if (!tc::mbar_wait(dec_empty(ds), ((it_dec / C::DEC_STAGES) & 1u) ^ 1u, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    decode_row(raw_a, sfa, smem + C::OFF_DEC_A + ds * C::DEC_A, r, kk);
+                    decode_row(raw_b, sfb, smem + C::OFF_DEC_B + ds * C::DEC_B, r, kk);
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(dec_full(ds));
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(raw_empty(rs));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = tc::idesc_bf16(C::BM, C::BN);
+            uint32_t it_dec = 0;
+            int local = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+                if (!tc::mbar_wait(acce(acc), aph ^ 1u, p.status)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * C::BN);
+                for (int kb = 0; kb < num_k && ok; ++kb) {
+                    for (int kk = 0; kk < 4; ++kk, ++it_dec) {
+                        const int ds = (int)(it_dec % C::DEC_STAGES);
+                        if (!tc::mbar_wait(dec_full(ds), (it_dec / C::DEC_STAGES) & 1u, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint32_t a_s = sb + C::OFF_DEC_A + ds * C::DEC_A;
+                        const uint32_t b_s = sb + C::OFF_DEC_B + ds * C::DEC_B;
+#pragma unroll
+                        for (int k16 = 0; k16 < 4; ++k16)
+                            tc::mma_bf16(d_tmem, tc::kmajor_sw128_desc(a_s + 32 * k16),
+                                         tc::kmajor_sw128_desc(b_s + 32 * k16), IDESC,
+                                         (kb | kk | k16) != 0 ? 1u : 0u);
+                        tc::commit(dec_empty(ds));
+                    }
+                }
+                if (ok) tc::commit(accf(acc));
+            }
+            tc::commit(drain);
+            tc::mbar_wait(drain, 0, p.status);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 6-9)
+        const int q = warp & 3;
+        const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
+        int local = 0;
+        for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+            const int64_t mb = tile % num_m, nb = tile / num_m;
+            const int acc = local & 1;
+            const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+            if (!tc::mbar_wait(accf(acc), aph, p.status)) break;
+            tc::fence_after_sync();
+            const int64_t m = mb * C::BM + q * 32 + lane;
+            const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::BN);
+#pragma unroll 1
+            for (int c = 0; c < C::BN; c += 32) {
+                uint32_t rr[32];
+                tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, rr);
+                tc::tmem_ld_wait();
+                if (c + 32 == C::BN) {
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(acce(acc));
+                }
+                const int64_t n0 = nb * C::BN + c;
+                if (OUT32) {
+                    float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        float4 o = make_float4(__fmul_rn(__uint_as_float(rr[4 * v + 0]), alpha),
+                                               __fmul_rn(__uint_as_float(rr[4 * v + 1]), alpha),
+                                               __fmul_rn(__uint_as_float(rr[4 * v + 2]), alpha),
+                                               __fmul_rn(__uint_as_float(rr[4 * v + 3]), alpha));
+                        if (p.accumulate) {
+                            const float4 old = reinterpret_cast<const float4*>(dst)[v];
+                            o.x = __fadd_rn(o.x, old.x);
+                            o.y = __fadd_rn(o.y, old.y);
+                            o.z = __fadd_rn(o.z, old.z);
+                            o.w = __fadd_rn(o.w, old.w);
+                        }
+                        reinterpret_cast<float4*>(dst)[v] = o;
+                    }
+                } else {
+                    uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const __nv_bfloat162 h =
+                                __floats2bfloat162_rn(__fmul_rn(__uint_as_float(rr[8 * v + 2 * k]), alpha),
+                                                      __fmul_rn(__uint_as_float(rr[8 * v + 2 * k + 1]), alpha));
+                            w[k] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <bool OUT32>
+cudaError_t run_emu(const GemmJob& j, cudaStream_t st) {
+    CUtensorMap ta, tb;
+    if (!make_tmap_u8_sw128(&ta, j.a_codes, j.M, j.K / 2, EmuCfg::BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8_sw128(&tb, j.b_codes, j.N, j.K / 2, EmuCfg::BN)) return cudaErrorInvalidValue;
+    EmuParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status};
+    auto kern = gemm_ue5m3_kernel<OUT32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, EmuCfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (j.M / EmuCfg::BM) * (j.N / EmuCfg::BN);
+    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+    kern<<<grid, EmuCfg::THREADS, EmuCfg::SMEM_BYTES, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_ue5m3(const GemmJob& j, cudaStream_t st) {
+    if (j.out_fp32) return run_emu<true>(j, st);
+    return run_emu<false>(j, st);
+}
+
+}  // namespace fp4bs

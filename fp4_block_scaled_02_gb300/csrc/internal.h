@@ -1,0 +1,85 @@
+// internal.h -- host-side interface between the C-ABI layer (api.cu) and the
+// kernel translation units (quantize.cu, gemm_nvfp4.cu, gemm_ue5m3.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fp4bs.h"
+
+namespace fp4bs {
+
+// One quantizer launch, after validation. Operand shape is rows x cols of the
+// INPUT; `colwise` makes the operand its transpose.
+struct QuantJob {
+    int scale_fmt;      // kFmtE4M3 / kFmtUE5M3 / kFmtUE8M0
+    int block;          // FP4_BLOCK_*
+    int sr;             // stochastic rounding
+    int colwise;
+    int rht;
+    int held;           // held-amax tensor scale
+    int refresh;        // held: this step refreshes the amax
+    float target_T;
+    uint32_t tensor_id;
+    uint64_t seed;
+    uint64_t step;
+    const uint16_t* in;
+    int64_t rows, cols;
+    // primary output (the operand) and, for 16x16, the optional transposed one
+    uint8_t* codes;
+    uint8_t* scales;
+    float* s_dec;
+    int layout;         // FP4_LAYOUT_*
+    uint8_t* codes_t;
+    uint8_t* scales_t;
+    float* s_dec_t;
+    int layout_t;
+    fp4_amax_state_t* state;
+    uint64_t* counters;  // nullable
+    float* partials;     // amax-pass workspace
+    int* status;         // device status word
+};
+
+// Largest number of amax partials (one per CTA of the amax pass).
+constexpr int kMaxAmaxPartials = 2048;
+
+int num_sms();
+cudaError_t launch_quantize(const QuantJob& job, cudaStream_t stream);
+// Number of amax partials the amax pass of `job` writes (0: no amax pass).
+int amax_partials_needed(const QuantJob& job);
+
+struct DequantJob {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* s_dec;
+    int64_t rows, cols;
+    int scale_fmt, block_k, layout;
+    void* out;
+    int out_fp32;
+};
+cudaError_t launch_dequantize(const DequantJob& job, cudaStream_t stream);
+
+// Block-scaled GEMM D = alpha * A * B^T over K-major quantized operands.
+struct GemmJob {
+    const uint8_t* a_codes;
+    const uint8_t* a_scales;
+    const float* a_sdec;
+    const uint8_t* b_codes;
+    const uint8_t* b_scales;
+    const float* b_sdec;
+    int64_t M, N, K;
+    int scale_fmt;
+    void* d;
+    int out_fp32;
+    int accumulate;
+    int* status;
+};
+cudaError_t launch_gemm_nvfp4(const GemmJob& job, cudaStream_t stream);
+cudaError_t launch_gemm_ue5m3(const GemmJob& job, cudaStream_t stream);
+
+// 2-D byte-matrix TMA descriptor with 128-byte rows per box row and 128-byte
+// swizzling (defined in gemm_nvfp4.cu).
+bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows);
+
+}  // namespace fp4bs

@@ -1,0 +1,689 @@
+// quantize.cu -- memory-bound quantizer kernels for sm_103a.
+//
+// Implements the quantization of "Pretraining Large Language Models with NVFP4"
+// (arXiv 2509.25149): tensor amax and tensor scale (App. B.1), block scale
+// (App. B.2), E2M1 conversion with RNE or stochastic rounding (App. B.3,
+// section 4.4), the 16-point random Hadamard transform on Wgrad operands
+// (section 4.2, App. C), 2D 16x16 weight scaling (section 4.3) and MXFP4 1x32
+// power-of-two scales (section A3, App. B.4); plus the UE5M3 block scales and
+// held-amax tensor scaling of the UE5M3 pretraining paper (arXiv 2609.02846).
+//
+// Data movement: 128-bit coalesced BF16 loads; each thread owns whole 16-element
+// blocks (rowwise: 16 consecutive elements; colwise: 16 tokens of 8 channels),
+// so block amax, scale and rounding stay in registers. Codes are stored as
+// packed 64-bit nibble words; groups of four lanes whose scales are adjacent in
+// the tensor-core layout merge them into one 32-bit store. Every kernel is a
+// grid-stride loop over a grid of a few CTAs per SM.
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "fp4_device.cuh"
+#include "internal.h"
+
+namespace fp4bs {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+struct QParams {
+    const uint16_t* in;
+    int64_t rows, cols;
+    uint8_t* codes;
+    uint8_t* scales;
+    float* s_dec;
+    uint8_t* codes_t;
+    uint8_t* scales_t;
+    float* s_dec_t;
+    fp4_amax_state_t* state;
+    uint64_t* counters;
+    const float* partials;
+    int npartials;
+    int held, refresh;
+    float target_T;
+    uint32_t tensor_id, step_lo, key0, key1;
+    uint64_t step;
+    int* status;
+};
+
+__device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+// Block-wide max of a non-negative float (all threads of the CTA call it).
+__device__ float cta_max(float v) {
+    __shared__ float red[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) m = fmaxf(m, red[i]);
+    __syncthreads();
+    return m;
+}
+
+// Tensor scale of this call (App. B.1; held amax per the UE5M3 paper), computed
+// redundantly by every CTA from the amax partials or the held state. CTA 0
+// publishes s_dec,G and, on refresh steps, the new held state. Returns false
+// (uniformly over the CTA) when a held state is needed but invalid.
+__device__ bool cta_tensor_scale(const QParams& q, float& s_enc, float& s_dec) {
+    __shared__ float s_amax;
+    __shared__ int s_ok;
+    if (q.held && !q.refresh) {
+        if (threadIdx.x == 0) {
+            s_ok = q.state->valid;
+            s_amax = q.state->amax_held;
+        }
+        __syncthreads();
+        if (!s_ok) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) record_status(q.status, kStatusState);
+            return false;
+        }
+    } else {
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < q.npartials; i += blockDim.x) m = fmaxf(m, q.partials[i]);
+        m = cta_max(m);
+        if (threadIdx.x == 0) s_amax = m;
+        __syncthreads();
+    }
+    const float amax = s_amax;
+    s_enc = global_encode_scale(amax, q.target_T);
+    s_dec = __fdiv_rn(1.0f, s_enc);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (q.s_dec) *q.s_dec = s_dec;
+        if (q.s_dec_t) *q.s_dec_t = s_dec;
+        if (q.held && q.refresh) {
+            q.state->amax_held = amax;
+            q.state->valid = 1;
+            q.state->last_refresh_step = q.step;
+        }
+    }
+    return true;
+}
+
+// Sum the four per-thread event counts over the warp and add them to the
+// caller's 64-bit counters.
+__device__ __forceinline__ void flush_counters(uint64_t* counters, uint32_t c0, uint32_t c1, uint32_t c2,
+                                               uint32_t c3) {
+    if (counters == nullptr) return;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        c0 += __shfl_xor_sync(0xFFFFFFFFu, c0, o);
+        c1 += __shfl_xor_sync(0xFFFFFFFFu, c1, o);
+        c2 += __shfl_xor_sync(0xFFFFFFFFu, c2, o);
+        c3 += __shfl_xor_sync(0xFFFFFFFFu, c3, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (c0) atomicAdd((unsigned long long*)&counters[0], (unsigned long long)c0);
+        if (c1) atomicAdd((unsigned long long*)&counters[1], (unsigned long long)c1);
+        if (c2) atomicAdd((unsigned long long*)&counters[2], (unsigned long long)c2);
+        if (c3) atomicAdd((unsigned long long*)&counters[3], (unsigned long long)c3);
+    }
+}
+
+struct Counts {
+    uint32_t esat = 0, eunder = 0, ssat = 0, sunder = 0;
+};
+
+// Quantize one 1x16 block held in v[16] (App. B.2-B.3): block amax, scale in
+// the block format (RNE, satfinite), local encode scale, E2M1 codes packed into
+// two 32-bit words (element i in nibble i). `g0` is the SR group of element 0.
+template <int FMT, bool SR>
+__device__ __forceinline__ uint32_t quantize_block16(const float v[16], float s_enc, float s_dec, uint64_t g0,
+                                                     const QParams& q, uint32_t& lo, uint32_t& hi, Counts& cnt,
+                                                     bool count_scale) {
+    using F = ScaleFmt<FMT>;
+    float amax_b = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(v[i]));
+    const float s = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const uint32_t sc = F::encode(s);
+    if (count_scale) cnt.ssat += s > F::kMax ? 1u : 0u;
+    lo = hi = 0u;
+    if (sc == 0u) {
+        if (count_scale) cnt.sunder += amax_b > 0.0f ? 1u : 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t code = (__float_as_uint(v[i]) >> 28) & 8u;
+            cnt.eunder += v[i] != 0.0f ? 1u : 0u;
+            if (i < 8) lo |= code << (4 * i);
+            else hi |= code << (4 * (i - 8));
+        }
+        return 0u;
+    }
+    const float s_enc_l = __fdiv_rn(1.0f, __fmul_rn(F::decode(sc), s_dec));
+    uint4 r0 = make_uint4(0, 0, 0, 0), r1 = make_uint4(0, 0, 0, 0);
+    if (SR) {
+        r0 = sr_group_bits(g0, q.tensor_id, q.step_lo, q.key0, q.key1);
+        r1 = sr_group_bits(g0 + 1, q.tensor_id, q.step_lo, q.key0, q.key1);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float val = __fmul_rn(v[i], s_enc_l);
+        cnt.esat += e2m1_saturates(val);
+        uint32_t code;
+        if (SR) code = e2m1_sr(val, sr_half(i < 8 ? r0 : r1, i & 7));
+        else code = e2m1_rne(val);
+        cnt.eunder += (v[i] != 0.0f && (code & 7u) == 0u) ? 1u : 0u;
+        if (i < 8) lo |= code << (4 * i);
+        else hi |= code << (4 * (i - 8));
+    }
+    return sc;
+}
+
+// ----------------------------------------------------------------------------
+// K1: tensor amax partials (App. B.1: one extra pass over the tensor).
+
+// Plain amax over all elements: max of |bf16| as 16-bit integers (BF16 bit
+// patterns of non-negative values order like their values).
+__global__ void __launch_bounds__(kThreads) amax_plain_kernel(const uint4* __restrict__ in, int64_t n_vec,
+                                                              float* __restrict__ partials) {
+    uint32_t m = 0u;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n_vec; i += 4 * stride) {
+        uint4 a = __ldg(in + i), b = __ldg(in + i + stride), c = __ldg(in + i + 2 * stride),
+              d = __ldg(in + i + 3 * stride);
+        m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                 __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+        m = __vmaxu2(m, __vmaxu2(__vmaxu2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
+                                 __vmaxu2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
+        m = __vmaxu2(m, __vmaxu2(__vmaxu2(c.x & 0x7FFF7FFFu, c.y & 0x7FFF7FFFu),
+                                 __vmaxu2(c.z & 0x7FFF7FFFu, c.w & 0x7FFF7FFFu)));
+        m = __vmaxu2(m, __vmaxu2(__vmaxu2(d.x & 0x7FFF7FFFu, d.y & 0x7FFF7FFFu),
+                                 __vmaxu2(d.z & 0x7FFF7FFFu, d.w & 0x7FFF7FFFu)));
+    }
+    for (; i < n_vec; i += stride) {
+        uint4 a = __ldg(in + i);
+        m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                 __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+    }
+    const uint32_t mm = max(m & 0xFFFFu, m >> 16);
+    const float f = cta_max(__uint_as_float(mm << 16));
+    if (threadIdx.x == 0) partials[blockIdx.x] = f;
+}
+
+// amax in the rotated space (App. C): each thread transforms 16 tokens of 8
+// channels (sixteen 128-bit loads) and keeps the max magnitude.
+__global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ in, int64_t T,
+                                                                 int64_t C, uint32_t key0, uint32_t key1,
+                                                                 float* __restrict__ partials) {
+    const uint32_t signs = rht_sign_word(key0, key1);
+    const int64_t ug = C / 8, uj = T / 16, units = ug * uj;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float m = 0.0f;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const int64_t g = u % ug, j = u / ug;
+        uint4 x[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) x[t] = ldg16(in + (16 * j + t) * C + 8 * g);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            float v[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const uint32_t w = ch < 2 ? x[t].x : ch < 4 ? x[t].y : ch < 6 ? x[t].z : x[t].w;
+                v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
+            }
+            rht16(v, signs);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) m = fmaxf(m, fabsf(v[t]));
+        }
+    }
+    m = cta_max(m);
+    if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+// ----------------------------------------------------------------------------
+// K2: rowwise 1x16 quantizer (activations X for Fprop, gradients dY for Dgrad).
+// Flat block index b covers rows x cols/16; block b's elements are the 16
+// consecutive inputs at 16 b, its codes the 8 bytes at 8 b.
+template <int FMT, bool SR, bool TCL>
+__global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
+    float s_enc, s_dec;
+    if (!cta_tensor_scale(q, s_enc, s_dec)) return;
+    const int64_t nb_row = q.cols / 16;
+    const int64_t nblk = q.rows * nb_row;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    Counts cnt;
+    for (int64_t base = warp * 32; base < nblk; base += nwarps * 32) {
+        const int64_t b = base + lane;
+        const bool active = b < nblk;
+        uint32_t sc = 0u;
+        if (active) {
+            const uint4 a = ldg16(q.in + 16 * b), c = ldg16(q.in + 16 * b + 8);
+            float v[16];
+            unpack16(a, c, v);
+            uint32_t lo, hi;
+            sc = quantize_block16<FMT, SR>(v, s_enc, s_dec, (uint64_t)(2 * b), q, lo, hi, cnt, true);
+            *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
+        }
+        if (TCL) {
+            // lanes 4k..4k+3 hold the four adjacent scale bytes of one row
+            uint32_t w = sc << (8 * (lane & 3));
+            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+            if (active && (lane & 3) == 0) {
+                const int64_t r = b / nb_row, j = b % nb_row;
+                *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(r, j, nb_row)) = w;
+            }
+        } else if (active) {
+            q.scales[b] = (uint8_t)sc;
+        }
+    }
+    flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
+}
+
+// ----------------------------------------------------------------------------
+// K3: colwise 1x16 quantizer with optional fused RHT16 (Wgrad operands X^T and
+// dY^T, section 4.2-4.3). The operand is the input's transpose: operand row c
+// (a channel) holds tokens along the dot dimension. A warp covers 4 token tiles
+// x 8 channel groups (64 tokens x 64 channels): lane = 4 * channel_group + tile,
+// so the four lanes of a channel group write 32 contiguous code bytes and four
+// adjacent scale bytes.
+template <int FMT, bool SR, bool RHT, bool TCL>
+__global__ void __launch_bounds__(kThreads) quantize_cols_kernel(QParams q) {
+    float s_enc, s_dec;
+    if (!cta_tensor_scale(q, s_enc, s_dec)) return;
+    const int64_t T = q.rows, C = q.cols;
+    const int64_t ug = C / 8, uj = T / 16;
+    const int64_t wg_count = (ug + 7) / 8, wj_count = (uj + 3) / 4;
+    const int64_t wunits = wg_count * wj_count;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const uint32_t signs = RHT ? rht_sign_word(q.key0, q.key1) : 0u;
+    Counts cnt;
+    for (int64_t wu = warp; wu < wunits; wu += nwarps) {
+        const int64_t g = (wu % wg_count) * 8 + (lane >> 2);
+        const int64_t j = (wu / wg_count) * 4 + (lane & 3);
+        const bool active = g < ug && j < uj;
+        uint4 x[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            x[t] = active ? ldg16(q.in + (16 * j + t) * C + 8 * g) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            float v[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const uint32_t w = ch < 2 ? x[t].x : ch < 4 ? x[t].y : ch < 6 ? x[t].z : x[t].w;
+                v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
+            }
+            if (RHT) rht16(v, signs);
+            const int64_t c = 8 * g + ch;
+            uint32_t lo = 0u, hi = 0u, sc = 0u;
+            if (active) {
+                sc = quantize_block16<FMT, SR>(v, s_enc, s_dec, (uint64_t)((c * T + 16 * j) >> 3), q, lo, hi, cnt,
+                                              true);
+                *reinterpret_cast<uint2*>(q.codes + c * (T / 2) + 8 * j) = make_uint2(lo, hi);
+            }
+            if (TCL) {
+                uint32_t w = sc << (8 * (lane & 3));
+                w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+                w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+                if (active && (lane & 3) == 0)
+                    *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(c, j, uj)) = w;
+            } else if (active) {
+                q.scales[c * uj + j] = (uint8_t)sc;
+            }
+        }
+    }
+    flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
+}
+
+// ----------------------------------------------------------------------------
+// K4: 2D 16x16 weight quantizer (section 4.3). A half-warp owns one 16x16 tile
+// of W [N x K]: lane i loads row i, the tile amax is a 16-lane shuffle max, and
+// each lane converts its row. The transposed operand W^T [K x N] reuses the same
+// codes: lane i gathers column i from the other lanes' packed rows, so
+// quantize(W)^T == quantize(W^T) holds by construction. Either output may be
+// omitted (null codes pointer).
+template <int FMT, bool TCL_W, bool TCL_WT>
+__global__ void __launch_bounds__(kThreads) quantize_2d_kernel(QParams q) {
+    float s_enc, s_dec;
+    if (!cta_tensor_scale(q, s_enc, s_dec)) return;
+    using F = ScaleFmt<FMT>;
+    const int64_t N = q.rows, K = q.cols, tn_count = N / 16, tk_count = K / 16;
+    const int64_t tiles = tn_count * tk_count;
+    const int lane = threadIdx.x & 31, i = lane & 15;
+    const int64_t hw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+    const int64_t nhw = ((int64_t)gridDim.x * blockDim.x) >> 4;
+    Counts cnt;
+    // loop bound rounded to whole warps so every shuffle has its full warp
+    for (int64_t base = hw & ~(int64_t)1; base < tiles; base += nhw) {
+        const int64_t t = base + (lane >> 4);
+        const bool active = t < tiles;
+        const int64_t tk = active ? t % tk_count : 0, tn = active ? t / tk_count : 0;
+        const int64_t n = 16 * tn + i, k0 = 16 * tk;
+        float v[16];
+        if (active) {
+            const uint4 a = ldg16(q.in + n * K + k0), c = ldg16(q.in + n * K + k0 + 8);
+            unpack16(a, c, v);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.0f;
+        }
+        float amax_t = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) amax_t = fmaxf(amax_t, fabsf(v[e]));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax_t = fmaxf(amax_t, __shfl_xor_sync(0xFFFFFFFFu, amax_t, o));
+        const float s = __fmul_rn(__fdiv_rn(amax_t, 6.0f), s_enc);
+        const uint32_t sc = F::encode(s);
+        const bool count_tile = active && i == 0;
+        if (count_tile) {
+            cnt.ssat += s > F::kMax ? 1u : 0u;
+            cnt.sunder += (sc == 0u && amax_t > 0.0f) ? 1u : 0u;
+        }
+        uint32_t lo = 0u, hi = 0u;
+        if (sc == 0u) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const uint32_t code = (__float_as_uint(v[e]) >> 28) & 8u;
+                if (active) cnt.eunder += v[e] != 0.0f ? 1u : 0u;
+                if (e < 8) lo |= code << (4 * e);
+                else hi |= code << (4 * (e - 8));
+            }
+        } else {
+            const float s_enc_l = __fdiv_rn(1.0f, __fmul_rn(F::decode(sc), s_dec));
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float val = __fmul_rn(v[e], s_enc_l);
+                const uint32_t code = e2m1_rne(val);
+                if (active) {
+                    cnt.esat += e2m1_saturates(val);
+                    cnt.eunder += (v[e] != 0.0f && (code & 7u) == 0u) ? 1u : 0u;
+                }
+                if (e < 8) lo |= code << (4 * e);
+                else hi |= code << (4 * (e - 8));
+            }
+        }
+        if (q.codes != nullptr && active) {
+            *reinterpret_cast<uint2*>(q.codes + n * (K / 2) + k0 / 2) = make_uint2(lo, hi);
+            q.scales[TCL_W ? tc_scale_offset(n, tk, tk_count) : n * tk_count + tk] = (uint8_t)sc;
+        }
+        if (q.codes_t != nullptr) {
+            // column i of the tile: nibble i of every row rr
+            uint32_t tlo = 0u, thi = 0u;
+            const int src_base = lane & 16;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const uint32_t wlo = __shfl_sync(0xFFFFFFFFu, lo, src_base + rr);
+                const uint32_t whi = __shfl_sync(0xFFFFFFFFu, hi, src_base + rr);
+                const uint32_t nib = (i < 8 ? (wlo >> (4 * i)) : (whi >> (4 * (i - 8)))) & 0xFu;
+                if (rr < 8) tlo |= nib << (4 * rr);
+                else thi |= nib << (4 * (rr - 8));
+            }
+            if (active) {
+                const int64_t kr = k0 + i;
+                *reinterpret_cast<uint2*>(q.codes_t + kr * (N / 2) + 8 * tn) = make_uint2(tlo, thi);
+                q.scales_t[TCL_WT ? tc_scale_offset(kr, tn, tn_count) : kr * tn_count + tn] = (uint8_t)sc;
+            }
+        }
+    }
+    flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
+}
+
+// ----------------------------------------------------------------------------
+// K5: MXFP4 1x32 rowwise quantizer (section A3, App. B.4): UE8M0 scale = the
+// power of two that rounds amax_B / 6 up, value scaled by 2^-e exactly, RNE.
+template <bool TCL>
+__global__ void __launch_bounds__(kThreads) quantize_mx_rows_kernel(QParams q) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (q.s_dec) *q.s_dec = 1.0f;
+    }
+    const int64_t nb_row = q.cols / 32, nblk = q.rows * nb_row;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    Counts cnt;
+    for (int64_t base = warp * 32; base < nblk; base += nwarps * 32) {
+        const int64_t b = base + lane;
+        const bool active = b < nblk;
+        uint32_t sc = 0u;
+        if (active) {
+            float v[32];
+            unpack16(ldg16(q.in + 32 * b), ldg16(q.in + 32 * b + 8), v);
+            unpack16(ldg16(q.in + 32 * b + 16), ldg16(q.in + 32 * b + 24), v + 16);
+            float amax_b = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) amax_b = fmaxf(amax_b, fabsf(v[e]));
+            int ex = ue8m0_exponent(amax_b);
+            if (ex > 127) {
+                ex = 127;
+                cnt.ssat++;
+            }
+            if (ex < -127) {
+                ex = -127;
+                if (amax_b > 0.0f) cnt.sunder++;
+            }
+            sc = (uint32_t)(ex + 127);
+            const float inv = exp2_exact(-ex);
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float val = __fmul_rn(v[e], inv);
+                const uint32_t code = e2m1_rne(val);
+                cnt.esat += e2m1_saturates(val);
+                cnt.eunder += (v[e] != 0.0f && (code & 7u) == 0u) ? 1u : 0u;
+                w[e >> 3] |= code << (4 * (e & 7));
+            }
+            *reinterpret_cast<uint4*>(q.codes + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (TCL) {
+            uint32_t w = sc << (8 * (lane & 3));
+            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+            if (active && (lane & 3) == 0) {
+                const int64_t r = b / nb_row, j = b % nb_row;
+                *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(r, j, nb_row)) = w;
+            }
+        } else if (active) {
+            q.scales[b] = (uint8_t)sc;
+        }
+    }
+    flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
+}
+
+// ----------------------------------------------------------------------------
+// K6: dequantize (section A3: decode back to the original range; App. B.3):
+// x = RN(RN(e2m1 * s_hat) * s_dec,G) in FP32, stored as BF16 (RNE) or FP32.
+template <int FMT, int BS, bool TCL, bool OUT32>
+__global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
+                                                              const uint8_t* __restrict__ scales,
+                                                              const float* __restrict__ s_dec_p, int64_t rows,
+                                                              int64_t cols, void* __restrict__ out) {
+    const float s_dec = *s_dec_p;
+    const int64_t nb_row = cols / BS, nblk = rows * nb_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride) {
+        const int64_t r = b / nb_row, j = b % nb_row;
+        const uint32_t sc = scales[TCL ? tc_scale_offset(r, j, nb_row) : b];
+        float s_hat;
+        if constexpr (FMT == kFmtUE8M0) s_hat = exp2_exact((int)sc - 127);
+        else s_hat = ScaleFmt<FMT>::decode(sc);
+        uint32_t w[BS / 8];
+#pragma unroll
+        for (int k = 0; k < BS / 8; ++k) w[k] = reinterpret_cast<const uint32_t*>(codes + (BS / 2) * b)[k];
+#pragma unroll
+        for (int e = 0; e < BS; e += 8) {
+            float o[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t code = (w[e >> 3] >> (4 * k)) & 0xFu;
+                const uint32_t m = code & 7u;
+                const float mag = m <= 4u ? 0.5f * (float)m : (m == 5u ? 3.0f : (m == 6u ? 4.0f : 6.0f));
+                const float val = (code & 8u) ? -mag : mag;
+                o[k] = __fmul_rn(__fmul_rn(val, s_hat), s_dec);
+            }
+            if (OUT32) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + BS * b + e);
+                dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+            } else {
+                uint32_t p[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * k], o[2 * k + 1]);
+                    p[k] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + BS * b + e) = make_uint4(p[0], p[1], p[2], p[3]);
+            }
+        }
+    }
+}
+
+int grid_for(int64_t threads_wanted, int per_sm) {
+    const int64_t want = (threads_wanted + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    int64_t g = want < cap ? want : cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
+    const bool tcl = j.layout == FP4_LAYOUT_TCGEN05;
+    if (j.block == FP4_BLOCK_16x16) {
+        const int64_t tiles = (j.rows / 16) * (j.cols / 16);
+        const int grid = grid_for(tiles * 16, 8);
+        // the kernel's primary output is W (rowwise); for COLWISE the operand is
+        // W^T, which the kernel writes through its transposed output
+        QParams p = q;
+        int lw, lwt;
+        if (j.colwise) {
+            p.codes = j.codes_t;
+            p.scales = j.scales_t;
+            p.s_dec = j.s_dec_t;
+            p.codes_t = j.codes;
+            p.scales_t = j.scales;
+            p.s_dec_t = j.s_dec;
+            lw = j.layout_t;
+            lwt = j.layout;
+        } else {
+            lw = j.layout;
+            lwt = j.layout_t;
+        }
+        const bool a = lw == FP4_LAYOUT_TCGEN05, b = lwt == FP4_LAYOUT_TCGEN05;
+        if (a && b) quantize_2d_kernel<FMT, true, true><<<grid, kThreads, 0, st>>>(p);
+        else if (a) quantize_2d_kernel<FMT, true, false><<<grid, kThreads, 0, st>>>(p);
+        else if (b) quantize_2d_kernel<FMT, false, true><<<grid, kThreads, 0, st>>>(p);
+        else quantize_2d_kernel<FMT, false, false><<<grid, kThreads, 0, st>>>(p);
+        return cudaGetLastError();
+    }
+    if (!j.colwise) {
+        const int grid = grid_for(j.rows * (j.cols / 16), 8);
+        if (j.sr) {
+            if (tcl) quantize_rows_kernel<FMT, true, true><<<grid, kThreads, 0, st>>>(q);
+            else quantize_rows_kernel<FMT, true, false><<<grid, kThreads, 0, st>>>(q);
+        } else {
+            if (tcl) quantize_rows_kernel<FMT, false, true><<<grid, kThreads, 0, st>>>(q);
+            else quantize_rows_kernel<FMT, false, false><<<grid, kThreads, 0, st>>>(q);
+        }
+        return cudaGetLastError();
+    }
+    const int64_t wunits = ((j.cols / 8 + 7) / 8) * ((j.rows / 16 + 3) / 4);
+    const int grid = grid_for(wunits * 32, 4);
+#define FP4_COLS(SR, RHT, TCL) quantize_cols_kernel<FMT, SR, RHT, TCL><<<grid, kThreads, 0, st>>>(q)
+    if (j.sr) {
+        if (j.rht) { if (tcl) FP4_COLS(true, true, true); else FP4_COLS(true, true, false); }
+        else { if (tcl) FP4_COLS(true, false, true); else FP4_COLS(true, false, false); }
+    } else {
+        if (j.rht) { if (tcl) FP4_COLS(false, true, true); else FP4_COLS(false, true, false); }
+        else { if (tcl) FP4_COLS(false, false, true); else FP4_COLS(false, false, false); }
+    }
+#undef FP4_COLS
+    return cudaGetLastError();
+}
+
+int amax_grid(const QuantJob& j) {
+    if (j.rht) {
+        const int64_t units = (j.cols / 8) * (j.rows / 16);
+        int g = grid_for(units, 4);
+        return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
+    }
+    const int64_t nvec = j.rows * j.cols / 8;
+    int g = grid_for((nvec + 3) / 4, 8);
+    return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
+}
+
+}  // namespace
+
+int amax_partials_needed(const QuantJob& j) {
+    if (j.scale_fmt == kFmtUE8M0) return 0;
+    if (j.held && !j.refresh) return 0;
+    if (j.rows == 0 || j.cols == 0) return 0;
+    return amax_grid(j);
+}
+
+cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
+    QParams q{};
+    q.in = j.in;
+    q.rows = j.rows;
+    q.cols = j.cols;
+    q.codes = j.codes;
+    q.scales = j.scales;
+    q.s_dec = j.s_dec;
+    q.codes_t = j.codes_t;
+    q.scales_t = j.scales_t;
+    q.s_dec_t = j.s_dec_t;
+    q.state = j.state;
+    q.counters = j.counters;
+    q.partials = j.partials;
+    q.held = j.held;
+    q.refresh = j.refresh;
+    q.target_T = j.target_T;
+    q.tensor_id = j.tensor_id;
+    q.step = j.step;
+    q.step_lo = (uint32_t)j.step;
+    q.key0 = (uint32_t)j.seed;
+    q.key1 = (uint32_t)(j.seed >> 32);
+    q.status = j.status;
+    if (j.rows == 0 || j.cols == 0) return cudaSuccess;
+
+    if (j.scale_fmt == kFmtUE8M0) {
+        const int grid = grid_for(j.rows * (j.cols / 32), 8);
+        if (j.layout == FP4_LAYOUT_TCGEN05) quantize_mx_rows_kernel<true><<<grid, kThreads, 0, st>>>(q);
+        else quantize_mx_rows_kernel<false><<<grid, kThreads, 0, st>>>(q);
+        return cudaGetLastError();
+    }
+    // pass 1 (current scaling, or a held-amax refresh step): amax partials
+    const int np = amax_partials_needed(j);
+    q.npartials = np;
+    if (np > 0) {
+        if (j.rht) amax_rht_cols_kernel<<<np, kThreads, 0, st>>>(j.in, j.rows, j.cols, q.key0, q.key1, j.partials);
+        else amax_plain_kernel<<<np, kThreads, 0, st>>>(reinterpret_cast<const uint4*>(j.in), j.rows * j.cols / 8,
+                                                         j.partials);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // pass 2: scale and convert
+    if (j.scale_fmt == kFmtE4M3) return launch_fmt<kFmtE4M3>(j, q, st);
+    return launch_fmt<kFmtUE5M3>(j, q, st);
+}
+
+cudaError_t launch_dequantize(const DequantJob& j, cudaStream_t st) {
+    if (j.rows == 0 || j.cols == 0) return cudaSuccess;
+    const int grid = grid_for(j.rows * (j.cols / j.block_k), 8);
+    const bool tcl = j.layout == FP4_LAYOUT_TCGEN05;
+#define FP4_DQ(FMT, BS)                                                                                           \
+    do {                                                                                                          \
+        if (tcl) {                                                                                                \
+            if (j.out_fp32) dequantize_kernel<FMT, BS, true, true><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            else dequantize_kernel<FMT, BS, true, false><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+        } else {                                                                                                  \
+            if (j.out_fp32) dequantize_kernel<FMT, BS, false, true><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            else dequantize_kernel<FMT, BS, false, false><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+        }                                                                                                         \
+    } while (0)
+    if (j.scale_fmt == kFmtE4M3) FP4_DQ(kFmtE4M3, 16);
+    else if (j.scale_fmt == kFmtUE5M3) FP4_DQ(kFmtUE5M3, 16);
+    else FP4_DQ(kFmtUE8M0, 32);
+#undef FP4_DQ
+    return cudaGetLastError();
+}
+
+}  // namespace fp4bs

@@ -1,0 +1,192 @@
+/*
+ * fp4bs.h -- C ABI of the GB300 FP4 block-scaled quantized linear library
+ * (libfp4bs.so, sm_103a).
+ *
+ * The library implements the data-parallel hot path of FP4 pretraining as
+ * "Pretraining Large Language Models with NVFP4" (arXiv 2509.25149) and the
+ * UE5M3 block-scale paper summarised at arXiv 2609.02846 describe it:
+ *   - a quantizer: tensor amax -> FP32 tensor scale (App. B.1; or a held amax
+ *     refreshed every N steps), per-block scale (App. B.2) in E4M3, UE5M3 or
+ *     UE8M0, E2M1 conversion with round-to-nearest-even or stochastic rounding
+ *     (App. B.3, section 4.4), optional 16x16 random Hadamard transform on the
+ *     Wgrad operands (section 4.2, App. C), 2D 16x16 weight scaling (4.3);
+ *   - the three block-scaled FP4 GEMMs of a linear layer (section 4.1, Fig. 5:
+ *     Fprop, Dgrad, Wgrad) on tcgen05 tensor cores (App. B.3), and a
+ *     software-emulated path for UE5M3 scales, which have no hardware support.
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller allocates and frees every buffer (inputs, codes,
+ *     scales, tensor scales, counters, held-amax state, workspace, outputs).
+ *     The library never allocates device memory. Pointers are DEVICE pointers
+ *     unless stated otherwise and must be 16-byte aligned.
+ *   - Execution: work is enqueued on the given CUDA stream (a cudaStream_t
+ *     passed as void*; NULL = legacy default stream) and the call returns before
+ *     it completes. Argument checks run synchronously on the host first: a call
+ *     that fails them returns an error and enqueues nothing.
+ *   - Device-side errors (a bounded wait that timed out, a held-amax state that
+ *     was never refreshed) are recorded in a per-device status word read by
+ *     fp4_device_status().
+ *   - Shapes: an operand is `rows x cols` with `cols` the dot-product dimension
+ *     (K-major); BF16 inputs are row-major with leading dimension = cols.
+ */
+#ifndef FP4BS_H
+#define FP4BS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP4_OK = 0,
+    FP4_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, inconsistent options */
+    FP4_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination */
+    FP4_ERR_SHAPE = 3,         /* dimension not a multiple the path needs */
+    FP4_ERR_ALIGNMENT = 4,     /* pointer not 16-byte aligned */
+    FP4_ERR_STATE = 5,         /* held-amax state invalid on a non-refresh step */
+    FP4_ERR_CUDA = 6,          /* a CUDA runtime call failed */
+    FP4_ERR_DEVICE_TIMEOUT = 7,/* a bounded device-side wait gave up */
+    FP4_ERR_WORKSPACE = 8      /* workspace missing or too small */
+} fp4_status_t;
+
+/* Block-scale formats.
+ *   E4M3  : NVFP4 (App. B.1-B.2): OCP E4M3, max 448, one FP32 tensor scale.
+ *   UE5M3 : unsigned E5M3, bias 15, max 114688 (0xFE; 0xFF reserved), with a
+ *           current or held tensor scale (UE5M3 page, method details).
+ *   UE8M0 : MXFP4 (section A3): power of two 2^(code-127), no tensor scale. */
+typedef enum { FP4_SCALE_E4M3 = 0, FP4_SCALE_UE5M3 = 1, FP4_SCALE_UE8M0 = 2 } fp4_scale_fmt_t;
+
+/* Block shapes: 1x16 along the dot dimension (activations, gradients),
+ * 16x16 (weights, section 4.3), 1x32 (MXFP4, section A3). */
+typedef enum { FP4_BLOCK_1x16 = 0, FP4_BLOCK_16x16 = 1, FP4_BLOCK_1x32 = 2 } fp4_block_t;
+
+typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_round_t;
+
+/* Tensor scale: per-call amax (App. B.1) or held amax refreshed when
+ * step % refresh_every == 0 (UE5M3 page: refresh every 50 steps). */
+typedef enum { FP4_TSCALE_CURRENT = 0, FP4_TSCALE_HELD = 1 } fp4_tscale_t;
+
+/* ROWWISE: the operand is the input itself (blocks run along its columns).
+ * COLWISE: the operand is the input's transpose (blocks run along the input's
+ * rows); this is how Wgrad consumes X and dY (section 4.3). */
+typedef enum { FP4_ORIENT_ROWWISE = 0, FP4_ORIENT_COLWISE = 1 } fp4_orient_t;
+
+/* Scale storage. PLAIN: row-major rows x (cols / block) bytes. TCGEN05: the
+ * tensor-core scale-factor layout; rows must be a multiple of 128 and
+ * cols / block a multiple of 4. Chunk (rt, kt) of 128 rows x 4 blocks is
+ * 512 bytes at offset 512 * (rt * (cols/block/4) + kt); row r, block j of a
+ * chunk is at byte 16 * (r % 32) + 4 * ((r % 128) / 32) + (j % 4). */
+typedef enum { FP4_LAYOUT_PLAIN = 0, FP4_LAYOUT_TCGEN05 = 1 } fp4_scale_layout_t;
+
+/* Quantizer options (all fields read by fp4_quantize). */
+typedef struct {
+    int32_t scale_fmt;       /* fp4_scale_fmt_t */
+    int32_t block;           /* fp4_block_t; UE8M0 <=> 1x32 */
+    int32_t round;           /* fp4_round_t; SR for gradients only (section 4.4) */
+    int32_t orient;          /* fp4_orient_t */
+    int32_t rht;             /* nonzero: 16-point RHT along the block dimension;
+                                COLWISE 1x16 only (section 4.2: Wgrad inputs) */
+    int32_t tscale;          /* fp4_tscale_t (ignored for UE8M0) */
+    float target_T;          /* scale target: 448 for E4M3; 448 or 2048 for UE5M3 */
+    uint32_t refresh_every;  /* held mode refresh period (50) */
+    uint32_t tensor_id;      /* keys the SR random stream; 0xFFFFFFFF is reserved */
+    int32_t scale_layout;    /* fp4_scale_layout_t for the outputs */
+    int32_t emit_transpose;  /* 16x16 only: also write the transposed operand */
+    int32_t reserved;        /* must be 0 */
+    uint64_t seed;           /* RNG seed: SR bits and the RHT sign vector */
+    uint64_t step;           /* training step: SR stream and held-amax refresh */
+} fp4_quant_params_t;
+
+/* A quantized operand: rows x cols E2M1 codes, K-major, element 2i of a row in
+ * the low nibble of byte i; block scales; and the FP32 decode tensor scale
+ * s_dec,G (App. B.1; 1.0 for UE8M0). */
+typedef struct {
+    uint8_t* codes;          /* rows * cols / 2 bytes */
+    uint8_t* scales;         /* rows * cols / block_k bytes */
+    float* s_dec_global;     /* one float */
+    int64_t rows;
+    int64_t cols;            /* dot-product dimension */
+    int32_t scale_fmt;       /* fp4_scale_fmt_t */
+    int32_t block_k;         /* 16 or 32: scale block length along cols */
+    int32_t scale_layout;    /* fp4_scale_layout_t */
+    int32_t reserved;        /* must be 0 */
+} fp4_tensor_t;
+
+/* Held-amax record of one tensor (device memory, 16 bytes, zero-initialised by
+ * the caller before first use). */
+typedef struct {
+    float amax_held;
+    int32_t valid;
+    uint64_t last_refresh_step;
+} fp4_amax_state_t;
+
+/* Sizes of the codes and scales buffers fp4_quantize writes for an input of
+ * rows x cols (for COLWISE the operand is cols x rows). Host only. */
+fp4_status_t fp4_quantized_sizes(const fp4_quant_params_t* p, int64_t rows, int64_t cols,
+                                 size_t* codes_bytes, size_t* scales_bytes);
+
+/* Device workspace bytes fp4_quantize needs (the per-CTA amax partials of the
+ * amax pass); 0 when no amax pass runs (UE8M0). Host only. */
+size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols);
+
+/* Quantize a row-major BF16 input `in_bf16` (rows x cols) into `out`
+ * ("Pretraining LLMs with NVFP4", App. B.1-B.3; sections 4.2-4.4).
+ *   out      : operand descriptor (rows/cols = operand shape, i.e. transposed
+ *              for COLWISE); codes, scales and s_dec_global are written.
+ *   out_t    : 16x16 with emit_transpose: the transposed operand (cols x rows)
+ *              with the same codes and scales transposed (section 4.3); else NULL.
+ *   state    : held-amax record (FP4_TSCALE_HELD), else NULL. On refresh steps it
+ *              is written; on other steps it must be valid (else the device status
+ *              becomes FP4_ERR_STATE and nothing is written).
+ *   counters : NULL or 4 device uint64: elem_sat, elem_underflow, scale_sat,
+ *              scale_underflow; the call ADDS its counts (the caller zeroes).
+ *   ws       : device workspace of fp4_workspace_bytes() bytes (any content).
+ * Shapes: block dimension a multiple of the block length; 16x16 needs both
+ * dimensions multiples of 16; TCGEN05 layout needs operand rows % 128 == 0 and
+ * operand cols % (4 * block) == 0. rows == 0 or cols == 0 is a no-op. */
+fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+                          const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
+                          uint64_t* counters, void* ws, size_t ws_bytes, void* stream);
+
+/* Decode an operand back to real values, x = e2m1 * s_hat * s_dec,G computed as
+ * RN(RN(e2m1 * s_hat) * s_dec,G) in FP32 (section A3; App. B.3), written as
+ * rows x cols BF16 (out_fp32 == 0) or FP32. */
+fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void* stream);
+
+/* Block-scaled GEMM D[M x N] = s_dec,G,A * s_dec,G,B * sum_k (a_mk s_A)(b_nk s_B)
+ * with FP32 accumulation ("Pretraining LLMs with NVFP4", App. B.3; A3 hardware
+ * support). A is M x K, B is N x K, both quantized, K-major, TCGEN05 scale
+ * layout, same scale format and block 16. E4M3 runs natively (tcgen05
+ * kind::mxf4nvf4); UE5M3 runs the software-emulated path (operands decoded to
+ * BF16 in shared memory, tcgen05 kind::f16). M and N must be multiples of 128
+ * and K of 256. Output row-major M x N: BF16 (out_fp32 == 0) or FP32; with
+ * accumulate != 0 (FP32 only) D is added to the existing output. */
+fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32,
+                      int accumulate, void* stream);
+
+/* The three GEMMs of a linear layer Y = X W^T (section 4.1, Fig. 5):
+ *   Fprop: Y[T x N]  = X[T x K]   . W[N x K]^T     (x rowwise, w 16x16), BF16 out
+ *   Dgrad: dX[T x K] = dY[T x N]  . Wt[K x N]^T    (dy rowwise, wt = W^T operand), BF16 out
+ *   Wgrad: dW[N x K] = dYt[N x T] . Xt[K x T]^T    (colwise + RHT operands), FP32 out
+ *          (weight gradients stay FP32, section 4.1); accumulate adds into dW. */
+fp4_status_t fp4_linear_fprop(const fp4_tensor_t* x, const fp4_tensor_t* w, void* y_bf16, void* stream);
+fp4_status_t fp4_linear_dgrad(const fp4_tensor_t* dy, const fp4_tensor_t* wt, void* dx_bf16, void* stream);
+fp4_status_t fp4_linear_wgrad(const fp4_tensor_t* dyt, const fp4_tensor_t* xt, float* dw_fp32,
+                              int accumulate, void* stream);
+
+/* Synchronise `stream`, then return and clear the current device's status word
+ * (FP4_OK when no device-side error was recorded). */
+fp4_status_t fp4_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* fp4_status_string(fp4_status_t s);
+
+/* Library ABI version (incremented on incompatible changes). */
+int fp4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP4BS_H */

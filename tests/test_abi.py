@@ -1,0 +1,76 @@
+"""The C-ABI library loads and exports every entry point include/fp4bs.h
+declares; host-side argument checks work without a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp4_block_scaled_02_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "fp4bs.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[A-Za-z_][\w\s\*]*?)\b(fp4_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "fp4_quantize" in names and "fp4_linear_wgrad" in names and len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    from fp4_block_scaled_02_gb300 import _lib
+    assert sorted(_lib.EXPORTED) == names
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fp4_abi_version() == 1
+    for s in range(9):
+        assert lib.fp4_status_string(s)
+    assert lib.fp4_status_string(0) == b"ok"
+
+
+def test_sizes_and_workspace_without_gpu(lib):
+    from fp4_block_scaled_02_gb300 import _lib as L
+    p = L.fp4_quant_params_t(0, 0, 0, 0, 0, 0, 448.0, 50, 0, 1, 0, 0, 0, 0)
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.fp4_quantized_sizes(ctypes.byref(p), 256, 512, ctypes.byref(c), ctypes.byref(s)) == 0
+    assert (c.value, s.value) == (256 * 256, 256 * 32)
+    p.orient = L.FP4_ORIENT_COLWISE
+    assert lib.fp4_quantized_sizes(ctypes.byref(p), 256, 512, ctypes.byref(c), ctypes.byref(s)) == 0
+    assert (c.value, s.value) == (512 * 128, 512 * 16)
+    assert lib.fp4_quantized_sizes(ctypes.byref(p), 250, 512, ctypes.byref(c), ctypes.byref(s)) == L.FP4_ERR_SHAPE
+    assert lib.fp4_workspace_bytes(ctypes.byref(p), 256, 512) >= 4
+    p.scale_fmt = L.FP4_SCALE_UE8M0
+    assert lib.fp4_workspace_bytes(ctypes.byref(p), 256, 512) == 0
+
+
+def test_argument_checks_return_before_any_launch(lib):
+    from fp4_block_scaled_02_gb300 import _lib as L
+    p = L.fp4_quant_params_t(0, 0, 0, 0, 0, 0, 448.0, 50, 0, 1, 0, 0, 0, 0)
+    t = L.fp4_tensor_t(16, 16, 16, 128, 64, 0, 16, 1, 0)
+    assert lib.fp4_quantize(None, None, 0, 0, None, None, None, None, None, 0, None) == L.FP4_ERR_INVALID_ARG
+    p.rht = 1   # RHT only with colwise 1x16
+    assert lib.fp4_quantize(ctypes.byref(p), ctypes.c_void_p(16), 128, 64, ctypes.byref(t), None, None, None,
+                            None, 0, None) == L.FP4_ERR_INVALID_ARG
+    p.rht = 0
+    p.tensor_id = 0xFFFFFFFF  # reserved
+    assert lib.fp4_quantize(ctypes.byref(p), ctypes.c_void_p(16), 128, 64, ctypes.byref(t), None, None, None,
+                            None, 0, None) == L.FP4_ERR_INVALID_ARG
+    p.tensor_id = 0
+    assert lib.fp4_quantize(ctypes.byref(p), ctypes.c_void_p(8), 128, 64, ctypes.byref(t), None, None, None,
+                            ctypes.c_void_p(16), 8192, None) == L.FP4_ERR_ALIGNMENT
+    a = L.fp4_tensor_t(16, 16, 16, 100, 256, 0, 16, 1, 0)
+    b = L.fp4_tensor_t(16, 16, 16, 128, 256, 0, 16, 1, 0)
+    assert lib.fp4_gemm(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(16), 1, 0, None) == L.FP4_ERR_SHAPE
+    a.rows = 128
+    a.scale_fmt = L.FP4_SCALE_UE8M0
+    assert lib.fp4_gemm(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(16), 1, 0, None) == L.FP4_ERR_UNSUPPORTED

@@ -1,0 +1,245 @@
+"""GPU parity of the block-scaled GEMMs against the oracle's FP64 GEMM.
+
+Acceptance per output element: |C - C_ref| <= 2^-20 * S with
+S = |alpha| sum_k |a_k b_k| (FP32 outputs), plus half a BF16 ulp of C_ref for
+BF16 outputs. Operands are quantized by the oracle and uploaded, so the GEMM is
+checked on its own; the end-to-end tests quantize on the GPU, check those bytes
+against the oracle, then run the three GEMMs of a linear layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+fb = pytest.importorskip("fp4_block_scaled_02_gb300")
+from gpu_common import (assert_quant_equal, gemm_bound_ok, oracle_quantize,  # noqa: E402
+                        to_gpu_bf16, upload_operand)
+import oracle  # noqa: E402
+from workloads import WORKLOADS, linear_inputs, random_bf16  # noqa: E402
+
+UE = fb.FP4_SCALE_UE5M3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    fb._lib.load()
+
+
+def _operand(seed, rows, cols, dist, fmt=fb.FP4_SCALE_E4M3, **kw):
+    bits = random_bf16(seed, (rows, cols), dist)
+    cfg = fb.QuantConfig(scale_fmt=fmt, **kw)
+    ref = oracle_quantize(cfg, bits)
+    return ref, upload_operand(ref, rows, cols, fmt)
+
+
+def _check(c_gpu, c_ref, s, bf16):
+    ok, err, tol = gemm_bound_ok(c_gpu, c_ref, s, bf16)
+    if not ok.all():
+        i = np.flatnonzero(~ok.reshape(-1))[:5]
+        raise AssertionError(f"{(~ok).sum()} of {ok.size} outside bound; first {i.tolist()}: "
+                             f"gpu {c_gpu.reshape(-1)[i]}, ref {c_ref.reshape(-1)[i]}, tol {tol.reshape(-1)[i]}")
+
+
+SHAPES = [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (1280, 1152, 768)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("out32", [False, True])
+def test_gemm_nvfp4_full_output(M, N, K, out32):
+    ra, a = _operand(31, M, K, "student_t4")
+    rb, b = _operand(32, N, K, "weight")
+    d = torch.empty((M, N), dtype=torch.float32 if out32 else torch.bfloat16, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert fb.fp4_device_status() == 0
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"])
+    _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
+
+
+def test_gemm_nvfp4_persistent_wrap_sampled():
+    # more output tiles than SMs: each CTA loops over several tiles and both accumulators
+    M, N, K = 2048, 2048, 512
+    ra, a = _operand(33, M, K, "normal")
+    rb, b = _operand(34, N, K, "log_normal_1e-4_2")
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert fb.fp4_device_status() == 0
+    rng = np.random.default_rng(0)
+    ms, ns = rng.integers(0, M, 4000), rng.integers(0, N, 4000)
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                           pairs=(ms, ns))
+    _check(d.cpu().numpy()[ms, ns], c_ref, s, bf16=False)
+
+
+def test_gemm_accumulate_fp32():
+    M, N, K = 256, 256, 512
+    ra, a = _operand(35, M, K, "normal")
+    rb, b = _operand(36, N, K, "normal")
+    base = torch.randn((M, N), dtype=torch.float32, device="cuda",
+                       generator=torch.Generator("cuda").manual_seed(0))
+    d = base.clone()
+    fb.fp4_linear_wgrad(a, b, d, accumulate=True)
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"])
+    got = d.cpu().numpy().astype(np.float64) - base.cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -20 * s + 2.0 ** -23 * np.abs(d.cpu().numpy())
+    assert np.all(np.abs(got - c_ref) <= tol)
+
+
+def test_gemm_zero_operand_gives_zero():
+    M, N, K = 128, 128, 256
+    ra, a = _operand(37, M, K, "normal")
+    a.codes.zero_()
+    rb, b = _operand(38, N, K, "normal")
+    d = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert torch.count_nonzero(d).item() == 0
+
+
+def test_gemm_shape_validation():
+    _, a = _operand(39, 128, 256, "normal")
+    _, b = _operand(40, 128, 256, "normal")
+    with pytest.raises(fb.Fp4Error) as e:
+        fb.fp4_gemm(a, b, torch.empty((128, 128), dtype=torch.bfloat16, device="cuda"), accumulate=True)
+    assert e.value.status == fb._lib.FP4_ERR_INVALID_ARG
+    a.rows = 100
+    with pytest.raises(fb.Fp4Error) as e:
+        fb.fp4_gemm(a, b, torch.empty((128, 128), dtype=torch.float32, device="cuda"))
+    assert e.value.status == fb._lib.FP4_ERR_SHAPE
+
+
+def _linear_end_to_end(w, which=0, fmt=fb.FP4_SCALE_E4M3, rht=True, sample=None):
+    """Quantize X, W, dY on the GPU per the recipe (checked bit-exact against the
+    oracle), run Fprop, Dgrad and Wgrad, and compare each with the oracle GEMM."""
+    inp = linear_inputs(w, which)
+    lin = w.linears[which]
+    T, K, N = lin.tokens, lin.k_in, lin.n_out
+    L = fb.Fp4Linear(T, K, N, scale_fmt=fmt, rht=rht, seed=w.rht_seed)
+    x, wt, dy = to_gpu_bf16(inp["x"]), to_gpu_bf16(inp["w"]), to_gpu_bf16(inp["dy"])
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    L.step(x, wt, dy, y, dx, dw)
+    assert fb.fp4_device_status() == 0
+    b = L.bufs
+    cfgs = {
+        "x": (L._cfg(0, 0), inp["x"]),
+        "w": (L._cfg(2, 0, block=fb.FP4_BLOCK_16x16), inp["w"]),
+        "wt": (L._cfg(2, 0, block=fb.FP4_BLOCK_16x16, orient=fb.FP4_ORIENT_COLWISE), inp["w"]),
+        "dy": (L._cfg(3, 0, round=fb.FP4_ROUND_SR), inp["dy"]),
+        "xt": (L._cfg(1, 0, orient=fb.FP4_ORIENT_COLWISE, rht=rht), inp["x"]),
+        "dyt": (L._cfg(4, 0, orient=fb.FP4_ORIENT_COLWISE, rht=rht, round=fb.FP4_ROUND_SR), inp["dy"]),
+    }
+    refs = {}
+    for k, (cfg, bits) in cfgs.items():
+        refs[k] = oracle_quantize(cfg, bits)
+        assert_quant_equal(b[k], refs[k], fb.FP4_LAYOUT_TCGEN05)
+    counters = L.counters.cpu().numpy()
+    assert counters[0].tolist() == refs["x"]["counters"].tolist()
+    assert counters[4].tolist() == refs["dyt"]["counters"].tolist()
+    for out, (ka, kb), bf16 in [(y, ("x", "w"), True), (dx, ("dy", "wt"), True), (dw, ("dyt", "xt"), False)]:
+        ra, rb = refs[ka], refs[kb]
+        if sample is None:
+            c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"])
+            _check(out.float().cpu().numpy(), c_ref, s, bf16)
+        else:
+            rng = np.random.default_rng(1)
+            ms = rng.integers(0, out.shape[0], sample)
+            ns = rng.integers(0, out.shape[1], sample)
+            c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                                   pairs=(ms, ns))
+            _check(out.float().cpu().numpy()[ms, ns], c_ref, s, bf16)
+
+
+def test_tiny_linear_end_to_end():
+    _linear_end_to_end(WORKLOADS["tiny"])
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_1p2b_linear_end_to_end_sampled(which):
+    _linear_end_to_end(WORKLOADS["1.2b"], which, sample=3000)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1280, 1152, 768)])
+@pytest.mark.parametrize("out32", [False, True])
+def test_gemm_ue5m3_emulated_full_output(M, N, K, out32):
+    ra, a = _operand(41, M, K, "log_normal_1e-4_2", fmt=UE, target_T=2048.0)
+    rb, b = _operand(42, N, K, "student_t4", fmt=UE, target_T=448.0)
+    d = torch.empty((M, N), dtype=torch.float32 if out32 else torch.bfloat16, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert fb.fp4_device_status() == 0
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                           scale_fmt=oracle.FMT_UE5M3)
+    _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
+
+
+def test_gemm_ue5m3_wide_scale_range_sampled():
+    # scales spread over many binades: a x10^3 drift against a held amax
+    # saturates some blocks and drives others toward the UE5M3 subnormals
+    M, N, K = 1024, 1024, 1024
+    from workloads import bf16_bits_to_f32, f32_to_bf16_bits
+    bits = random_bf16(43, (M, K), "log_normal_1e-4_2")
+    cfg = fb.QuantConfig(scale_fmt=UE, tscale=fb.FP4_TSCALE_HELD, target_T=2048.0)
+    st = oracle.HeldState()
+    oracle_quantize(cfg, bits, state=st)
+    cfg.step = 1
+    drift = f32_to_bf16_bits(bf16_bits_to_f32(bits) * np.float32(1e3))
+    ra = oracle_quantize(cfg, drift, state=st)
+    assert ra["counters"][2] > 0
+    a = upload_operand(ra, M, K, UE)
+    rb, b = _operand(44, N, K, "weight", fmt=UE)
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    rng = np.random.default_rng(2)
+    ms, ns = rng.integers(0, M, 3000), rng.integers(0, N, 3000)
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                           scale_fmt=oracle.FMT_UE5M3, pairs=(ms, ns))
+    _check(d.cpu().numpy()[ms, ns], c_ref, s, bf16=False)
+
+
+@pytest.mark.parametrize("T_target", [448.0, 2048.0])
+def test_ue5m3_periodic_scaling_sweep_steps(T_target):
+    """Sweep workload (4096 -> 4096, T = 8192): held amax refreshed every 50 steps,
+    UE5M3 scales, SR on gradients, no RHT, emulated GEMMs. Steps 0, 49, 50, 99
+    run in order on the GPU and the oracle; quantized bytes, counters and held
+    state match exactly and sampled GEMM outputs meet the bound."""
+    from workloads import sweep_dy
+    w = WORKLOADS["ue5m3_sweep"]
+    lin = w.linears[0]
+    inp = linear_inputs(w, 0)
+    T, K, N = lin.tokens, lin.k_in, lin.n_out
+    L = fb.Fp4Linear(T, K, N, scale_fmt=UE, rht=False, held=True, target_T=T_target, seed=w.sr_seed)
+    x, wt = to_gpu_bf16(inp["x"]), to_gpu_bf16(inp["w"])
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    states = {k: oracle.HeldState() for k in ("x", "w", "dy", "xt", "dyt")}
+    rng = np.random.default_rng(3)
+    for step in (0, 49, 50, 99):
+        dyb = sweep_dy(inp["dy"], step, w.steps)
+        L.counters.zero_()
+        L.step(x, wt, to_gpu_bf16(dyb), y, dx, dw, step=step)
+        assert fb.fp4_device_status() == 0
+        cfgs = {
+            "x": (L._cfg(0, step), inp["x"], 0),
+            "w": (L._cfg(2, step, block=fb.FP4_BLOCK_16x16), inp["w"], 2),
+            "dy": (L._cfg(3, step, round=fb.FP4_ROUND_SR), dyb, 3),
+            "xt": (L._cfg(1, step, orient=fb.FP4_ORIENT_COLWISE), inp["x"], 1),
+            "dyt": (L._cfg(4, step, orient=fb.FP4_ORIENT_COLWISE, round=fb.FP4_ROUND_SR), dyb, 4),
+        }
+        refs = {}
+        for k, (cfg, bits, ci) in cfgs.items():
+            refs[k] = oracle_quantize(cfg, bits, state=states[k])
+            assert_quant_equal(L.bufs[k], refs[k], fb.FP4_LAYOUT_TCGEN05)
+            assert L.counters[ci].cpu().numpy().tolist() == refs[k]["counters"].tolist(), (step, k)
+            gst = L.states[ci]
+            assert np.float32(gst.amax) == states[k].amax[0] and gst.last_refresh_step == int(states[k].last[0])
+        ms, ns = rng.integers(0, T, 1500), rng.integers(0, N, 1500)
+        for out, (ka, kb), bf16 in [(y, ("x", "w"), True), (dw, ("dyt", "xt"), False)]:
+            ra, rb = refs[ka], refs[kb]
+            mm = ms % out.shape[0]
+            nn = ns % out.shape[1]
+            c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                                   scale_fmt=oracle.FMT_UE5M3, pairs=(mm, nn))
+            _check(out.float().cpu().numpy()[mm, nn], c_ref, s, bf16)

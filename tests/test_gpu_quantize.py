@@ -1,0 +1,185 @@
+"""GPU parity of the quantizer kernels against the CPU oracle, through the C ABI.
+
+Bit-exact on codes, scale bytes (plain and tensor-core layouts), the FP32
+decode tensor scale, the four event counters and the held-amax state. Sizes
+span several tiles; plain-layout cases have ragged shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+fb = pytest.importorskip("fp4_block_scaled_02_gb300")
+from gpu_common import (assert_quant_equal, gpu_quantize, new_ws, oracle_quantize,  # noqa: E402
+                        to_gpu_bf16)
+import oracle  # noqa: E402
+from workloads import bf16_bits_to_f32, f32_to_bf16_bits, random_bf16  # noqa: E402
+
+TC, PLAIN = fb.FP4_LAYOUT_TCGEN05, fb.FP4_LAYOUT_PLAIN
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    fb._lib.load()
+
+
+ROWWISE_CASES = [
+    # (shape, dist, round, layout, seed, tensor_id, step)
+    ((384, 512), "student_t4", fb.FP4_ROUND_RNE, TC, 0, 0, 0),
+    ((256, 768), "log_normal_1e-4_2", fb.FP4_ROUND_SR, TC, 5, 3, 17),
+    ((128, 64), "normal_outliers", fb.FP4_ROUND_RNE, TC, 0, 0, 0),
+    ((37, 80), "normal", fb.FP4_ROUND_RNE, PLAIN, 0, 0, 0),
+    ((129, 48), "log_uniform_1e-6_1e-2", fb.FP4_ROUND_SR, PLAIN, 9, 7, 3),
+]
+
+
+@pytest.mark.parametrize("case", ROWWISE_CASES)
+def test_rowwise_1x16(case):
+    shape, dist, rnd, layout, seed, tid, step = case
+    bits = random_bf16(11, shape, dist)
+    cfg = fb.QuantConfig(round=rnd, layout=layout, seed=seed, tensor_id=tid, step=step)
+    out, _, cnt = gpu_quantize(cfg, bits)
+    assert_quant_equal(out, oracle_quantize(cfg, bits), layout, cnt)
+
+
+COLWISE_CASES = [
+    # (input shape (tokens, channels), dist, round, rht, layout, seed)
+    ((512, 256), "student_t4", fb.FP4_ROUND_RNE, False, TC, 0),
+    ((512, 256), "normal_outliers", fb.FP4_ROUND_RNE, True, TC, 0),
+    ((256, 384), "log_normal_1e-4_2", fb.FP4_ROUND_SR, True, TC, 1),
+    ((192, 128), "log_uniform_1e-6_1e-2", fb.FP4_ROUND_SR, False, TC, 3),
+    ((48, 24), "normal", fb.FP4_ROUND_RNE, True, PLAIN, 0),
+    ((80, 40), "log_normal_1e-4_2", fb.FP4_ROUND_SR, True, PLAIN, 2),
+]
+
+
+@pytest.mark.parametrize("case", COLWISE_CASES)
+def test_colwise_1x16_with_rht(case):
+    shape, dist, rnd, rht, layout, seed = case
+    bits = random_bf16(12, shape, dist)
+    cfg = fb.QuantConfig(round=rnd, rht=rht, orient=fb.FP4_ORIENT_COLWISE, layout=layout, seed=seed,
+                         tensor_id=4, step=2)
+    out, _, cnt = gpu_quantize(cfg, bits)
+    assert_quant_equal(out, oracle_quantize(cfg, bits), layout, cnt)
+
+
+@pytest.mark.parametrize("shape,layout", [((384, 256), TC), ((256, 512), TC), ((48, 80), PLAIN)])
+@pytest.mark.parametrize("orient", [fb.FP4_ORIENT_ROWWISE, fb.FP4_ORIENT_COLWISE])
+def test_weights_2d_both_orientations(shape, layout, orient):
+    bits = random_bf16(13, shape, "weight")
+    cfg = fb.QuantConfig(block=fb.FP4_BLOCK_16x16, layout=layout, emit_transpose=True, orient=orient)
+    out, out_t, cnt = gpu_quantize(cfg, bits, with_transpose=True)
+    ref = oracle_quantize(cfg, bits)
+    ref_t = oracle_quantize(cfg, bits, colwise=orient == fb.FP4_ORIENT_ROWWISE)
+    assert_quant_equal(out, ref, layout, cnt)
+    assert_quant_equal(out_t, ref_t, layout)
+    # quantize(W)^T == quantize(W^T): the two outputs hold the same nibbles
+    a = out.codes.cpu().numpy()
+    b = out_t.codes.cpu().numpy()
+    ua = np.stack([a & 0xF, a >> 4], axis=-1).reshape(a.shape[0], -1)
+    ub = np.stack([b & 0xF, b >> 4], axis=-1).reshape(b.shape[0], -1)
+    assert np.array_equal(ua.T, ub)
+
+
+@pytest.mark.parametrize("shape,layout", [((256, 512), TC), ((384, 128), TC), ((10, 64), PLAIN), ((3, 96), PLAIN)])
+def test_mxfp4_1x32(shape, layout):
+    bits = random_bf16(14, shape, "student_t4")
+    cfg = fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE8M0, block=fb.FP4_BLOCK_1x32, layout=layout)
+    out, _, cnt = gpu_quantize(cfg, bits)
+    ref = oracle_quantize(cfg, bits)
+    assert_quant_equal(out, ref, layout, cnt)
+    assert int(cnt[0]) == 0
+
+
+def test_ue5m3_current_and_held_amax():
+    base = random_bf16(15, (256, 512), "log_normal_1e-4_2")
+    state = fb.AmaxState()
+    ostate = oracle.HeldState()
+    for step, factor in [(0, 1.0), (1, 30.0), (49, 1e-3), (50, 1e3), (51, 1.0)]:
+        bits = f32_to_bf16_bits(bf16_bits_to_f32(base) * np.float32(factor))
+        cfg = fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE5M3, tscale=fb.FP4_TSCALE_HELD, target_T=2048.0,
+                             round=fb.FP4_ROUND_SR, step=step, seed=4, tensor_id=3)
+        out, _, cnt = gpu_quantize(cfg, bits, state=state)
+        ref = oracle_quantize(cfg, bits, state=ostate)
+        assert_quant_equal(out, ref, TC, cnt)
+        assert state.valid == 1 and state.last_refresh_step == int(ostate.last[0])
+        assert np.float32(state.amax) == ostate.amax[0]
+    cfg = fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE5M3, target_T=448.0)
+    out, _, cnt = gpu_quantize(cfg, base)
+    assert_quant_equal(out, oracle_quantize(cfg, base), TC, cnt)
+
+
+def test_held_state_invalid_on_non_refresh_step_sets_status():
+    assert fb.fp4_device_status() == 0
+    bits = random_bf16(16, (128, 64), "normal")
+    cfg = fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE5M3, tscale=fb.FP4_TSCALE_HELD, target_T=2048.0, step=7)
+    out, _, cnt = gpu_quantize(cfg, bits, state=fb.AmaxState())
+    assert fb.fp4_device_status() == fb._lib.FP4_ERR_STATE
+    assert fb.fp4_device_status() == 0          # reading clears it
+    assert np.all(out.codes.cpu().numpy() == 0xAA)   # nothing written
+    assert int(cnt.sum()) == 0
+
+
+def test_current_scaling_nvfp4_large_values_and_zero_tensor():
+    bits = np.zeros((128, 64), dtype=np.uint16)
+    cfg = fb.QuantConfig()
+    out, _, cnt = gpu_quantize(cfg, bits)
+    assert_quant_equal(out, oracle_quantize(cfg, bits), TC, cnt)
+    big = random_bf16(17, (128, 128), "normal")
+    big = f32_to_bf16_bits(bf16_bits_to_f32(big) * np.float32(1e30))
+    out, _, cnt = gpu_quantize(cfg, big)
+    assert_quant_equal(out, oracle_quantize(cfg, big), TC, cnt)
+
+
+def test_empty_input_is_a_no_op():
+    cfg = fb.QuantConfig(layout=PLAIN)
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    out = fb.QTensor.empty(0, 64, layout=PLAIN)
+    fb.fp4_quantize(cfg, x, out, ws=new_ws())
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("fmt,block,shape", [(fb.FP4_SCALE_E4M3, fb.FP4_BLOCK_1x16, (256, 256)),
+                                             (fb.FP4_SCALE_UE5M3, fb.FP4_BLOCK_1x16, (128, 512)),
+                                             (fb.FP4_SCALE_UE8M0, fb.FP4_BLOCK_1x32, (128, 256))])
+@pytest.mark.parametrize("layout", [TC, PLAIN])
+def test_dequantize(fmt, block, shape, layout):
+    bits = random_bf16(18, shape, "student_t4")
+    cfg = fb.QuantConfig(scale_fmt=fmt, block=block, layout=layout)
+    out, _, _ = gpu_quantize(cfg, bits)
+    ref = oracle_quantize(cfg, bits)
+    bs = 32 if fmt == fb.FP4_SCALE_UE8M0 else 16
+    want = oracle.dequantize(ref["codes"], ref["scales"], ref["s_dec"], {0: 0, 1: 1, 2: 2}[fmt], bs)
+    y32 = torch.empty(shape, dtype=torch.float32, device="cuda")
+    fb.fp4_dequantize(out, y32)
+    y16 = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    fb.fp4_dequantize(out, y16)
+    torch.cuda.synchronize()
+    assert np.array_equal(y32.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert torch.equal(y16.cpu(), torch.from_numpy(want).to(torch.bfloat16))
+
+
+def test_quantize_is_deterministic():
+    bits = random_bf16(19, (256, 512), "log_normal_1e-4_2")
+    cfg = fb.QuantConfig(round=fb.FP4_ROUND_SR, rht=True, orient=fb.FP4_ORIENT_COLWISE, seed=3)
+    a, _, ca = gpu_quantize(cfg, bits)
+    b, _, cb = gpu_quantize(cfg, bits)
+    assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales) and torch.equal(ca, cb)
+
+
+def test_validation_errors_launch_nothing():
+    x = to_gpu_bf16(random_bf16(20, (128, 64), "normal"))
+    out = fb.QTensor.empty(128, 64)
+    with pytest.raises(fb.Fp4Error) as e:
+        fb.fp4_quantize(fb.QuantConfig(), x, out, ws=None)            # current scaling needs workspace
+    assert e.value.status == fb._lib.FP4_ERR_WORKSPACE
+    with pytest.raises(fb.Fp4Error) as e:
+        fb.fp4_quantize(fb.QuantConfig(rht=True), x, out, ws=new_ws())  # RHT needs colwise
+    assert e.value.status == fb._lib.FP4_ERR_INVALID_ARG
+    bad = fb.QTensor.empty(128, 48)
+    with pytest.raises(fb.Fp4Error) as e:
+        fb.fp4_quantize(fb.QuantConfig(), to_gpu_bf16(random_bf16(21, (128, 48), "normal")), bad, ws=new_ws())
+    assert e.value.status == fb._lib.FP4_ERR_SHAPE                      # 48/16 = 3 blocks: not a multiple of 4
