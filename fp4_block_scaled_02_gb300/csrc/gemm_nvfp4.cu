@@ -18,8 +18,15 @@
 //                 stage back to the producer;
 //   warps 2-5   : epilogue -- tcgen05.ld the FP32 accumulator (each warp owns
 //                 its 32-lane quadrant), scale by alpha, store BF16 / FP32.
-// Two accumulators in tensor memory let the epilogue of tile t overlap the
-// main loop of tile t+1. Every mbarrier wait is bounded (see tcgen05.cuh).
+// K is accumulated in chunks of 1024 values (CHUNK_STAGES stages): each chunk
+// starts a fresh accumulator in one of two tensor-memory buffers, and the
+// epilogue adds the chunk partials in FP32 registers with round-to-nearest.
+// Measured on GB300, one accumulator carried over K = 8192 drifts toward zero
+// (every out-of-bound output was smaller in magnitude than the exact sum), a
+// bias that grows with the number of MMAs folded into the accumulator; chunking
+// bounds it by the chunk length instead of K, and the two buffers let the
+// epilogue fold chunk c while the MMAs of chunk c+1 (or of the next tile) run.
+// Every mbarrier wait is bounded (see tcgen05.cuh).
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -50,6 +57,7 @@ template <int BN_, int STAGES_>
 struct NvCfg {
     static constexpr int BM = 128, BN = BN_, STAGES = STAGES_;
     static constexpr int BK = 256;                 // FP4 values per stage = 128 bytes per row
+    static constexpr int CHUNK_STAGES = 4;         // K values per accumulator chunk = 1024
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = BN * 128;
     static constexpr int SFA_BYTES = BM * 16;      // 16 scale blocks of 16 per row per stage
@@ -149,16 +157,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC = tc::idesc_mxf4nvf4(Cfg::BM, Cfg::BN);
-            uint32_t it = 0;
-            int local = 0;
+            uint32_t it = 0, chunk = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
-                const int acc = local % Cfg::NUM_ACC;
-                const uint32_t aph = (uint32_t)(local / Cfg::NUM_ACC) & 1u;
-                if (!tc::mbar_wait(acce_bar(acc), aph ^ 1u, p.status)) break;
-                tc::fence_after_sync();
-                const uint32_t d_tmem = tmem + (uint32_t)(acc * Cfg::BN);
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                uint32_t d_tmem = tmem;
                 for (int kb = 0; kb < num_k; ++kb, ++it) {
+                    const bool first = kb % Cfg::CHUNK_STAGES == 0;
+                    const bool last = kb % Cfg::CHUNK_STAGES == Cfg::CHUNK_STAGES - 1 || kb == num_k - 1;
+                    const int buf = (int)(chunk % Cfg::NUM_ACC);
+                    if (first) {
+                        // the epilogue must have drained this buffer's previous chunk
+                        if (!tc::mbar_wait(acce_bar(buf), ((chunk / Cfg::NUM_ACC) & 1u) ^ 1u, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        d_tmem = tmem + (uint32_t)(buf * Cfg::BN);
+                    }
                     const int s = (int)(it % Cfg::STAGES);
                     const uint32_t ph = (it / Cfg::STAGES) & 1u;
                     if (!tc::mbar_wait(full_bar(s), ph, p.status)) {
@@ -184,11 +199,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     for (int kk = 0; kk < 4; ++kk) {
                         tc::mma_mxf4nvf4(d_tmem, tc::kmajor_sw128_desc(a_s + 32 * kk),
                                          tc::kmajor_sw128_desc(b_s + 32 * kk), IDESC, sfa_t + 4 * kk,
-                                         sfb_t + (Cfg::BN / 32) * kk, (kb | kk) != 0 ? 1u : 0u);
+                                         sfb_t + (Cfg::BN / 32) * kk, (!first || kk != 0) ? 1u : 0u);
                     }
                     tc::commit(empty_bar(s));
+                    if (last) {
+                        tc::commit(accf_bar(buf));
+                        ++chunk;
+                    }
                 }
-                if (ok) tc::commit(accf_bar(acc));
             }
             // wait until every MMA this thread issued has retired before the
             // tensor memory is released
@@ -199,57 +217,64 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // the TMEM lane quadrant this warp may access
         const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
-        int local = 0;
-        for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+        const int nchunks = (num_k + Cfg::CHUNK_STAGES - 1) / Cfg::CHUNK_STAGES;
+        uint32_t chunk = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
             const int64_t mb = tile % num_m, nb = tile / num_m;
-            const int acc = local % Cfg::NUM_ACC;
-            const uint32_t aph = (uint32_t)(local / Cfg::NUM_ACC) & 1u;
-            if (!tc::mbar_wait(accf_bar(acc), aph, p.status)) break;
-            tc::fence_after_sync();
-            const int64_t m = mb * Cfg::BM + q * 32 + lane;
-            const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Cfg::BN);
-#pragma unroll 1
-            for (int c = 0; c < Cfg::BN; c += 32) {
-                uint32_t r[32];
-                tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
-                tc::tmem_ld_wait();
-                if (c + 32 == Cfg::BN) {
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(acce_bar(acc));
+            float acc[Cfg::BN];
+#pragma unroll
+            for (int c = 0; c < Cfg::BN; ++c) acc[c] = 0.0f;
+            for (int ch = 0; ch < nchunks; ++ch, ++chunk) {
+                const int buf = (int)(chunk % Cfg::NUM_ACC);
+                if (!tc::mbar_wait(accf_bar(buf), (chunk / Cfg::NUM_ACC) & 1u, p.status)) {
+                    ok = false;
+                    break;
                 }
-                const int64_t n0 = nb * Cfg::BN + c;
-                if (OUT32) {
-                    float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+                tc::fence_after_sync();
+                const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * Cfg::BN);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        float4 o = make_float4(__fmul_rn(__uint_as_float(r[4 * v + 0]), alpha),
-                                               __fmul_rn(__uint_as_float(r[4 * v + 1]), alpha),
-                                               __fmul_rn(__uint_as_float(r[4 * v + 2]), alpha),
-                                               __fmul_rn(__uint_as_float(r[4 * v + 3]), alpha));
-                        if (p.accumulate) {
-                            const float4 old = reinterpret_cast<const float4*>(dst)[v];
-                            o.x = __fadd_rn(o.x, old.x);
-                            o.y = __fadd_rn(o.y, old.y);
-                            o.z = __fadd_rn(o.z, old.z);
-                            o.w = __fadd_rn(o.w, old.w);
-                        }
-                        reinterpret_cast<float4*>(dst)[v] = o;
+                for (int c = 0; c < Cfg::BN; c += 32) {
+                    uint32_t r[32];
+                    tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[c + i] = __fadd_rn(acc[c + i], __uint_as_float(r[i]));
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(acce_bar(buf));
+            }
+            if (!ok) break;
+            const int64_t m = mb * Cfg::BM + q * 32 + lane;
+            const int64_t n0 = nb * Cfg::BN;
+            if (OUT32) {
+                float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+#pragma unroll
+                for (int v = 0; v < Cfg::BN / 4; ++v) {
+                    float4 o = make_float4(__fmul_rn(acc[4 * v + 0], alpha), __fmul_rn(acc[4 * v + 1], alpha),
+                                           __fmul_rn(acc[4 * v + 2], alpha), __fmul_rn(acc[4 * v + 3], alpha));
+                    if (p.accumulate) {
+                        const float4 old = reinterpret_cast<const float4*>(dst)[v];
+                        o.x = __fadd_rn(o.x, old.x);
+                        o.y = __fadd_rn(o.y, old.y);
+                        o.z = __fadd_rn(o.z, old.z);
+                        o.w = __fadd_rn(o.w, old.w);
                     }
-                } else {
-                    uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
+                    reinterpret_cast<float4*>(dst)[v] = o;
+                }
+            } else {
+                uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t w[4];
+                for (int v = 0; v < Cfg::BN / 8; ++v) {
+                    uint32_t w[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const __nv_bfloat162 h =
-                                __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * v + 2 * k]), alpha),
-                                                      __fmul_rn(__uint_as_float(r[8 * v + 2 * k + 1]), alpha));
-                            w[k] = *reinterpret_cast<const uint32_t*>(&h);
-                        }
-                        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(acc[8 * v + 2 * k], alpha),
+                                                                       __fmul_rn(acc[8 * v + 2 * k + 1], alpha));
+                        w[k] = *reinterpret_cast<const uint32_t*>(&h);
                     }
+                    reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
         }

@@ -18,7 +18,10 @@
 //               writes the 128-byte-swizzled K-major layout the tensor core reads;
 //   warp 1    : one lane issues tcgen05.mma kind::f16 (K = 16) on each decoded
 //               slice and commits it back to the decoders;
-//   warps 6-9 : epilogue (tcgen05.ld, x alpha, BF16/FP32 store).
+//   warps 6-9 : epilogue: each raw stage (K = 256) is one accumulator chunk in
+//               one of two tensor-memory buffers; the epilogue folds the chunk
+//               partials in FP32 registers with round-to-nearest (the same
+//               bias control as the NVFP4 kernel), then stores alpha * sum.
 #include <cstdint>
 
 #include <cuda.h>
@@ -228,16 +231,18 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC = tc::idesc_bf16(C::BM, C::BN);
-            uint32_t it_dec = 0;
-            int local = 0;
+            uint32_t it_dec = 0, chunk = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
-                const int acc = local & 1;
-                const uint32_t aph = (uint32_t)(local >> 1) & 1u;
-                if (!tc::mbar_wait(acce(acc), aph ^ 1u, p.status)) break;
-                tc::fence_after_sync();
-                const uint32_t d_tmem = tmem + (uint32_t)(acc * C::BN);
-                for (int kb = 0; kb < num_k && ok; ++kb) {
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < num_k && ok; ++kb, ++chunk) {
+                    // one raw stage = one accumulator chunk
+                    const int buf = (int)(chunk & 1u);
+                    if (!tc::mbar_wait(acce(buf), ((chunk >> 1) & 1u) ^ 1u, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t d_tmem = tmem + (uint32_t)(buf * C::BN);
                     for (int kk = 0; kk < 4; ++kk, ++it_dec) {
                         const int ds = (int)(it_dec % C::DEC_STAGES);
                         if (!tc::mbar_wait(dec_full(ds), (it_dec / C::DEC_STAGES) & 1u, p.status)) {
@@ -250,12 +255,11 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
 #pragma unroll
                         for (int k16 = 0; k16 < 4; ++k16)
                             tc::mma_bf16(d_tmem, tc::kmajor_sw128_desc(a_s + 32 * k16),
-                                         tc::kmajor_sw128_desc(b_s + 32 * k16), IDESC,
-                                         (kb | kk | k16) != 0 ? 1u : 0u);
+                                         tc::kmajor_sw128_desc(b_s + 32 * k16), IDESC, (kk | k16) != 0 ? 1u : 0u);
                         tc::commit(dec_empty(ds));
                     }
+                    if (ok) tc::commit(accf(buf));
                 }
-                if (ok) tc::commit(accf(acc));
             }
             tc::commit(drain);
             tc::mbar_wait(drain, 0, p.status);
@@ -264,57 +268,63 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         // ------------------------------------------------------------ epilogue (warps 6-9)
         const int q = warp & 3;
         const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
-        int local = 0;
-        for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+        uint32_t chunk = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
             const int64_t mb = tile % num_m, nb = tile / num_m;
-            const int acc = local & 1;
-            const uint32_t aph = (uint32_t)(local >> 1) & 1u;
-            if (!tc::mbar_wait(accf(acc), aph, p.status)) break;
-            tc::fence_after_sync();
-            const int64_t m = mb * C::BM + q * 32 + lane;
-            const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::BN);
-#pragma unroll 1
-            for (int c = 0; c < C::BN; c += 32) {
-                uint32_t rr[32];
-                tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, rr);
-                tc::tmem_ld_wait();
-                if (c + 32 == C::BN) {
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(acce(acc));
+            float acc[C::BN];
+#pragma unroll
+            for (int c = 0; c < C::BN; ++c) acc[c] = 0.0f;
+            for (int kb = 0; kb < num_k; ++kb, ++chunk) {
+                const int buf = (int)(chunk & 1u);
+                if (!tc::mbar_wait(accf(buf), (chunk >> 1) & 1u, p.status)) {
+                    ok = false;
+                    break;
                 }
-                const int64_t n0 = nb * C::BN + c;
-                if (OUT32) {
-                    float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+                tc::fence_after_sync();
+                const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::BN);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        float4 o = make_float4(__fmul_rn(__uint_as_float(rr[4 * v + 0]), alpha),
-                                               __fmul_rn(__uint_as_float(rr[4 * v + 1]), alpha),
-                                               __fmul_rn(__uint_as_float(rr[4 * v + 2]), alpha),
-                                               __fmul_rn(__uint_as_float(rr[4 * v + 3]), alpha));
-                        if (p.accumulate) {
-                            const float4 old = reinterpret_cast<const float4*>(dst)[v];
-                            o.x = __fadd_rn(o.x, old.x);
-                            o.y = __fadd_rn(o.y, old.y);
-                            o.z = __fadd_rn(o.z, old.z);
-                            o.w = __fadd_rn(o.w, old.w);
-                        }
-                        reinterpret_cast<float4*>(dst)[v] = o;
+                for (int c = 0; c < C::BN; c += 32) {
+                    uint32_t rr[32];
+                    tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, rr);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[c + i] = __fadd_rn(acc[c + i], __uint_as_float(rr[i]));
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(acce(buf));
+            }
+            if (!ok) break;
+            const int64_t m = mb * C::BM + q * 32 + lane;
+            const int64_t n0 = nb * C::BN;
+            if (OUT32) {
+                float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+#pragma unroll
+                for (int v = 0; v < C::BN / 4; ++v) {
+                    float4 o = make_float4(__fmul_rn(acc[4 * v + 0], alpha), __fmul_rn(acc[4 * v + 1], alpha),
+                                           __fmul_rn(acc[4 * v + 2], alpha), __fmul_rn(acc[4 * v + 3], alpha));
+                    if (p.accumulate) {
+                        const float4 old = reinterpret_cast<const float4*>(dst)[v];
+                        o.x = __fadd_rn(o.x, old.x);
+                        o.y = __fadd_rn(o.y, old.y);
+                        o.z = __fadd_rn(o.z, old.z);
+                        o.w = __fadd_rn(o.w, old.w);
                     }
-                } else {
-                    uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
+                    reinterpret_cast<float4*>(dst)[v] = o;
+                }
+            } else {
+                uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t w[4];
+                for (int v = 0; v < C::BN / 8; ++v) {
+                    uint32_t w[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const __nv_bfloat162 h =
-                                __floats2bfloat162_rn(__fmul_rn(__uint_as_float(rr[8 * v + 2 * k]), alpha),
-                                                      __fmul_rn(__uint_as_float(rr[8 * v + 2 * k + 1]), alpha));
-                            w[k] = *reinterpret_cast<const uint32_t*>(&h);
-                        }
-                        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(acc[8 * v + 2 * k], alpha),
+                                                                       __fmul_rn(acc[8 * v + 2 * k + 1], alpha));
+                        w[k] = *reinterpret_cast<const uint32_t*>(&h);
                     }
+                    reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
         }
