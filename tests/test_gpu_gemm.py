@@ -243,3 +243,81 @@ def test_ue5m3_periodic_scaling_sweep_steps(T_target):
             c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
                                    scale_fmt=oracle.FMT_UE5M3, pairs=(mm, nn))
             _check(out.float().cpu().numpy()[mm, nn], c_ref, s, bf16)
+
+
+def _banded_linear(w, which, band=128, samples=2000):
+    """Full-size linear of a large workload: the GPU runs the whole recipe; the
+    oracle quantizes one band of `band` operand rows of every operand (the
+    tensor amax still covers the whole tensor), those bytes must match the GPU's
+    exactly, and GEMM outputs sampled inside the bands must meet the bound."""
+    inp = linear_inputs(w, which)
+    lin = w.linears[which]
+    T, K, N = lin.tokens, lin.k_in, lin.n_out
+    L = fb.Fp4Linear(T, K, N, rht=True, seed=w.rht_seed)
+    x, wt, dy = to_gpu_bf16(inp["x"]), to_gpu_bf16(inp["w"]), to_gpu_bf16(inp["dy"])
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    L.step(x, wt, dy, y, dx, dw)
+    assert fb.fp4_device_status() == 0
+    rng = np.random.default_rng(5)
+    cfgs = {
+        "x": (L._cfg(0, 0), inp["x"], T),
+        "w": (L._cfg(2, 0, block=fb.FP4_BLOCK_16x16), inp["w"], N),
+        "wt": (L._cfg(2, 0, block=fb.FP4_BLOCK_16x16, orient=fb.FP4_ORIENT_COLWISE), inp["w"], K),
+        "dy": (L._cfg(3, 0, round=fb.FP4_ROUND_SR), inp["dy"], T),
+        "xt": (L._cfg(1, 0, orient=fb.FP4_ORIENT_COLWISE, rht=True), inp["x"], K),
+        "dyt": (L._cfg(4, 0, orient=fb.FP4_ORIENT_COLWISE, rht=True, round=fb.FP4_ROUND_SR), inp["dy"], N),
+    }
+    refs, r0s = {}, {}
+    for k, (cfg, bits, R) in cfgs.items():
+        r0 = int(rng.integers(0, R // band)) * band
+        r0s[k] = r0
+        ref = oracle.quantize(bits, scale_fmt=oracle.FMT_E4M3,
+                              block=oracle.BLOCK_16x16 if cfg.block == fb.FP4_BLOCK_16x16 else oracle.BLOCK_1x16,
+                              sr=cfg.round == fb.FP4_ROUND_SR, colwise=cfg.orient == fb.FP4_ORIENT_COLWISE,
+                              rht=cfg.rht, seed=cfg.seed, tensor_id=cfg.tensor_id, step=0,
+                              op_rows=(r0, r0 + band))
+        refs[k] = ref
+        q = L.bufs[k]
+        assert np.array_equal(q.codes[r0:r0 + band].cpu().numpy(), ref["codes"]), k
+        # scales of the band: the band is one 128-row tile of the tensor-core layout
+        nb = q.cols // 16
+        got = q.scales.view(-1, nb * 128)[r0 // 128].cpu().numpy()
+        assert np.array_equal(got, oracle.swizzle_scales(ref["scales"])), k
+        assert np.float32(q.s_dec[0].item()) == np.float32(ref["s_dec"]), k
+    for out, (ka, kb), bf16 in [(y, ("x", "w"), True), (dx, ("dy", "wt"), True), (dw, ("dyt", "xt"), False)]:
+        ra, rb = refs[ka], refs[kb]
+        ms = rng.integers(0, band, samples)
+        ns = rng.integers(0, band, samples)
+        c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                               pairs=(ms, ns))
+        _check(out.float().cpu().numpy()[r0s[ka] + ms, r0s[kb] + ns], c_ref, s, bf16)
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_8b_linear_full_size_banded(which):
+    _banded_linear(WORKLOADS["8b"], which)
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_12b_linear_full_size_banded(which):
+    _banded_linear(WORKLOADS["12b"], which)
+
+
+def test_8b_mxfp4_side_by_side_counters():
+    """The 8B workload's activations and gradients through the MXFP4 1x32
+    quantizer next to NVFP4: full-tensor event counters equal the oracle's."""
+    w = WORKLOADS["8b"]
+    inp = linear_inputs(w, 0)
+    for key in ("x", "dy"):
+        bits = inp[key]
+        for cfg in (fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE8M0, block=fb.FP4_BLOCK_1x32),
+                    fb.QuantConfig()):
+            out = fb.QTensor.empty(bits.shape[0], bits.shape[1], cfg.scale_fmt)
+            cnt = torch.zeros(4, dtype=torch.int64, device="cuda")
+            fb.fp4_quantize(cfg, to_gpu_bf16(bits), out, counters=cnt,
+                            ws=torch.empty(4096, dtype=torch.float32, device="cuda"))
+            ref = oracle_quantize(cfg, bits)
+            assert cnt.cpu().numpy().tolist() == ref["counters"].tolist(), (key, cfg.scale_fmt)
+            assert np.array_equal(out.codes.cpu().numpy(), ref["codes"])
