@@ -161,6 +161,46 @@ fp4_status_t check_operand(const fp4_tensor_t* t) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Allocation-free quantize.
+//
+// Some callers cannot allocate device memory at all: a plug-in running inside
+// another framework's engine, whose memory budget is owned and pre-planned by
+// that engine, or a latency-critical loop that must never reach an allocator.
+// fp4_quantize needs a caller-provided workspace for the amax partials of its
+// first pass; fp4_quantize_noalloc instead uses the library's own file-scope
+// scratch array below. Its size is the largest number of partials the amax
+// pass ever writes (kNoAllocScratchFloats floats = 8 KB), and every GPU that
+// loads this library keeps that array until the process exits.
+//
+// The array's host-side name is only a stand-in for the device symbol, so its
+// device address is looked up once per device (cudaGetSymbolAddress, with the
+// device current) by the first call made on that device; make that first call
+// before any stream capture begins. Every call shares the one array and it
+// keeps the last call's contents; nothing in it needs to start at zero,
+// because the amax pass writes every partial the conversion pass reads. Calls
+// whose work overlaps on the GPU (different streams, no ordering between
+// them) race on the array.
+namespace {
+
+constexpr int kNoAllocScratchFloats = kMaxAmaxPartials;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+float* g_noalloc_ptr[kMaxDevices];
+
+float* noalloc_scratch_ptr() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        float* ptr = nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp4_abi_version(void) { return 1; }
@@ -205,6 +245,24 @@ fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int6
                           uint64_t* counters, void* ws, size_t ws_bytes, void* stream) {
     QuantJob job;
     fp4_status_t s = check_quantize(p, in_bf16, rows, cols, out, out_t, state, counters, ws, ws_bytes, job);
+    if (s != FP4_OK) return s;
+    if (rows == 0 || cols == 0) return FP4_OK;
+    job.status = device_status_ptr();
+    if (job.status == nullptr) return FP4_ERR_CUDA;
+    return from_cuda(launch_quantize(job, static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+                                  const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
+                                  uint64_t* counters, void* stream) {
+    float* scratch = noalloc_scratch_ptr();
+    if (scratch == nullptr) return FP4_ERR_CUDA;
+    QuantJob job;
+    // the scratch is offered as a workspace of its fixed size: a call that
+    // would need more amax partials than it holds is rejected with
+    // FP4_ERR_WORKSPACE before anything is launched
+    fp4_status_t s = check_quantize(p, in_bf16, rows, cols, out, out_t, state, counters, scratch,
+                                    sizeof(float) * kNoAllocScratchFloats, job);
     if (s != FP4_OK) return s;
     if (rows == 0 || cols == 0) return FP4_OK;
     job.status = device_status_ptr();

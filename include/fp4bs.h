@@ -150,6 +150,22 @@ fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int6
                           const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                           uint64_t* counters, void* ws, size_t ws_bytes, void* stream);
 
+/* fp4_quantize without a workspace argument, for callers that cannot
+ * allocate device memory at all (for example a plug-in inside another
+ * framework's engine that owns the memory budget, or a latency-critical loop
+ * that must never reach an allocator). The papers have no counterpart: this is
+ * a library convenience. The amax partials go to a library-owned 8 KB device
+ * array (2048 floats, held by every GPU that loads the library until exit)
+ * instead of a caller workspace; calls needing more partials than it holds
+ * are rejected with FP4_ERR_WORKSPACE (no shape does: the amax pass caps its
+ * partials at 2048). The first call on each device looks up the array's device
+ * address, so make it before any stream capture. All calls share the array:
+ * calls that overlap on the GPU race on it. Everything else is as for
+ * fp4_quantize, and no device memory is allocated or freed. */
+fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+                                  const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
+                                  uint64_t* counters, void* stream);
+
 /* Decode an operand back to real values, x = e2m1 * s_hat * s_dec,G computed as
  * RN(RN(e2m1 * s_hat) * s_dec,G) in FP32 (section A3; App. B.3), written as
  * rows x cols BF16 (out_fp32 == 0) or FP32. */
