@@ -69,6 +69,33 @@ __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
     return (lo + up) | sign;
 }
 
+// Eight FP32 values -> eight E2M1 codes (element i in nibble i) with the
+// hardware conversion cvt.rn.satfinite.e2m1x2.f32, which rounds to nearest-even
+// and saturates at +-6 (its first source goes to the upper nibble). The sign
+// bits of the inputs are OR-ed in afterwards so that values rounding to zero
+// keep their sign whatever the instruction does with negative zero.
+__device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(out)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    uint32_t signs = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) signs |= (__float_as_uint(v[i]) >> (28 - 4 * i)) & (8u << (4 * i));
+    return out | signs;
+}
+
+// Number of zero-magnitude codes among the 8 nibbles of a code word.
+__device__ __forceinline__ uint32_t zero_mag_count8(uint32_t w) {
+    const uint32_t t = w & 0x77777777u;
+    return 8u - (uint32_t)__popc((t | (t >> 1) | (t >> 2)) & 0x11111111u);
+}
+
 // Count of values that saturate (|v| > 6 before rounding).
 __device__ __forceinline__ uint32_t e2m1_saturates(float v) { return fabsf(v) > 6.0f ? 1u : 0u; }
 

@@ -8,12 +8,14 @@
 // power-of-two scales (section A3, App. B.4); plus the UE5M3 block scales and
 // held-amax tensor scaling of the UE5M3 pretraining paper (arXiv 2609.02846).
 //
-// Data movement: 128-bit coalesced BF16 loads; each thread owns whole 16-element
-// blocks (rowwise: 16 consecutive elements; colwise: 16 tokens of 8 channels),
-// so block amax, scale and rounding stay in registers. Codes are stored as
-// packed 64-bit nibble words; groups of four lanes whose scales are adjacent in
-// the tensor-core layout merge them into one 32-bit store. Every kernel is a
-// grid-stride loop over a grid of a few CTAs per SM.
+// Data movement: coalesced 128-bit (rowwise) or 64-bit (colwise) BF16 loads;
+// each thread owns whole 16-element blocks (rowwise: 16 consecutive elements;
+// colwise: 16 tokens of 4 channels), so block amax, scale and rounding stay in
+// registers. RNE conversion uses the hardware E2M1 convert (two values per
+// instruction); event counts use bit tricks on the packed codes. Codes are
+// stored as packed 64-bit nibble words; groups of four lanes whose scales are
+// adjacent in the tensor-core layout merge them into one 32-bit store. Every
+// kernel is a grid-stride loop over a grid of a few CTAs per SM.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -126,49 +128,85 @@ struct Counts {
     uint32_t esat = 0, eunder = 0, ssat = 0, sunder = 0;
 };
 
-// Quantize one 1x16 block held in v[16] (App. B.2-B.3): block amax, scale in
-// the block format (RNE, satfinite), local encode scale, E2M1 codes packed into
-// two 32-bit words (element i in nibble i). `g0` is the SR group of element 0.
-template <int FMT, bool SR>
-__device__ __forceinline__ uint32_t quantize_block16(const float v[16], float s_enc, float s_dec, uint64_t g0,
-                                                     const QParams& q, uint32_t& lo, uint32_t& hi, Counts& cnt,
-                                                     bool count_scale) {
-    using F = ScaleFmt<FMT>;
-    float amax_b = 0.0f;
+// Sign bits of eight values placed at bit 3 of nibble i (the code's sign).
+__device__ __forceinline__ uint32_t sign_nibbles8(const float* v) {
+    uint32_t s = 0u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(v[i]));
+    for (int i = 0; i < 8; ++i) s |= (__float_as_uint(v[i]) >> (28 - 4 * i)) & (8u << (4 * i));
+    return s;
+}
+
+// Max |x| and the number of zeros (either sign) of 16 BF16 values held as 8
+// words, computed on the bit patterns (|x| of a BF16 orders like its low 15 bits).
+__device__ __forceinline__ float amax_bf16x16(const uint32_t w[8], uint32_t& nzero) {
+    uint32_t m = 0u, z = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t a = w[i] & 0x7FFF7FFFu;
+        m = __vmaxu2(m, a);
+        z += (uint32_t)__popc(__vcmpeq2(a, 0u));
+    }
+    nzero = z >> 4;
+    return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+}
+
+__device__ __forceinline__ float amax_f32x16(const float v[16], uint32_t& nzero) {
+    float m = 0.0f;
+    uint32_t z = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        m = fmaxf(m, fabsf(v[i]));
+        z += (__float_as_uint(v[i]) << 1) == 0u ? 1u : 0u;
+    }
+    nzero = z;
+    return m;
+}
+
+// Quantize one 1x16 block held in v[16] whose amax and zero count are known
+// (App. B.2-B.3): scale in the block format (RNE, satfinite), local encode
+// scale, E2M1 codes packed into two 32-bit words (element i in nibble i).
+// `g0` is the SR group of element 0. Event counts: scale saturation and
+// underflow (when count_scale); element saturation, counted per element only
+// when the scaled block amax exceeds 6 (rounding is monotone, so otherwise no
+// element can); element underflow = zero-magnitude codes minus zero inputs.
+template <int FMT, bool SR>
+__device__ __forceinline__ uint32_t quantize_block16(const float v[16], float amax_b, uint32_t nzero, float s_enc,
+                                                     float s_dec, uint64_t g0, const QParams& q, uint32_t& lo,
+                                                     uint32_t& hi, Counts& cnt, bool count_scale) {
+    using F = ScaleFmt<FMT>;
     const float s = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
     const uint32_t sc = F::encode(s);
     if (count_scale) cnt.ssat += s > F::kMax ? 1u : 0u;
-    lo = hi = 0u;
     if (sc == 0u) {
         if (count_scale) cnt.sunder += amax_b > 0.0f ? 1u : 0u;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t code = (__float_as_uint(v[i]) >> 28) & 8u;
-            cnt.eunder += v[i] != 0.0f ? 1u : 0u;
-            if (i < 8) lo |= code << (4 * i);
-            else hi |= code << (4 * (i - 8));
-        }
+        cnt.eunder += 16u - nzero;
+        lo = sign_nibbles8(v);
+        hi = sign_nibbles8(v + 8);
         return 0u;
     }
     const float s_enc_l = __fdiv_rn(1.0f, __fmul_rn(F::decode(sc), s_dec));
-    uint4 r0 = make_uint4(0, 0, 0, 0), r1 = make_uint4(0, 0, 0, 0);
-    if (SR) {
-        r0 = sr_group_bits(g0, q.tensor_id, q.step_lo, q.key0, q.key1);
-        r1 = sr_group_bits(g0 + 1, q.tensor_id, q.step_lo, q.key0, q.key1);
-    }
+    float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float val = __fmul_rn(v[i], s_enc_l);
-        cnt.esat += e2m1_saturates(val);
-        uint32_t code;
-        if (SR) code = e2m1_sr(val, sr_half(i < 8 ? r0 : r1, i & 7));
-        else code = e2m1_rne(val);
-        cnt.eunder += (v[i] != 0.0f && (code & 7u) == 0u) ? 1u : 0u;
-        if (i < 8) lo |= code << (4 * i);
-        else hi |= code << (4 * (i - 8));
+    for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(v[i], s_enc_l);
+    if (__fmul_rn(amax_b, s_enc_l) > 6.0f) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[i]);
     }
+    if (SR) {
+        const uint4 r0 = sr_group_bits(g0, q.tensor_id, q.step_lo, q.key0, q.key1);
+        const uint4 r1 = sr_group_bits(g0 + 1, q.tensor_id, q.step_lo, q.key0, q.key1);
+        lo = hi = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t code = e2m1_sr(x[i], sr_half(i < 8 ? r0 : r1, i & 7));
+            if (i < 8) lo |= code << (4 * i);
+            else hi |= code << (4 * (i - 8));
+        }
+    } else {
+        lo = e2m1_rne_x8(x);
+        hi = e2m1_rne_x8(x + 8);
+    }
+    cnt.eunder += zero_mag_count8(lo) + zero_mag_count8(hi) - nzero;
     return sc;
 }
 
@@ -204,26 +242,26 @@ __global__ void __launch_bounds__(kThreads) amax_plain_kernel(const uint4* __res
     if (threadIdx.x == 0) partials[blockIdx.x] = f;
 }
 
-// amax in the rotated space (App. C): each thread transforms 16 tokens of 8
-// channels (sixteen 128-bit loads) and keeps the max magnitude.
+// amax in the rotated space (App. C): each thread transforms 16 tokens of 4
+// channels (sixteen 64-bit loads) and keeps the max magnitude.
 __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ in, int64_t T,
                                                                  int64_t C, uint32_t key0, uint32_t key1,
                                                                  float* __restrict__ partials) {
     const uint32_t signs = rht_sign_word(key0, key1);
-    const int64_t ug = C / 8, uj = T / 16, units = ug * uj;
+    const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     float m = 0.0f;
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
         const int64_t g = u % ug, j = u / ug;
-        uint4 x[16];
+        uint2 x[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) x[t] = ldg16(in + (16 * j + t) * C + 8 * g);
+        for (int t = 0; t < 16; ++t) x[t] = __ldg(reinterpret_cast<const uint2*>(in + (16 * j + t) * C + 4 * g));
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
             float v[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                const uint32_t w = ch < 2 ? x[t].x : ch < 4 ? x[t].y : ch < 6 ? x[t].z : x[t].w;
+                const uint32_t w = ch < 2 ? x[t].x : x[t].y;
                 v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
             }
             rht16(v, signs);
@@ -255,10 +293,13 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
         uint32_t sc = 0u;
         if (active) {
             const uint4 a = ldg16(q.in + 16 * b), c = ldg16(q.in + 16 * b + 8);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+            uint32_t nzero;
+            const float amax_b = amax_bf16x16(w, nzero);
             float v[16];
             unpack16(a, c, v);
             uint32_t lo, hi;
-            sc = quantize_block16<FMT, SR>(v, s_enc, s_dec, (uint64_t)(2 * b), q, lo, hi, cnt, true);
+            sc = quantize_block16<FMT, SR>(v, amax_b, nzero, s_enc, s_dec, (uint64_t)(2 * b), q, lo, hi, cnt, true);
             *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
         }
         if (TCL) {
@@ -280,16 +321,17 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
 // ----------------------------------------------------------------------------
 // K3: colwise 1x16 quantizer with optional fused RHT16 (Wgrad operands X^T and
 // dY^T, section 4.2-4.3). The operand is the input's transpose: operand row c
-// (a channel) holds tokens along the dot dimension. A warp covers 4 token tiles
-// x 8 channel groups (64 tokens x 64 channels): lane = 4 * channel_group + tile,
-// so the four lanes of a channel group write 32 contiguous code bytes and four
-// adjacent scale bytes.
+// (a channel) holds tokens along the dot dimension. Each thread owns 16 tokens
+// of 4 channels (sixteen 64-bit loads); a warp covers 4 token tiles x 8 channel
+// groups (64 tokens x 32 channels), lane = 4 * channel_group + tile, so the
+// four lanes of a channel write 32 contiguous code bytes and four adjacent
+// scale bytes.
 template <int FMT, bool SR, bool RHT, bool TCL>
 __global__ void __launch_bounds__(kThreads) quantize_cols_kernel(QParams q) {
     float s_enc, s_dec;
     if (!cta_tensor_scale(q, s_enc, s_dec)) return;
     const int64_t T = q.rows, C = q.cols;
-    const int64_t ug = C / 8, uj = T / 16;
+    const int64_t ug = C / 4, uj = T / 16;
     const int64_t wg_count = (ug + 7) / 8, wj_count = (uj + 3) / 4;
     const int64_t wunits = wg_count * wj_count;
     const int lane = threadIdx.x & 31;
@@ -301,24 +343,26 @@ __global__ void __launch_bounds__(kThreads) quantize_cols_kernel(QParams q) {
         const int64_t g = (wu % wg_count) * 8 + (lane >> 2);
         const int64_t j = (wu / wg_count) * 4 + (lane & 3);
         const bool active = g < ug && j < uj;
-        uint4 x[16];
+        uint2 x[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-            x[t] = active ? ldg16(q.in + (16 * j + t) * C + 8 * g) : make_uint4(0, 0, 0, 0);
+            x[t] = active ? __ldg(reinterpret_cast<const uint2*>(q.in + (16 * j + t) * C + 4 * g)) : make_uint2(0, 0);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
             float v[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                const uint32_t w = ch < 2 ? x[t].x : ch < 4 ? x[t].y : ch < 6 ? x[t].z : x[t].w;
+                const uint32_t w = ch < 2 ? x[t].x : x[t].y;
                 v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
             }
             if (RHT) rht16(v, signs);
-            const int64_t c = 8 * g + ch;
+            const int64_t c = 4 * g + ch;
             uint32_t lo = 0u, hi = 0u, sc = 0u;
             if (active) {
-                sc = quantize_block16<FMT, SR>(v, s_enc, s_dec, (uint64_t)((c * T + 16 * j) >> 3), q, lo, hi, cnt,
-                                              true);
+                uint32_t nzero;
+                const float amax_b = amax_f32x16(v, nzero);
+                sc = quantize_block16<FMT, SR>(v, amax_b, nzero, s_enc, s_dec, (uint64_t)((c * T + 16 * j) >> 3), q,
+                                              lo, hi, cnt, true);
                 *reinterpret_cast<uint2*>(q.codes + c * (T / 2) + 8 * j) = make_uint2(lo, hi);
             }
             if (TCL) {
@@ -380,26 +424,26 @@ __global__ void __launch_bounds__(kThreads) quantize_2d_kernel(QParams q) {
             cnt.sunder += (sc == 0u && amax_t > 0.0f) ? 1u : 0u;
         }
         uint32_t lo = 0u, hi = 0u;
-        if (sc == 0u) {
+        uint32_t nzero = 0u;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const uint32_t code = (__float_as_uint(v[e]) >> 28) & 8u;
-                if (active) cnt.eunder += v[e] != 0.0f ? 1u : 0u;
-                if (e < 8) lo |= code << (4 * e);
-                else hi |= code << (4 * (e - 8));
-            }
+        for (int e = 0; e < 16; ++e) nzero += (__float_as_uint(v[e]) << 1) == 0u ? 1u : 0u;
+        if (sc == 0u) {
+            lo = sign_nibbles8(v);
+            hi = sign_nibbles8(v + 8);
+            if (active) cnt.eunder += 16u - nzero;
         } else {
             const float s_enc_l = __fdiv_rn(1.0f, __fmul_rn(F::decode(sc), s_dec));
+            float x[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float val = __fmul_rn(v[e], s_enc_l);
-                const uint32_t code = e2m1_rne(val);
-                if (active) {
-                    cnt.esat += e2m1_saturates(val);
-                    cnt.eunder += (v[e] != 0.0f && (code & 7u) == 0u) ? 1u : 0u;
+            for (int e = 0; e < 16; ++e) x[e] = __fmul_rn(v[e], s_enc_l);
+            lo = e2m1_rne_x8(x);
+            hi = e2m1_rne_x8(x + 8);
+            if (active) {
+                if (__fmul_rn(amax_t, s_enc_l) > 6.0f) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) cnt.esat += e2m1_saturates(x[e]);
                 }
-                if (e < 8) lo |= code << (4 * e);
-                else hi |= code << (4 * (e - 8));
+                cnt.eunder += zero_mag_count8(lo) + zero_mag_count8(hi) - nzero;
             }
         }
         if (q.codes != nullptr && active) {
@@ -463,15 +507,22 @@ __global__ void __launch_bounds__(kThreads) quantize_mx_rows_kernel(QParams q) {
             }
             sc = (uint32_t)(ex + 127);
             const float inv = exp2_exact(-ex);
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            float x[32];
+            uint32_t nzero = 0u;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float val = __fmul_rn(v[e], inv);
-                const uint32_t code = e2m1_rne(val);
-                cnt.esat += e2m1_saturates(val);
-                cnt.eunder += (v[e] != 0.0f && (code & 7u) == 0u) ? 1u : 0u;
-                w[e >> 3] |= code << (4 * (e & 7));
+                x[e] = __fmul_rn(v[e], inv);
+                nzero += (__float_as_uint(v[e]) << 1) == 0u ? 1u : 0u;
             }
+            if (__fmul_rn(amax_b, inv) > 6.0f) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) cnt.esat += e2m1_saturates(x[e]);
+            }
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = e2m1_rne_x8(x + 8 * k);
+            cnt.eunder += zero_mag_count8(w[0]) + zero_mag_count8(w[1]) + zero_mag_count8(w[2]) +
+                          zero_mag_count8(w[3]) - nzero;
             *reinterpret_cast<uint4*>(q.codes + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         if (TCL) {
@@ -585,8 +636,8 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
         }
         return cudaGetLastError();
     }
-    const int64_t wunits = ((j.cols / 8 + 7) / 8) * ((j.rows / 16 + 3) / 4);
-    const int grid = grid_for(wunits * 32, 4);
+    const int64_t wunits = ((j.cols / 4 + 7) / 8) * ((j.rows / 16 + 3) / 4);
+    const int grid = grid_for(wunits * 32, 8);
 #define FP4_COLS(SR, RHT, TCL) quantize_cols_kernel<FMT, SR, RHT, TCL><<<grid, kThreads, 0, st>>>(q)
     if (j.sr) {
         if (j.rht) { if (tcl) FP4_COLS(true, true, true); else FP4_COLS(true, true, false); }
@@ -601,8 +652,8 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
 
 int amax_grid(const QuantJob& j) {
     if (j.rht) {
-        const int64_t units = (j.cols / 8) * (j.rows / 16);
-        int g = grid_for(units, 4);
+        const int64_t units = (j.cols / 4) * (j.rows / 16);
+        int g = grid_for(units, 8);
         return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
     }
     const int64_t nvec = j.rows * j.cols / 8;

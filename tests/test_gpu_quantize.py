@@ -183,3 +183,28 @@ def test_validation_errors_launch_nothing():
     with pytest.raises(fb.Fp4Error) as e:
         fb.fp4_quantize(fb.QuantConfig(), to_gpu_bf16(random_bf16(21, (128, 48), "normal")), bad, ws=new_ws())
     assert e.value.status == fb._lib.FP4_ERR_SHAPE                      # 48/16 = 3 blocks: not a multiple of 4
+
+
+def test_e2m1_conversion_exhaustive_over_bf16_magnitudes():
+    """Every BF16 value in [-6, 6] (both zeros and every tie point included)
+    reaches the E2M1 conversion unscaled: one block holds 2688 = 6 * 448, so
+    s_enc,G = 1, and every other block's first element is 6, so its E4M3
+    scale is exactly 1 and v = x. Codes must equal the oracle's."""
+    pos = np.arange(0, 0x40C1, dtype=np.uint16)                  # +0 .. +6.0
+    vals = np.concatenate([pos, pos | 0x8000])                   # and their negatives (incl. -0)
+    per_block = 15
+    nblk = -(-vals.size // per_block)
+    body = np.zeros(nblk * per_block, dtype=np.uint16)
+    body[:vals.size] = vals
+    blocks = body.reshape(nblk, per_block)
+    six = np.full((nblk, 1), 0x40C0, dtype=np.uint16)            # 6.0
+    bits = np.concatenate([six, blocks], axis=1)
+    head = np.zeros((1, 16), dtype=np.uint16)
+    head[0, 0] = f32_to_bf16_bits(np.array([2688.0], np.float32))[0]
+    bits = np.ascontiguousarray(np.concatenate([head, bits], axis=0))
+    for rnd in (fb.FP4_ROUND_RNE, fb.FP4_ROUND_SR):
+        cfg = fb.QuantConfig(layout=PLAIN, round=rnd, seed=5, tensor_id=2)
+        out, _, cnt = gpu_quantize(cfg, bits)
+        ref = oracle_quantize(cfg, bits)
+        assert ref["s_dec"] == 1.0
+        assert_quant_equal(out, ref, PLAIN, cnt)
