@@ -12,10 +12,15 @@
 //   warp 0      : TMA producer -- A/B code tiles (128-byte swizzled rows of 256
 //                 FP4 values) and the tiles' scale chunks (1-D bulk copies) into
 //                 a STAGES-deep shared-memory ring guarded by mbarriers;
+//   warp 6      : one lane copies each stage's scale chunks into tensor memory
+//                 (eight tcgen05.cp.32x128b.warpx4) and commits them to a
+//                 per-stage barrier;
 //   warp 1      : allocates tensor memory and one lane issues, per stage, four
-//                 tcgen05.cp scale copies per operand into tensor memory and four
 //                 tcgen05.mma kind::mxf4nvf4 (K = 64 each), then commits the
-//                 stage back to the producer;
+//                 stage back to the producer. Measured on GB300, a single thread
+//                 issuing the scale copies as well spent ~90 % of its time issuing
+//                 and left the tensor pipe ~80 % idle, so the copies live on their
+//                 own warp;
 //   warps 2-5   : epilogue -- tcgen05.ld the FP32 accumulator (each warp owns
 //                 its 32-lane quadrant), scale by alpha, store BF16 / FP32.
 // K is accumulated in chunks of 1024 values (CHUNK_STAGES stages): each chunk
@@ -75,10 +80,10 @@ struct NvCfg {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 224;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -95,6 +100,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     auto accf_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + a); };
     auto acce_bar = [&](int a) { return sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + Cfg::NUM_ACC + a); };
     const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + 2 * Cfg::NUM_ACC);
+    auto sf_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + 2 * Cfg::NUM_ACC + 1 + s); };
+    const uint32_t sf_drain_bar = sb + Cfg::OFF_BAR + 8u * (3 * Cfg::STAGES + 2 * Cfg::NUM_ACC + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
 
     const int64_t num_m = p.M / Cfg::BM, num_n = p.N / Cfg::BN, tiles = num_m * num_n;
@@ -111,6 +118,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc::mbar_init(acce_bar(a), 4);
         }
         tc::mbar_init(drain_bar, 1);
+        for (int s = 0; s < Cfg::STAGES; ++s) tc::mbar_init(sf_bar(s), 1);
+        tc::mbar_init(sf_drain_bar, 1);
         tc::mbar_init_fence();
         tc::prefetch_tmap(&tmap_a);
         tc::prefetch_tmap(&tmap_b);
@@ -176,7 +185,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     const int s = (int)(it % Cfg::STAGES);
                     const uint32_t ph = (it / Cfg::STAGES) & 1u;
-                    if (!tc::mbar_wait(full_bar(s), ph, p.status)) {
+                    // the scale warp's barrier completes after the stage's data
+                    // landed (it waited on the full barrier) and its scale
+                    // copies into tensor memory finished
+                    if (!tc::mbar_wait(full_bar(s), ph, p.status) || !tc::mbar_wait(sf_bar(s), ph, p.status)) {
                         ok = false;
                         break;
                     }
@@ -185,16 +197,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t sfb_t = sfa_t + Cfg::SF_COLS_A;
                     const uint32_t a_s = sb + Cfg::OFF_A + s * Cfg::A_BYTES;
                     const uint32_t b_s = sb + Cfg::OFF_B + s * Cfg::B_BYTES;
-                    const uint32_t sfa_s = sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
-                    const uint32_t sfb_s = sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        tc::cp_32x128b_warpx4(sfa_t + 4 * kk, tc::scale_chunk_desc(sfa_s + 512 * kk));
-#pragma unroll
-                        for (int h = 0; h < Cfg::BN / 128; ++h)
-                            tc::cp_32x128b_warpx4(sfb_t + (Cfg::BN / 32) * kk + 4 * h,
-                                                  tc::scale_chunk_desc(sfb_s + 2048 * h + 512 * kk));
-                    }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         tc::mma_mxf4nvf4(d_tmem, tc::kmajor_sw128_desc(a_s + 32 * kk),
@@ -212,6 +214,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // tensor memory is released
             tc::commit(drain_bar);
             tc::mbar_wait(drain_bar, 0, p.status);
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ scale copies
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < num_k; ++kb, ++it) {
+                    const int s = (int)(it % Cfg::STAGES);
+                    const uint32_t ph = (it / Cfg::STAGES) & 1u;
+                    // a stage's scale columns are reused only after the producer
+                    // refilled the stage, i.e. after the MMAs that read them retired
+                    if (!tc::mbar_wait(full_bar(s), ph, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t sfa_t = tmem + (uint32_t)(Cfg::SF_TMEM_BASE + s * Cfg::SF_COLS_STAGE);
+                    const uint32_t sfb_t = sfa_t + Cfg::SF_COLS_A;
+                    const uint32_t sfa_s = sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
+                    const uint32_t sfb_s = sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        tc::cp_32x128b_warpx4(sfa_t + 4 * kk, tc::scale_chunk_desc(sfa_s + 512 * kk));
+#pragma unroll
+                        for (int h = 0; h < Cfg::BN / 128; ++h)
+                            tc::cp_32x128b_warpx4(sfb_t + (Cfg::BN / 32) * kk + 4 * h,
+                                                  tc::scale_chunk_desc(sfb_s + 2048 * h + 512 * kk));
+                    }
+                    tc::commit(sf_bar(s));
+                }
+            }
+            // every copy this thread issued retires before tensor memory is released
+            tc::commit(sf_drain_bar);
+            tc::mbar_wait(sf_drain_bar, 0, p.status);
         }
     } else {
         // ------------------------------------------------------------ epilogue
