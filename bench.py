@@ -2,9 +2,10 @@
 
 One step = the whole hot path over one batch of the 1.2B Transformer FFN
 workload (T = 8192 tokens; linears 2048 -> 6144 and 6144 -> 2048): for each
-linear, five quantizations (X rowwise, X^T colwise + RHT16, W 16x16 in both
-orientations, dY rowwise SR, dY^T colwise + RHT16 + SR; each with its tensor
-amax pass) and the three block-scaled NVFP4 GEMMs (Fprop, Dgrad, Wgrad).
+linear, the five quantized operands (X rowwise and X^T colwise + RHT16 from one
+pass over X, W 16x16 in both orientations, dY rowwise SR and dY^T colwise +
+RHT16 + SR from one pass over dY; each pass preceded by its tensor-amax pass)
+and the three block-scaled NVFP4 GEMMs (Fprop, Dgrad, Wgrad).
 
 `value` is fwd+bwd GEMM TFLOP/s of the whole step (6 T N K per linear divided
 by the step time, quantization included) with inputs resident in HBM; `e2e`
@@ -31,11 +32,11 @@ METRIC = "FP4 linear fwd+bwd TFLOP/s; quantize GB/s (% of FP4/HBM roofline)"
 # Nominal dense-rate ratio FP4 : BF16 on GB300 (13.5 : 2.25 PFLOP/s).
 FP4_OVER_BF16 = 6.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Algorithmic bytes per element of each quantization (BF16 in, E2M1 + 8-bit
-# scale out; current scaling reads the input twice): 2 * 2 + 1/2 + 1/16, and
-# for 16x16 weights emitting both orientations 2 * 2 + 2 * (1/2 + 1/16).
-BYTES_1x16_CURRENT = 4.5625
-BYTES_2D_BOTH = 5.125
+# Algorithmic bytes per input element of the step's quantizations, current
+# scaling (one amax pass and one conversion pass over the BF16 input, E2M1 codes
+# plus one 8-bit scale per 16 values written per operand): X and dY each yield a
+# rowwise and a colwise operand, W yields W and W^T -- all 2 * 2 + 2 * (1/2 + 1/16).
+BYTES_TWO_OPERANDS = 5.125
 
 
 def load_peaks():
@@ -231,9 +232,9 @@ def run_gpu(args, workload):
                      for k, v in inp.items()})
 
     gemm_flops = sum(3 * 2.0 * lin.tokens * lin.k_in * lin.n_out for lin, *_ in layers)
-    quant_bytes = sum(BYTES_1x16_CURRENT * 2 * lin.tokens * (lin.k_in + lin.n_out)
-                      + BYTES_2D_BOTH * lin.n_out * lin.k_in for lin, *_ in layers)
-    launches_per_step = sum(10 + 3 for _ in layers)   # 5 x (amax + quantize) + 3 GEMMs per linear
+    quant_bytes = sum(BYTES_TWO_OPERANDS * (lin.tokens * (lin.k_in + lin.n_out) + lin.n_out * lin.k_in)
+                      for lin, *_ in layers)
+    launches_per_step = sum(6 + 3 for _ in layers)   # 3 x (amax + quantize) + 3 GEMMs per linear
 
     def step(ev=None):
         for lin, L, di, o in layers:
@@ -321,7 +322,7 @@ def run_gpu(args, workload):
                  "kernel": "gemm_nvfp4_kernel (6 launches per step)"}
     quant_roof = {"bound": "hbm", "achieved": quant_gbs, "peak": hbm_peak, "unit": "GB/s",
                   "frac": quant_gbs / hbm_peak, "traffic": traffic.get("quantize"),
-                  "peak_source": f"{src} hbm_gbs", "kernel": "amax + quantize kernels (20 launches per step)"}
+                  "peak_source": f"{src} hbm_gbs", "kernel": "amax + quantize kernels (12 launches per step)"}
     dominant, other = (gemm_roof, quant_roof) if g_ms >= q_ms else (quant_roof, gemm_roof)
     cpu = cpu_baseline_entry(workload, args.ref_tokens, args.ref_feats) if not args.no_cpu_baseline else None
     lin_desc = [[l.k_in, l.n_out] for l in workload.linears]

@@ -22,7 +22,7 @@ from ._lib import (FP4_BLOCK_1x16, FP4_BLOCK_1x32, FP4_BLOCK_16x16, FP4_LAYOUT_P
                    FP4_ORIENT_COLWISE, FP4_ORIENT_ROWWISE, FP4_ROUND_RNE, FP4_ROUND_SR, FP4_SCALE_E4M3,
                    FP4_SCALE_UE5M3, FP4_SCALE_UE8M0, FP4_TSCALE_CURRENT, FP4_TSCALE_HELD, Fp4Error)
 
-__all__ = ["QTensor", "QuantConfig", "AmaxState", "fp4_quantize", "fp4_dequantize", "fp4_gemm",
+__all__ = ["QTensor", "QuantConfig", "AmaxState", "fp4_quantize", "fp4_quantize_dual", "fp4_dequantize", "fp4_gemm",
            "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
            "fp4_workspace_bytes", "fp4_quantized_sizes", "Fp4Error", "Fp4Linear"]
 
@@ -135,6 +135,23 @@ def fp4_quantize(cfg: QuantConfig, x: torch.Tensor, out: QTensor, out_t: QTensor
     _lib.check(st, "fp4_quantize")
 
 
+def fp4_quantize_dual(cfg_row: QuantConfig, cfg_col: QuantConfig, x: torch.Tensor, out_row: QTensor,
+                      out_col: QTensor, state_row: AmaxState | None = None, state_col: AmaxState | None = None,
+                      counters_row: torch.Tensor | None = None, counters_col: torch.Tensor | None = None,
+                      ws: torch.Tensor | None = None, stream=None) -> None:
+    """Rowwise and colwise quantization of `x` in one pass (see fp4_quantize_dual in fp4bs.h)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    pr, pc = cfg_row.params(), cfg_col.params()
+    dr, dc = out_row.desc(), out_col.desc()
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    st = _lib.load().fp4_quantize_dual(ctypes.byref(pr), ctypes.byref(pc), _ptr(x), x.shape[0], x.shape[1],
+                                       ctypes.byref(dr), ctypes.byref(dc),
+                                       _ptr(state_row.buf) if state_row is not None else None,
+                                       _ptr(state_col.buf) if state_col is not None else None,
+                                       _ptr(counters_row), _ptr(counters_col), _ptr(ws), ws_bytes, _stream(stream))
+    _lib.check(st, "fp4_quantize_dual")
+
+
 def fp4_dequantize(t: QTensor, out: torch.Tensor, stream=None) -> None:
     assert out.is_contiguous() and out.dtype in (torch.float32, torch.bfloat16)
     d = t.desc()
@@ -207,7 +224,7 @@ class Fp4Linear:
             "dyt": QTensor.empty(N, T, f, device=dev),      # dY^T colwise   (Wgrad A)
             "xt": QTensor.empty(K, T, f, device=dev),       # X^T colwise    (Wgrad B)
         }
-        self.ws = torch.empty(fp4_workspace_bytes(QuantConfig(), 1, 1) // 4 + 4, dtype=torch.float32,
+        self.ws = torch.empty(2 * fp4_workspace_bytes(QuantConfig(), 1, 1) // 4 + 4, dtype=torch.float32,
                               device=dev)
         self.counters = torch.zeros((5, 4), dtype=torch.int64, device=dev)
         self.states = [AmaxState(dev) for _ in range(5)] if self.held else [None] * 5
@@ -220,18 +237,33 @@ class Fp4Linear:
         return QuantConfig(**base)
 
     def quantize_all(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor, step: int = 0, stream=None):
+        """X -> X (rowwise) and X^T (colwise + RHT) in one pass; W -> W and W^T
+        (16x16); dY -> dY (rowwise, SR) and dY^T (colwise + RHT, SR) in one pass.
+        Falls back to separate calls for shapes the one-pass kernel does not take."""
         b, c = self.bufs, self.counters
         rht = self.rht
-        fp4_quantize(self._cfg(0, step), x, b["x"], state=self.states[0], counters=c[0], ws=self.ws,
-                     stream=stream)
+        dual_ok = self.tokens % 128 == 0 and self.k_in % 128 == 0 and self.n_out % 128 == 0
+        if dual_ok:
+            fp4_quantize_dual(self._cfg(0, step), self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x,
+                              b["x"], b["xt"], self.states[0], self.states[1], c[0], c[1], ws=self.ws,
+                              stream=stream)
+        else:
+            fp4_quantize(self._cfg(0, step), x, b["x"], state=self.states[0], counters=c[0], ws=self.ws,
+                         stream=stream)
+            fp4_quantize(self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x, b["xt"], state=self.states[1],
+                         counters=c[1], ws=self.ws, stream=stream)
         fp4_quantize(self._cfg(2, step, block=FP4_BLOCK_16x16, emit_transpose=True), w, b["w"], b["wt"],
                      state=self.states[2], counters=c[2], ws=self.ws, stream=stream)
-        fp4_quantize(self._cfg(3, step, round=FP4_ROUND_SR), dy, b["dy"], state=self.states[3], counters=c[3],
-                     ws=self.ws, stream=stream)
-        fp4_quantize(self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x, b["xt"], state=self.states[1],
-                     counters=c[1], ws=self.ws, stream=stream)
-        fp4_quantize(self._cfg(4, step, orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR), dy, b["dyt"],
-                     state=self.states[4], counters=c[4], ws=self.ws, stream=stream)
+        if dual_ok:
+            fp4_quantize_dual(self._cfg(3, step, round=FP4_ROUND_SR),
+                              self._cfg(4, step, orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR), dy,
+                              b["dy"], b["dyt"], self.states[3], self.states[4], c[3], c[4], ws=self.ws,
+                              stream=stream)
+        else:
+            fp4_quantize(self._cfg(3, step, round=FP4_ROUND_SR), dy, b["dy"], state=self.states[3], counters=c[3],
+                         ws=self.ws, stream=stream)
+            fp4_quantize(self._cfg(4, step, orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR), dy, b["dyt"],
+                         state=self.states[4], counters=c[4], ws=self.ws, stream=stream)
 
     def gemms(self, y: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor, stream=None):
         b = self.bufs

@@ -34,7 +34,7 @@ FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05 = 0, 1
 
 EXPORTED = ["fp4_quantized_sizes", "fp4_workspace_bytes", "fp4_quantize", "fp4_dequantize", "fp4_gemm",
             "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
-            "fp4_status_string", "fp4_abi_version", "fp4_quantize_noalloc"]
+            "fp4_status_string", "fp4_abi_version", "fp4_quantize_noalloc", "fp4_quantize_dual"]
 
 
 class fp4_quant_params_t(ctypes.Structure):
@@ -81,6 +81,8 @@ def load() -> ctypes.CDLL:
             L.fp4_workspace_bytes.restype = sz
             L.fp4_quantize.argtypes = [QP, P, i64, i64, TP, TP, P, P, P, sz, P]
             L.fp4_quantize.restype = i32
+            L.fp4_quantize_dual.argtypes = [QP, QP, P, i64, i64, TP, TP, P, P, P, P, P, sz, P]
+            L.fp4_quantize_dual.restype = i32
             L.fp4_quantize_noalloc.argtypes = [QP, P, i64, i64, TP, TP, P, P, P]
             L.fp4_quantize_noalloc.restype = i32
             L.fp4_dequantize.argtypes = [TP, P, i32, P]

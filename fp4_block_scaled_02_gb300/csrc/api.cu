@@ -270,6 +270,34 @@ fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf
     return from_cuda(launch_quantize(job, static_cast<cudaStream_t>(stream)));
 }
 
+fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
+                               int64_t rows, int64_t cols, const fp4_tensor_t* out_row, const fp4_tensor_t* out_col,
+                               fp4_amax_state_t* state_row, fp4_amax_state_t* state_col, uint64_t* counters_row,
+                               uint64_t* counters_col, void* ws, size_t ws_bytes, void* stream) {
+    if (p_row == nullptr || p_col == nullptr) return FP4_ERR_INVALID_ARG;
+    if (p_row->orient != FP4_ORIENT_ROWWISE || p_col->orient != FP4_ORIENT_COLWISE) return FP4_ERR_INVALID_ARG;
+    if (p_row->block != FP4_BLOCK_1x16 || p_col->block != FP4_BLOCK_1x16) return FP4_ERR_UNSUPPORTED;
+    if (p_row->scale_fmt != p_col->scale_fmt || p_row->scale_fmt == FP4_SCALE_UE8M0) return FP4_ERR_UNSUPPORTED;
+    if (p_row->round != p_col->round || p_row->tscale != p_col->tscale) return FP4_ERR_UNSUPPORTED;
+    if (p_row->tscale == FP4_TSCALE_HELD && p_row->refresh_every != p_col->refresh_every) return FP4_ERR_UNSUPPORTED;
+    if (p_row->step != p_col->step) return FP4_ERR_UNSUPPORTED;
+    if (p_row->scale_layout != FP4_LAYOUT_TCGEN05 || p_col->scale_layout != FP4_LAYOUT_TCGEN05)
+        return FP4_ERR_UNSUPPORTED;
+    if (rows % 128 != 0 || cols % 128 != 0) return FP4_ERR_SHAPE;
+    const size_t half = (size_t)kMaxAmaxPartials * sizeof(float);
+    if (ws == nullptr || ws_bytes < 2 * half) return FP4_ERR_WORKSPACE;
+    QuantJob jr, jc;
+    fp4_status_t s = check_quantize(p_row, in_bf16, rows, cols, out_row, nullptr, state_row, counters_row, ws, half, jr);
+    if (s != FP4_OK) return s;
+    s = check_quantize(p_col, in_bf16, rows, cols, out_col, nullptr, state_col, counters_col,
+                       static_cast<char*>(ws) + half, half, jc);
+    if (s != FP4_OK) return s;
+    if (rows == 0 || cols == 0) return FP4_OK;
+    jr.status = jc.status = device_status_ptr();
+    if (jr.status == nullptr) return FP4_ERR_CUDA;
+    return from_cuda(launch_quantize_dual(jr, jc, static_cast<cudaStream_t>(stream)));
+}
+
 fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void* stream) {
     if (t == nullptr || out == nullptr) return FP4_ERR_INVALID_ARG;
     if (t->rows == 0 || t->cols == 0) return FP4_OK;

@@ -53,20 +53,30 @@ __device__ __forceinline__ uint32_t e2m1_rne(float v) {
 }
 
 // Stochastic rounding (section 4.4) with a 16-bit uniform r16: |v| in
-// [lo, hi) rounds up iff r16 < frac * 2^16, frac = (|v| - lo) / (hi - lo),
-// which is exact in FP32 (|v| - lo by Sterbenz, hi - lo a power of two).
+// [lo, hi) rounds up iff r16 < frac * 2^16, frac = (|v| - lo) / (hi - lo).
+// The test is done exactly on the bit pattern of |v| = 2^e (1 + m):
+//   |v| in [1, 6): lo is |v| truncated to one mantissa bit (code 2 + 2e + that
+//     bit), hi - lo = 2^(e-1), so frac * 2^16 = (low 22 mantissa bits) / 2^6;
+//   |v| in [0.5, 1): lo = 0.5 (code 1), frac * 2^16 = (23 mantissa bits) / 2^7;
+//   |v| < 0.5: lo = 0 (code 0), frac * 2^16 = |v| * 2^17 (an exact scaling).
+// |v| >= 6 saturates to 6.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-    const float a = fabsf(v);
-    const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    if (a >= 6.0f) return 7u | sign;
-    const uint32_t lo = (uint32_t)(a >= 0.5f) + (uint32_t)(a >= 1.0f) + (uint32_t)(a >= 1.5f) +
-                        (uint32_t)(a >= 2.0f) + (uint32_t)(a >= 3.0f) + (uint32_t)(a >= 4.0f);
-    // lower neighbour value and reciprocal gap to the upper neighbour
-    const float flo = lo <= 4u ? 0.5f * (float)lo : (lo == 5u ? 3.0f : 4.0f);
-    const float inv_gap = lo <= 3u ? 2.0f : (lo <= 5u ? 1.0f : 0.5f);
-    const float frac = __fmul_rn(__fsub_rn(a, flo), inv_gap);
-    const uint32_t up = (float)r16 < __fmul_rn(frac, 65536.0f) ? 1u : 0u;
-    return (lo + up) | sign;
+    const uint32_t b = __float_as_uint(v);
+    const uint32_t sign = (b >> 28) & 8u;
+    const uint32_t a = b & 0x7FFFFFFFu;
+    if (a >= 0x40C00000u) return 7u | sign;
+    uint32_t code, up;
+    if (a >= 0x3F800000u) {
+        code = 2u + 2u * ((a >> 23) - 127u) + ((a >> 22) & 1u);
+        up = (r16 << 6) < (a & 0x3FFFFFu) ? 1u : 0u;
+    } else if (a >= 0x3F000000u) {
+        code = 1u;
+        up = (r16 << 7) < (a & 0x7FFFFFu) ? 1u : 0u;
+    } else {
+        code = 0u;
+        up = (float)r16 < __fmul_rn(__uint_as_float(a), 131072.0f) ? 1u : 0u;
+    }
+    return (code + up) | sign;
 }
 
 // Eight FP32 values -> eight E2M1 codes (element i in nibble i) with the

@@ -46,6 +46,10 @@ constexpr int kMaxAmaxPartials = 2048;
 
 int num_sms();
 cudaError_t launch_quantize(const QuantJob& job, cudaStream_t stream);
+// Rowwise (jr) and colwise (jc) quantization of the same input in one pass
+// (T % 128 == 0, C % 128 == 0, tensor-core scale layout, same format, rounding
+// and tensor-scale mode; each job's partials hold kMaxAmaxPartials floats).
+cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStream_t stream);
 // Number of amax partials the amax pass of `job` writes (0: no amax pass).
 int amax_partials_needed(const QuantJob& job);
 

@@ -588,6 +588,151 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __r
     }
 }
 
+// ----------------------------------------------------------------------------
+// K7: dual quantizer. One BF16 input X [T x C] yields both operands a linear
+// layer takes from it -- X rowwise (1x16 blocks along C, Fprop / Dgrad) and X^T
+// colwise (1x16 blocks along T, optional RHT16, Wgrad) -- from one read of X.
+// Each output is bit-identical to what its own quantize call would produce
+// (its own tensor scale, rounding mode, tensor id and counters).
+
+// Both amaxes from one read: plain max|x| for the rowwise operand and, with the
+// RHT, max|H x| over 16-token tiles for the colwise one. Each thread owns 16
+// tokens x 4 channels.
+template <bool RHT>
+__global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __restrict__ in, int64_t T, int64_t C,
+                                                             uint32_t key0, uint32_t key1,
+                                                             float* __restrict__ partials_row,
+                                                             float* __restrict__ partials_col) {
+    const uint32_t signs = RHT ? rht_sign_word(key0, key1) : 0u;
+    const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    uint32_t mr = 0u;
+    float mc = 0.0f;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const int64_t g = u % ug, j = u / ug;
+        uint2 x[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) x[t] = __ldg(reinterpret_cast<const uint2*>(in + (16 * j + t) * C + 4 * g));
+#pragma unroll
+        for (int t = 0; t < 16; ++t) mr = __vmaxu2(mr, __vmaxu2(x[t].x & 0x7FFF7FFFu, x[t].y & 0x7FFF7FFFu));
+        if (RHT) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float v[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint32_t w = ch < 2 ? x[t].x : x[t].y;
+                    v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
+                }
+                rht16(v, signs);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) mc = fmaxf(mc, fabsf(v[t]));
+            }
+        }
+    }
+    const float fr = cta_max(__uint_as_float(max(mr & 0xFFFFu, mr >> 16) << 16));
+    const float fc = RHT ? cta_max(mc) : fr;
+    if (threadIdx.x == 0) {
+        partials_row[blockIdx.x] = fr;
+        partials_col[blockIdx.x] = fc;
+    }
+}
+
+constexpr int kDualTT = 64;    // tokens per tile
+constexpr int kDualTC = 128;   // channels per tile
+
+// The conversion pass. A CTA stages a 64-token x 128-channel tile of X in
+// shared memory (the next tile's loads are in flight while this one is
+// converted); each thread then converts two rowwise blocks (16 consecutive
+// channels of one token, two 128-bit shared loads each) and one colwise pair
+// (16 tokens of two adjacent channels, sixteen 32-bit shared loads), so a warp
+// reads 32 consecutive channel pairs of one token row per load and never
+// conflicts on a bank. T % 128 == 0 and C % 128 == 0.
+template <int FMT, bool SR_ROW, bool SR_COL, bool RHT>
+__global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QParams qc) {
+    __shared__ __align__(16) uint16_t tile[kDualTT * kDualTC];
+    float se_r, sd_r, se_c, sd_c;
+    if (!cta_tensor_scale(qr, se_r, sd_r)) return;
+    __syncthreads();
+    if (!cta_tensor_scale(qc, se_c, sd_c)) return;
+    const int64_t T = qr.rows, C = qr.cols;
+    const int64_t tiles_c = C / kDualTC, ntiles = (T / kDualTT) * tiles_c;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t signs = RHT ? rht_sign_word(qc.key0, qc.key1) : 0u;
+    const int64_t nb_row = C / 16, nb_col = T / 16;
+    Counts cr, cc;
+    uint4 pre[4];
+    auto load_tile = [&](int64_t t) {
+        const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int q = tid + kThreads * i;  // 16-byte chunk q: row q / 16, chunk q % 16
+            pre[i] = ldg16(qr.in + (t0 + (q >> 4)) * C + c0 + 8 * (q & 15));
+        }
+    };
+    int64_t t = blockIdx.x;
+    if (t < ntiles) load_tile(t);
+    for (; t < ntiles; t += gridDim.x) {
+        __syncthreads();  // the previous tile's readers are done
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int q = tid + kThreads * i;
+            *reinterpret_cast<uint4*>(&tile[(q >> 4) * kDualTC + 8 * (q & 15)]) = pre[i];
+        }
+        __syncthreads();
+        if (t + gridDim.x < ntiles) load_tile(t + gridDim.x);
+        const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
+        // rowwise: blocks k = tid and tid + 256 of the tile's 64 x 8 blocks
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int k = tid + kThreads * i, r = k >> 3, b = k & 7;
+            const uint4 a = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b]);
+            const uint4 c = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b + 8]);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+            uint32_t nzero;
+            const float amax_b = amax_bf16x16(w, nzero);
+            float v[16];
+            unpack16(a, c, v);
+            const int64_t row = t0 + r, j = (c0 >> 4) + b, bg = row * nb_row + j;
+            uint32_t lo, hi;
+            const uint32_t sc =
+                quantize_block16<FMT, SR_ROW>(v, amax_b, nzero, se_r, sd_r, (uint64_t)(2 * bg), qr, lo, hi, cr, true);
+            *reinterpret_cast<uint2*>(qr.codes + 8 * bg) = make_uint2(lo, hi);
+            uint32_t ww = sc << (8 * (lane & 3));
+            ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 1);
+            ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 2);
+            if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(qr.scales + tc_scale_offset(row, j, nb_row)) = ww;
+        }
+        // colwise: channel pair cp, token block jb
+        {
+            const int cp = tid & 63, jb = tid >> 6;
+            float v0[16], v1[16];
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(16 * jb + tt) * kDualTC + 2 * cp]);
+                v0[tt] = bf16_lo(w);
+                v1[tt] = bf16_hi(w);
+            }
+            const int64_t jg = (t0 >> 4) + jb;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                float* v = ch ? v1 : v0;
+                if (RHT) rht16(v, signs);
+                uint32_t nzero;
+                const float amax_b = amax_f32x16(v, nzero);
+                const int64_t c = c0 + 2 * cp + ch;
+                uint32_t lo, hi;
+                const uint32_t sc = quantize_block16<FMT, SR_COL>(v, amax_b, nzero, se_c, sd_c,
+                                                                  (uint64_t)((c * T + 16 * jg) >> 3), qc, lo, hi, cc, true);
+                *reinterpret_cast<uint2*>(qc.codes + c * (T / 2) + 8 * jg) = make_uint2(lo, hi);
+                qc.scales[tc_scale_offset(c, jg, nb_col)] = (uint8_t)sc;
+            }
+        }
+    }
+    flush_counters(qr.counters, cr.esat, cr.eunder, cr.ssat, cr.sunder);
+    flush_counters(qc.counters, cc.esat, cc.eunder, cc.ssat, cc.sunder);
+}
+
 int grid_for(int64_t threads_wanted, int per_sm) {
     const int64_t want = (threads_wanted + kThreads - 1) / kThreads;
     const int64_t cap = (int64_t)num_sms() * per_sm;
@@ -661,16 +806,7 @@ int amax_grid(const QuantJob& j) {
     return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
 }
 
-}  // namespace
-
-int amax_partials_needed(const QuantJob& j) {
-    if (j.scale_fmt == kFmtUE8M0) return 0;
-    if (j.held && !j.refresh) return 0;
-    if (j.rows == 0 || j.cols == 0) return 0;
-    return amax_grid(j);
-}
-
-cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
+QParams make_params(const QuantJob& j) {
     QParams q{};
     q.in = j.in;
     q.rows = j.rows;
@@ -693,6 +829,20 @@ cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
     q.key0 = (uint32_t)j.seed;
     q.key1 = (uint32_t)(j.seed >> 32);
     q.status = j.status;
+    return q;
+}
+
+}  // namespace
+
+int amax_partials_needed(const QuantJob& j) {
+    if (j.scale_fmt == kFmtUE8M0) return 0;
+    if (j.held && !j.refresh) return 0;
+    if (j.rows == 0 || j.cols == 0) return 0;
+    return amax_grid(j);
+}
+
+cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
+    QParams q = make_params(j);
     if (j.rows == 0 || j.cols == 0) return cudaSuccess;
 
     if (j.scale_fmt == kFmtUE8M0) {
@@ -734,6 +884,43 @@ cudaError_t launch_dequantize(const DequantJob& j, cudaStream_t st) {
     else if (j.scale_fmt == kFmtUE5M3) FP4_DQ(kFmtUE5M3, 16);
     else FP4_DQ(kFmtUE8M0, 32);
 #undef FP4_DQ
+    return cudaGetLastError();
+}
+
+int dual_amax_grid(const QuantJob& jc) {
+    const int64_t units = (jc.rows / 16) * (jc.cols / 4);  // input T x C: 16 tokens x 4 channels per thread
+    int g = grid_for(units, 8);
+    return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
+}
+
+cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStream_t st) {
+    if (jr.rows == 0 || jr.cols == 0) return cudaSuccess;
+    QParams qr = make_params(jr), qc = make_params(jc);
+    const bool amax_pass = !(jr.held && !jr.refresh);
+    if (amax_pass) {
+        const int np = dual_amax_grid(jc);
+        qr.npartials = qc.npartials = np;
+        if (jc.rht)
+            amax_dual_kernel<true><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, qc.key0, qc.key1, jr.partials,
+                                                             jc.partials);
+        else
+            amax_dual_kernel<false><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, qc.key0, qc.key1, jr.partials,
+                                                              jc.partials);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t ntiles = (jr.rows / kDualTT) * (jr.cols / kDualTC);
+    const int64_t cap = (int64_t)num_sms() * 2;
+    const int grid = (int)(ntiles < cap ? ntiles : cap);
+#define FP4_DUAL(FMT, SR, RHT) quantize_dual_kernel<FMT, SR, SR, RHT><<<grid, kThreads, 0, st>>>(qr, qc)
+    if (jr.scale_fmt == kFmtE4M3) {
+        if (jr.sr) { if (jc.rht) FP4_DUAL(kFmtE4M3, true, true); else FP4_DUAL(kFmtE4M3, true, false); }
+        else { if (jc.rht) FP4_DUAL(kFmtE4M3, false, true); else FP4_DUAL(kFmtE4M3, false, false); }
+    } else {
+        if (jr.sr) { if (jc.rht) FP4_DUAL(kFmtUE5M3, true, true); else FP4_DUAL(kFmtUE5M3, true, false); }
+        else { if (jc.rht) FP4_DUAL(kFmtUE5M3, false, true); else FP4_DUAL(kFmtUE5M3, false, false); }
+    }
+#undef FP4_DUAL
     return cudaGetLastError();
 }
 

@@ -150,6 +150,21 @@ fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int6
                           const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                           uint64_t* counters, void* ws, size_t ws_bytes, void* stream);
 
+/* Rowwise and colwise quantization of ONE input in a single pass: the two
+ * operands a linear layer takes from X (or dY) -- `out_row` (rows x cols,
+ * blocks along cols, for Fprop/Dgrad) and `out_col` (cols x rows, blocks along
+ * rows, optional RHT, for Wgrad). Each output, its tensor scale, held state and
+ * counters are bit-identical to a separate fp4_quantize call with p_row /
+ * p_col ("Pretraining LLMs with NVFP4", App. B; sections 4.2-4.4); the input is
+ * read once per pass instead of twice. Requirements: p_row ROWWISE and p_col
+ * COLWISE, both 1x16, same scale format (E4M3 or UE5M3), rounding mode,
+ * tensor-scale mode and step, TCGEN05 scale layout; rows and cols multiples
+ * of 128; ws at least 2 * fp4_workspace_bytes() bytes. */
+fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
+                               int64_t rows, int64_t cols, const fp4_tensor_t* out_row, const fp4_tensor_t* out_col,
+                               fp4_amax_state_t* state_row, fp4_amax_state_t* state_col, uint64_t* counters_row,
+                               uint64_t* counters_col, void* ws, size_t ws_bytes, void* stream);
+
 /* fp4_quantize without a workspace argument, for callers that cannot
  * allocate device memory at all (for example a plug-in inside another
  * framework's engine that owns the memory budget, or a latency-critical loop

@@ -208,3 +208,43 @@ def test_e2m1_conversion_exhaustive_over_bf16_magnitudes():
         ref = oracle_quantize(cfg, bits)
         assert ref["s_dec"] == 1.0
         assert_quant_equal(out, ref, PLAIN, cnt)
+
+
+DUAL_CASES = [
+    # (input shape, dist, scale fmt, round, rht, held, target_T)
+    ((256, 384), "student_t4", fb.FP4_SCALE_E4M3, fb.FP4_ROUND_RNE, True, False, 448.0),
+    ((384, 256), "log_normal_1e-4_2", fb.FP4_SCALE_E4M3, fb.FP4_ROUND_SR, True, False, 448.0),
+    ((256, 256), "normal_outliers", fb.FP4_SCALE_E4M3, fb.FP4_ROUND_RNE, False, False, 448.0),
+    ((512, 640), "log_normal_1e-4_2", fb.FP4_SCALE_UE5M3, fb.FP4_ROUND_SR, False, True, 2048.0),
+]
+
+
+@pytest.mark.parametrize("case", DUAL_CASES)
+def test_dual_quantize_equals_two_separate_calls_and_oracle(case):
+    shape, dist, fmt, rnd, rht, held, T = case
+    base = random_bf16(22, shape, dist)
+    tsc = fb.FP4_TSCALE_HELD if held else fb.FP4_TSCALE_CURRENT
+    states = [fb.AmaxState() for _ in range(4)]
+    ostates = [oracle.HeldState(), oracle.HeldState()]
+    for step, factor in ([(0, 1.0), (1, 50.0), (50, 0.02)] if held else [(3, 1.0)]):
+        bits = f32_to_bf16_bits(bf16_bits_to_f32(base) * np.float32(factor))
+        x = to_gpu_bf16(bits)
+        cr = fb.QuantConfig(scale_fmt=fmt, round=rnd, tscale=tsc, target_T=T, seed=7, tensor_id=3, step=step)
+        cc = fb.QuantConfig(scale_fmt=fmt, round=rnd, tscale=tsc, target_T=T, seed=7, tensor_id=4, step=step,
+                            orient=fb.FP4_ORIENT_COLWISE, rht=rht)
+        R, C = shape
+        dr, dc = fb.QTensor.empty(R, C, fmt), fb.QTensor.empty(C, R, fmt)
+        sr_, sc_ = fb.QTensor.empty(R, C, fmt), fb.QTensor.empty(C, R, fmt)
+        cnt = torch.zeros((4, 4), dtype=torch.int64, device="cuda")
+        ws = torch.zeros(8192, dtype=torch.float32, device="cuda")
+        fb.fp4_quantize_dual(cr, cc, x, dr, dc, states[0], states[1], cnt[0], cnt[1], ws=ws)
+        fb.fp4_quantize(cr, x, sr_, state=states[2], counters=cnt[2], ws=new_ws())
+        fb.fp4_quantize(cc, x, sc_, state=states[3], counters=cnt[3], ws=new_ws())
+        assert fb.fp4_device_status() == 0
+        for a, b in ((dr, sr_), (dc, sc_)):
+            assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+            assert a.s_dec[0:1].view(torch.int32).item() == b.s_dec[0:1].view(torch.int32).item()
+        assert torch.equal(cnt[0], cnt[2]) and torch.equal(cnt[1], cnt[3])
+        assert torch.equal(states[0].buf, states[2].buf) and torch.equal(states[1].buf, states[3].buf)
+        assert_quant_equal(dr, oracle_quantize(cr, bits, state=ostates[0] if held else None), TC, cnt[0])
+        assert_quant_equal(dc, oracle_quantize(cc, bits, state=ostates[1] if held else None), TC, cnt[1])
