@@ -165,9 +165,13 @@ uint8_t orc_e2m1_rne(float v) {
 /* Stochastic rounding ([NV] 4.4): round |v| to one of its two neighbouring E2M1
  * magnitudes lo <= |v| < hi, choosing hi with probability proportional to the
  * distance from lo. Reading of the random-bit contract: r16 is a uniform 16-bit
- * integer and the value rounds up iff r16 < frac * 2^16, where
- * frac = (|v| - lo) / (hi - lo) is exact in FP32 (Sterbenz lemma: hi <= 2 lo
- * whenever lo > 0, and hi - lo is a power of two). |v| > 6 saturates to 6. */
+ * integer added to the fraction frac = (|v| - lo) / (hi - lo) taken to 16 bits,
+ * and the carry out of the sum rounds up:
+ *     up  iff  r16 + floor(frac * 2^16) >= 2^16,
+ * so P(up) = floor(frac * 2^16) / 2^16, within 2^-16 of frac (the bits of the
+ * fraction below 2^-16 are dropped, never rounded up). frac is exact in FP32
+ * (Sterbenz lemma: hi <= 2 lo whenever lo > 0, and hi - lo is a power of two),
+ * and so is frac * 2^16. |v| >= 6 saturates to 6; the code's sign bit is v's. */
 uint8_t orc_e2m1_sr(float v, uint32_t r16) {
     float a = fabsf(v);
     uint8_t sign = signbit(v) ? 8 : 0;
@@ -177,7 +181,8 @@ uint8_t orc_e2m1_sr(float v, uint32_t r16) {
     float flo = (float)E2M1_MAG[lo];
     float fhi = (float)E2M1_MAG[lo + 1];
     float frac = (a - flo) / (fhi - flo);
-    int up = (float)(r16 & 0xFFFFu) < frac * 65536.0f;
+    uint32_t f16 = (uint32_t)floorf(frac * 65536.0f);
+    int up = (r16 & 0xFFFFu) + f16 >= 65536u;
     return (uint8_t)(sign | (lo + up));
 }
 
