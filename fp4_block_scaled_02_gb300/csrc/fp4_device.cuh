@@ -40,50 +40,38 @@ __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float v
 // E2M1 ("Pretraining LLMs with NVFP4", section A3): magnitudes
 // {0, 0.5, 1, 1.5, 2, 3, 4, 6}, code = sign * 8 + magnitude index.
 //
-// Round-to-nearest-even with saturation at 6 (App. B.3), as a sum of threshold
-// tests: each midpoint between neighbours rounds toward the even index, so the
-// tests at 0.25, 1.25, 2.5 and 5 are strict and those at 0.75, 1.75, 3.5 are
-// inclusive. The sign bit of the code is the sign bit of v.
-__device__ __forceinline__ uint32_t e2m1_rne(float v) {
-    const float a = fabsf(v);
-    const uint32_t m = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
-                       (uint32_t)(a > 5.0f);
-    return m | ((__float_as_uint(v) >> 28) & 8u);
+// Stochastic rounding (section 4.4) of two values with the hardware conversion
+// cvt.rs.satfinite.e2m1x4.f32: for each value |x| in [lo, hi) it adds a 16-bit
+// random integer R to the fraction frac = (|x| - lo) / (hi - lo) taken to 16
+// bits and rounds up on the carry, i.e. up iff R + floor(frac * 2^16) >= 2^16;
+// |x| >= 6 saturates; the code keeps x's sign. Of its four sources, the fourth
+// (lowest nibble of the result) draws R from bytes 2:0 of the random operand and
+// the second (third nibble) from bytes 3:1; the other two sources, fed zeros,
+// draw bit-reversed copies of those and are discarded. x0 uses the low half of
+// w and x1 the high half, so the 32-bit word is byte-permuted into that order.
+// Returns x0's code in bits 0-3 and x1's in bits 4-7 (bits 8-15: don't care).
+__device__ __forceinline__ uint32_t e2m1_sr_pair(float x0, float x1, uint32_t w) {
+    const uint32_t rb = __byte_perm(w, 0u, 0x3120);
+    uint16_t d;
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(d)
+        : "f"(0.0f), "f"(x1), "f"(0.0f), "f"(x0), "r"(rb));
+    const uint32_t t = d;
+    return t | (t >> 4);
 }
 
-// Stochastic rounding (section 4.4) with a 16-bit uniform r16: |v| in
-// [lo, hi) rounds up iff r16 < frac * 2^16, frac = (|v| - lo) / (hi - lo).
-// The test is done exactly on the bit pattern of |v| = 2^e (1 + m):
-//   |v| in [1, 6): lo is |v| truncated to one mantissa bit (code 2 + 2e + that
-//     bit), hi - lo = 2^(e-1), so frac * 2^16 = (low 22 mantissa bits) / 2^6;
-//   |v| in [0.5, 1): lo = 0.5 (code 1), frac * 2^16 = (23 mantissa bits) / 2^7;
-//   |v| < 0.5: lo = 0 (code 0), frac * 2^16 = |v| * 2^17 (an exact scaling).
-// |v| >= 6 saturates to 6.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-    const uint32_t b = __float_as_uint(v);
-    const uint32_t sign = (b >> 28) & 8u;
-    const uint32_t a = b & 0x7FFFFFFFu;
-    if (a >= 0x40C00000u) return 7u | sign;
-    uint32_t code, up;
-    if (a >= 0x3F800000u) {
-        code = 2u + 2u * ((a >> 23) - 127u) + ((a >> 22) & 1u);
-        up = (r16 << 6) < (a & 0x3FFFFFu) ? 1u : 0u;
-    } else if (a >= 0x3F000000u) {
-        code = 1u;
-        up = (r16 << 7) < (a & 0x7FFFFFu) ? 1u : 0u;
-    } else {
-        code = 0u;
-        up = (float)r16 < __fmul_rn(__uint_as_float(a), 131072.0f) ? 1u : 0u;
-    }
-    return (code + up) | sign;
+// Eight values -> eight SR codes (element i in nibble i); element 2k and 2k+1
+// take the low and high 16 bits of word k of r.
+__device__ __forceinline__ uint32_t e2m1_sr_x8(const float* x, const uint4& r) {
+    const uint32_t t0 = e2m1_sr_pair(x[0], x[1], r.x), t1 = e2m1_sr_pair(x[2], x[3], r.y);
+    const uint32_t t2 = e2m1_sr_pair(x[4], x[5], r.z), t3 = e2m1_sr_pair(x[6], x[7], r.w);
+    return __byte_perm(__byte_perm(t0, t1, 0x0040u), __byte_perm(t2, t3, 0x0040u), 0x5410u);
 }
 
 // Eight FP32 values -> eight E2M1 codes (element i in nibble i) with the
-// hardware conversion cvt.rn.satfinite.e2m1x2.f32, which rounds to nearest-even
-// and saturates at +-6 (its first source goes to the upper nibble). The sign
-// bits of the inputs are OR-ed in afterwards so that values rounding to zero
-// keep their sign whatever the instruction does with negative zero.
+// hardware conversion cvt.rn.satfinite.e2m1x2.f32, which rounds to nearest-even,
+// saturates at +-6 and keeps the sign of values that round to zero (its first
+// source goes to the upper nibble).
 __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
     uint32_t out;
     asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
@@ -94,10 +82,7 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
         "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
         : "=r"(out)
         : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
-    uint32_t signs = 0u;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) signs |= (__float_as_uint(v[i]) >> (28 - 4 * i)) & (8u << (4 * i));
-    return out | signs;
+    return out;
 }
 
 // Number of zero-magnitude codes among the 8 nibbles of a code word.
@@ -145,11 +130,28 @@ constexpr int kFmtUE8M0 = 2;
 
 template <int FMT>
 struct ScaleFmt;
+// E4M3 through the hardware conversions: cvt.rn.satfinite.e4m3x2.f32 rounds to
+// nearest-even (subnormals included) and saturates at 448; every E4M3 value is
+// an FP16 value, so the decode through f16x2 is exact.
+__device__ __forceinline__ uint32_t e4m3_encode_hw(float s) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(0.0f), "f"(s));
+    return (uint32_t)d & 0xFFu;
+}
+__device__ __forceinline__ float e4m3_decode_hw(uint32_t code) {
+    uint32_t h2;
+    const uint16_t c2 = (uint16_t)(code | (code << 8));  // same code in both lanes
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+    float f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
 template <>
 struct ScaleFmt<kFmtE4M3> {
     static constexpr float kMax = 448.0f;
-    __device__ static __forceinline__ uint32_t encode(float s) { return scale_encode_m3<7, 0x7Eu>(s, kMax); }
-    __device__ static __forceinline__ float decode(uint32_t c) { return scale_decode_m3<7>(c & 0x7Fu); }
+    __device__ static __forceinline__ uint32_t encode(float s) { return e4m3_encode_hw(s); }
+    __device__ static __forceinline__ float decode(uint32_t c) { return e4m3_decode_hw(c & 0x7Fu); }
 };
 template <>
 struct ScaleFmt<kFmtUE5M3> {
@@ -207,32 +209,75 @@ __device__ __forceinline__ uint32_t sr_half(const uint4& w, int i) {  // element
     return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
 }
 
-// Sign vector of the random Hadamard transform (section 4.2: one vector shared
-// by every layer for the whole run): bit i of word 0 of Philox(counter =
-// (0, 0, 0xFFFFFFFF, 0xFFFFFFFF), key = seed); a set bit negates row i.
-__device__ __forceinline__ uint32_t rht_sign_word(uint32_t key0, uint32_t key1) {
-    return philox4x32_10(make_uint4(0u, 0u, 0xFFFFFFFFu, 0xFFFFFFFFu), key0, key1).x & 0xFFFFu;
+// ---------------------------------------------------------------------------
+// Packed FP32 pairs: two independent lanes per 64-bit register, each operation
+// one IEEE binary32 round-to-nearest-even per lane (add/sub/mul.rn.f32x2).
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 f2_pack(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2 r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
-// v <- D_r * (H_16 / 4) * v ("Pretraining LLMs with NVFP4", App. C): butterfly
-// stages of half-width 1, 2, 4, 8 producing the Sylvester-ordered transform,
-// then the (1/sqrt 2)^4 = 1/4 normalisation, then the sign of row i.
-__device__ __forceinline__ void rht16(float v[16], uint32_t signs) {
+// x[i] = RN(v[i] * m) for 16 values, two per instruction.
+__device__ __forceinline__ void scale16(const float v[16], float m, float x[16]) {
+    const f2 mm = f2_pack(m, m);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) f2_unpack(f2_mul(f2_pack(v[i], v[i + 1]), mm), x[i], x[i + 1]);
+}
+
+// Unnormalised, unsigned 16-point Walsh-Hadamard butterfly in Sylvester order
+// (the H_16 part of the RHT, App. C) on two independent vectors held in the two
+// lanes of v[16]: stages of half-width 1, 2, 4, 8, each a[i] + a[i+h] and
+// a[i] - a[i+h] rounded to nearest, exactly the per-lane steps of rht16.
+__device__ __forceinline__ void wht16x2(f2 v[16]) {
 #pragma unroll
     for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (i & h) continue;
-            const float a = v[i], b = v[i + h];
-            v[i] = __fadd_rn(a, b);
-            v[i + h] = __fsub_rn(a, b);
+            const f2 a = v[i], b = v[i + h];
+            v[i] = f2_add(a, b);
+            v[i + h] = f2_sub(a, b);
         }
     }
+}
+
+// Sign nibble masks of the RHT sign vector: bit 3 of nibble i (i < 8) of lo, and
+// of nibble i - 8 of hi, is bit i of signs.
+__device__ __forceinline__ void rht_sign_masks(uint32_t signs, uint32_t& lo, uint32_t& hi) {
+    lo = 0u;
+    hi = 0u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float q = __fmul_rn(v[i], 0.25f);
-        v[i] = __uint_as_float(__float_as_uint(q) ^ (((signs >> i) & 1u) << 31));
+    for (int i = 0; i < 8; ++i) {
+        lo |= ((signs >> i) & 1u) << (4 * i + 3);
+        hi |= ((signs >> (i + 8)) & 1u) << (4 * i + 3);
     }
+}
+
+// Sign vector of the random Hadamard transform (section 4.2: one vector shared
+// by every layer for the whole run): bit i of word 0 of Philox(counter =
+// (0, 0, 0xFFFFFFFF, 0xFFFFFFFF), key = seed); a set bit negates row i.
+__device__ __forceinline__ uint32_t rht_sign_word(uint32_t key0, uint32_t key1) {
+    return philox4x32_10(make_uint4(0u, 0u, 0xFFFFFFFFu, 0xFFFFFFFFu), key0, key1).x & 0xFFFFu;
 }
 
 // ---------------------------------------------------------------------------

@@ -162,17 +162,24 @@ __device__ __forceinline__ float amax_f32x16(const float v[16], uint32_t& nzero)
     return m;
 }
 
-// Quantize one 1x16 block held in v[16] whose amax and zero count are known
-// (App. B.2-B.3): scale in the block format (RNE, satfinite), local encode
-// scale, E2M1 codes packed into two 32-bit words (element i in nibble i).
+// Quantize one 1x16 block (App. B.2-B.3): scale in the block format (RNE,
+// satfinite), local encode scale, E2M1 codes packed into two 32-bit words
+// (element i in nibble i). The block's values are w_i = sign_i * pre * v[i]:
+// plain blocks pass pre = 1 and zero sign masks; RHT blocks pass the raw
+// Hadamard butterfly in v, pre = 1/4 and the sign vector as nibble masks
+// (bit 3 of nibble i), so the normalisation and the signs fold into the
+// element scale and the code sign bits. amax_b is max |w_i| and nzero the
+// number of zero w_i. Folding is exact: pre * v[i] is exact, and so is
+// pre * s_enc,L except below 2^-124, where the two products are taken apart.
 // `g0` is the SR group of element 0. Event counts: scale saturation and
 // underflow (when count_scale); element saturation, counted per element only
 // when the scaled block amax exceeds 6 (rounding is monotone, so otherwise no
 // element can); element underflow = zero-magnitude codes minus zero inputs.
 template <int FMT, bool SR>
-__device__ __forceinline__ uint32_t quantize_block16(const float v[16], float amax_b, uint32_t nzero, float s_enc,
-                                                     float s_dec, uint64_t g0, const QParams& q, uint32_t& lo,
-                                                     uint32_t& hi, Counts& cnt, bool count_scale) {
+__device__ __forceinline__ uint32_t quantize_block16(const float v[16], float amax_b, uint32_t nzero, float pre,
+                                                     uint32_t smask_lo, uint32_t smask_hi, float s_enc, float s_dec,
+                                                     uint64_t g0, const QParams& q, uint32_t& lo, uint32_t& hi,
+                                                     Counts& cnt, bool count_scale) {
     using F = ScaleFmt<FMT>;
     const float s = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
     const uint32_t sc = F::encode(s);
@@ -180,14 +187,18 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float am
     if (sc == 0u) {
         if (count_scale) cnt.sunder += amax_b > 0.0f ? 1u : 0u;
         cnt.eunder += 16u - nzero;
-        lo = sign_nibbles8(v);
-        hi = sign_nibbles8(v + 8);
+        lo = sign_nibbles8(v) ^ smask_lo;
+        hi = sign_nibbles8(v + 8) ^ smask_hi;
         return 0u;
     }
-    const float s_enc_l = __fdiv_rn(1.0f, __fmul_rn(F::decode(sc), s_dec));
+    const float s_enc_l = __frcp_rn(__fmul_rn(F::decode(sc), s_dec));
     float x[16];
+    if (pre == 1.0f || s_enc_l >= 0x1p-124f) {
+        scale16(v, __fmul_rn(pre, s_enc_l), x);
+    } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(v[i], s_enc_l);
+        for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(__fmul_rn(v[i], pre), s_enc_l);
+    }
     if (__fmul_rn(amax_b, s_enc_l) > 6.0f) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[i]);
@@ -195,17 +206,14 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float am
     if (SR) {
         const uint4 r0 = sr_group_bits(g0, q.tensor_id, q.step_lo, q.key0, q.key1);
         const uint4 r1 = sr_group_bits(g0 + 1, q.tensor_id, q.step_lo, q.key0, q.key1);
-        lo = hi = 0u;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t code = e2m1_sr(x[i], sr_half(i < 8 ? r0 : r1, i & 7));
-            if (i < 8) lo |= code << (4 * i);
-            else hi |= code << (4 * (i - 8));
-        }
+        lo = e2m1_sr_x8(x, r0);
+        hi = e2m1_sr_x8(x + 8, r1);
     } else {
         lo = e2m1_rne_x8(x);
         hi = e2m1_rne_x8(x + 8);
     }
+    lo ^= smask_lo;
+    hi ^= smask_hi;
     cnt.eunder += zero_mag_count8(lo) + zero_mag_count8(hi) - nzero;
     return sc;
 }
@@ -243,11 +251,11 @@ __global__ void __launch_bounds__(kThreads) amax_plain_kernel(const uint4* __res
 }
 
 // amax in the rotated space (App. C): each thread transforms 16 tokens of 4
-// channels (sixteen 64-bit loads) and keeps the max magnitude.
+// channels (sixteen 64-bit loads, two channels per packed butterfly) and keeps
+// the max magnitude. The RHT's signs do not change magnitudes and its 1/4 is an
+// exact scaling, so the max is taken over the raw butterfly and scaled once.
 __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ in, int64_t T,
-                                                                 int64_t C, uint32_t key0, uint32_t key1,
-                                                                 float* __restrict__ partials) {
-    const uint32_t signs = rht_sign_word(key0, key1);
+                                                                 int64_t C, float* __restrict__ partials) {
     const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     float m = 0.0f;
@@ -257,19 +265,23 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
 #pragma unroll
         for (int t = 0; t < 16; ++t) x[t] = __ldg(reinterpret_cast<const uint2*>(in + (16 * j + t) * C + 4 * g));
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            float v[16];
+        for (int pr = 0; pr < 2; ++pr) {
+            f2 pv[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                const uint32_t w = ch < 2 ? x[t].x : x[t].y;
-                v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
+                const uint32_t w = pr ? x[t].y : x[t].x;
+                pv[t] = f2_pack(bf16_lo(w), bf16_hi(w));
             }
-            rht16(v, signs);
+            wht16x2(pv);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) m = fmaxf(m, fabsf(v[t]));
+            for (int t = 0; t < 16; ++t) {
+                float a, b;
+                f2_unpack(pv[t], a, b);
+                m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
+            }
         }
     }
-    m = cta_max(m);
+    m = cta_max(__fmul_rn(m, 0.25f));
     if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }
 
@@ -299,7 +311,8 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
             float v[16];
             unpack16(a, c, v);
             uint32_t lo, hi;
-            sc = quantize_block16<FMT, SR>(v, amax_b, nzero, s_enc, s_dec, (uint64_t)(2 * b), q, lo, hi, cnt, true);
+            sc = quantize_block16<FMT, SR>(v, amax_b, nzero, 1.0f, 0u, 0u, s_enc, s_dec, (uint64_t)(2 * b), q, lo, hi, cnt,
+                                           true);
             *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
         }
         if (TCL) {
@@ -338,6 +351,8 @@ __global__ void __launch_bounds__(kThreads) quantize_cols_kernel(QParams q) {
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const uint32_t signs = RHT ? rht_sign_word(q.key0, q.key1) : 0u;
+    uint32_t smask_lo = 0u, smask_hi = 0u;
+    if (RHT) rht_sign_masks(signs, smask_lo, smask_hi);
     Counts cnt;
     for (int64_t wu = warp; wu < wunits; wu += nwarps) {
         const int64_t g = (wu % wg_count) * 8 + (lane >> 2);
@@ -348,31 +363,43 @@ __global__ void __launch_bounds__(kThreads) quantize_cols_kernel(QParams q) {
         for (int t = 0; t < 16; ++t)
             x[t] = active ? __ldg(reinterpret_cast<const uint2*>(q.in + (16 * j + t) * C + 4 * g)) : make_uint2(0, 0);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            float v[16];
+        for (int pr = 0; pr < 2; ++pr) {
+            // channels 4g + 2pr (low lane) and 4g + 2pr + 1 (high lane)
+            f2 pv[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                const uint32_t w = ch < 2 ? x[t].x : x[t].y;
-                v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
+                const uint32_t w = pr ? x[t].y : x[t].x;
+                pv[t] = f2_pack(bf16_lo(w), bf16_hi(w));
             }
-            if (RHT) rht16(v, signs);
-            const int64_t c = 4 * g + ch;
-            uint32_t lo = 0u, hi = 0u, sc = 0u;
-            if (active) {
-                uint32_t nzero;
-                const float amax_b = amax_f32x16(v, nzero);
-                sc = quantize_block16<FMT, SR>(v, amax_b, nzero, s_enc, s_dec, (uint64_t)((c * T + 16 * j) >> 3), q,
-                                              lo, hi, cnt, true);
-                *reinterpret_cast<uint2*>(q.codes + c * (T / 2) + 8 * j) = make_uint2(lo, hi);
-            }
-            if (TCL) {
-                uint32_t w = sc << (8 * (lane & 3));
-                w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
-                w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
-                if (active && (lane & 3) == 0)
-                    *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(c, j, uj)) = w;
-            } else if (active) {
-                q.scales[c * uj + j] = (uint8_t)sc;
+            if (RHT) wht16x2(pv);
+#pragma unroll
+            for (int ln = 0; ln < 2; ++ln) {
+                float v[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    float a, b;
+                    f2_unpack(pv[t], a, b);
+                    v[t] = ln ? b : a;
+                }
+                const int64_t c = 4 * g + 2 * pr + ln;
+                uint32_t lo = 0u, hi = 0u, sc = 0u;
+                if (active) {
+                    uint32_t nzero;
+                    const float amax_v = amax_f32x16(v, nzero);
+                    sc = quantize_block16<FMT, SR>(v, RHT ? __fmul_rn(amax_v, 0.25f) : amax_v, nzero,
+                                                  RHT ? 0.25f : 1.0f, smask_lo, smask_hi, s_enc, s_dec,
+                                                  (uint64_t)((c * T + 16 * j) >> 3), q, lo, hi, cnt, true);
+                    *reinterpret_cast<uint2*>(q.codes + c * (T / 2) + 8 * j) = make_uint2(lo, hi);
+                }
+                if (TCL) {
+                    uint32_t w = sc << (8 * (lane & 3));
+                    w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+                    w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+                    if (active && (lane & 3) == 0)
+                        *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(c, j, uj)) = w;
+                } else if (active) {
+                    q.scales[c * uj + j] = (uint8_t)sc;
+                }
             }
         }
     }
@@ -432,10 +459,9 @@ __global__ void __launch_bounds__(kThreads) quantize_2d_kernel(QParams q) {
             hi = sign_nibbles8(v + 8);
             if (active) cnt.eunder += 16u - nzero;
         } else {
-            const float s_enc_l = __fdiv_rn(1.0f, __fmul_rn(F::decode(sc), s_dec));
+            const float s_enc_l = __frcp_rn(__fmul_rn(F::decode(sc), s_dec));
             float x[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = __fmul_rn(v[e], s_enc_l);
+            scale16(v, s_enc_l, x);
             lo = e2m1_rne_x8(x);
             hi = e2m1_rne_x8(x + 8);
             if (active) {
@@ -509,11 +535,10 @@ __global__ void __launch_bounds__(kThreads) quantize_mx_rows_kernel(QParams q) {
             const float inv = exp2_exact(-ex);
             float x[32];
             uint32_t nzero = 0u;
+            scale16(v, inv, x);
+            scale16(v + 16, inv, x + 16);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                x[e] = __fmul_rn(v[e], inv);
-                nzero += (__float_as_uint(v[e]) << 1) == 0u ? 1u : 0u;
-            }
+            for (int e = 0; e < 32; ++e) nzero += (__float_as_uint(v[e]) << 1) == 0u ? 1u : 0u;
             if (__fmul_rn(amax_b, inv) > 6.0f) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) cnt.esat += e2m1_saturates(x[e]);
@@ -600,10 +625,8 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __r
 // tokens x 4 channels.
 template <bool RHT>
 __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __restrict__ in, int64_t T, int64_t C,
-                                                             uint32_t key0, uint32_t key1,
                                                              float* __restrict__ partials_row,
                                                              float* __restrict__ partials_col) {
-    const uint32_t signs = RHT ? rht_sign_word(key0, key1) : 0u;
     const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     uint32_t mr = 0u;
@@ -617,21 +640,25 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __r
         for (int t = 0; t < 16; ++t) mr = __vmaxu2(mr, __vmaxu2(x[t].x & 0x7FFF7FFFu, x[t].y & 0x7FFF7FFFu));
         if (RHT) {
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                float v[16];
+            for (int pr = 0; pr < 2; ++pr) {
+                f2 pv[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const uint32_t w = ch < 2 ? x[t].x : x[t].y;
-                    v[t] = (ch & 1) ? bf16_hi(w) : bf16_lo(w);
+                    const uint32_t w = pr ? x[t].y : x[t].x;
+                    pv[t] = f2_pack(bf16_lo(w), bf16_hi(w));
                 }
-                rht16(v, signs);
+                wht16x2(pv);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) mc = fmaxf(mc, fabsf(v[t]));
+                for (int t = 0; t < 16; ++t) {
+                    float a, b;
+                    f2_unpack(pv[t], a, b);
+                    mc = fmaxf(mc, fmaxf(fabsf(a), fabsf(b)));
+                }
             }
         }
     }
     const float fr = cta_max(__uint_as_float(max(mr & 0xFFFFu, mr >> 16) << 16));
-    const float fc = RHT ? cta_max(mc) : fr;
+    const float fc = RHT ? cta_max(__fmul_rn(mc, 0.25f)) : fr;
     if (threadIdx.x == 0) {
         partials_row[blockIdx.x] = fr;
         partials_col[blockIdx.x] = fc;
@@ -659,6 +686,8 @@ __global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QPa
     const int64_t tiles_c = C / kDualTC, ntiles = (T / kDualTT) * tiles_c;
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t signs = RHT ? rht_sign_word(qc.key0, qc.key1) : 0u;
+    uint32_t smask_lo = 0u, smask_hi = 0u;
+    if (RHT) rht_sign_masks(signs, smask_lo, smask_hi);
     const int64_t nb_row = C / 16, nb_col = T / 16;
     Counts cr, cc;
     uint4 pre[4];
@@ -696,7 +725,8 @@ __global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QPa
             const int64_t row = t0 + r, j = (c0 >> 4) + b, bg = row * nb_row + j;
             uint32_t lo, hi;
             const uint32_t sc =
-                quantize_block16<FMT, SR_ROW>(v, amax_b, nzero, se_r, sd_r, (uint64_t)(2 * bg), qr, lo, hi, cr, true);
+                quantize_block16<FMT, SR_ROW>(v, amax_b, nzero, 1.0f, 0u, 0u, se_r, sd_r, (uint64_t)(2 * bg), qr, lo, hi,
+                                              cr, true);
             *reinterpret_cast<uint2*>(qr.codes + 8 * bg) = make_uint2(lo, hi);
             uint32_t ww = sc << (8 * (lane & 3));
             ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 1);
@@ -706,24 +736,30 @@ __global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QPa
         // colwise: channel pair cp, token block jb
         {
             const int cp = tid & 63, jb = tid >> 6;
-            float v0[16], v1[16];
+            f2 pv[16];
 #pragma unroll
             for (int tt = 0; tt < 16; ++tt) {
                 const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(16 * jb + tt) * kDualTC + 2 * cp]);
-                v0[tt] = bf16_lo(w);
-                v1[tt] = bf16_hi(w);
+                pv[tt] = f2_pack(bf16_lo(w), bf16_hi(w));
             }
+            if (RHT) wht16x2(pv);
             const int64_t jg = (t0 >> 4) + jb;
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
-                float* v = ch ? v1 : v0;
-                if (RHT) rht16(v, signs);
+                float v[16];
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    float a, b;
+                    f2_unpack(pv[tt], a, b);
+                    v[tt] = ch ? b : a;
+                }
                 uint32_t nzero;
-                const float amax_b = amax_f32x16(v, nzero);
+                const float amax_v = amax_f32x16(v, nzero);
                 const int64_t c = c0 + 2 * cp + ch;
                 uint32_t lo, hi;
-                const uint32_t sc = quantize_block16<FMT, SR_COL>(v, amax_b, nzero, se_c, sd_c,
-                                                                  (uint64_t)((c * T + 16 * jg) >> 3), qc, lo, hi, cc, true);
+                const uint32_t sc = quantize_block16<FMT, SR_COL>(
+                    v, RHT ? __fmul_rn(amax_v, 0.25f) : amax_v, nzero, RHT ? 0.25f : 1.0f, smask_lo, smask_hi, se_c,
+                    sd_c, (uint64_t)((c * T + 16 * jg) >> 3), qc, lo, hi, cc, true);
                 *reinterpret_cast<uint2*>(qc.codes + c * (T / 2) + 8 * jg) = make_uint2(lo, hi);
                 qc.scales[tc_scale_offset(c, jg, nb_col)] = (uint8_t)sc;
             }
@@ -855,7 +891,7 @@ cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
     const int np = amax_partials_needed(j);
     q.npartials = np;
     if (np > 0) {
-        if (j.rht) amax_rht_cols_kernel<<<np, kThreads, 0, st>>>(j.in, j.rows, j.cols, q.key0, q.key1, j.partials);
+        if (j.rht) amax_rht_cols_kernel<<<np, kThreads, 0, st>>>(j.in, j.rows, j.cols, j.partials);
         else amax_plain_kernel<<<np, kThreads, 0, st>>>(reinterpret_cast<const uint4*>(j.in), j.rows * j.cols / 8,
                                                          j.partials);
         cudaError_t e = cudaGetLastError();
@@ -901,11 +937,9 @@ cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStr
         const int np = dual_amax_grid(jc);
         qr.npartials = qc.npartials = np;
         if (jc.rht)
-            amax_dual_kernel<true><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, qc.key0, qc.key1, jr.partials,
-                                                             jc.partials);
+            amax_dual_kernel<true><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials);
         else
-            amax_dual_kernel<false><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, qc.key0, qc.key1, jr.partials,
-                                                              jc.partials);
+            amax_dual_kernel<false><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -202,10 +202,41 @@ def test_e2m1_conversion_exhaustive_over_bf16_magnitudes():
     head = np.zeros((1, 16), dtype=np.uint16)
     head[0, 0] = f32_to_bf16_bits(np.array([2688.0], np.float32))[0]
     bits = np.ascontiguousarray(np.concatenate([head, bits], axis=0))
-    for rnd in (fb.FP4_ROUND_RNE, fb.FP4_ROUND_SR):
-        cfg = fb.QuantConfig(layout=PLAIN, round=rnd, seed=5, tensor_id=2)
+    # RNE once; SR with four different draws per value (steps 0..3)
+    for rnd, step in [(fb.FP4_ROUND_RNE, 0)] + [(fb.FP4_ROUND_SR, k) for k in range(4)]:
+        cfg = fb.QuantConfig(layout=PLAIN, round=rnd, seed=5, tensor_id=2, step=step)
         out, _, cnt = gpu_quantize(cfg, bits)
         ref = oracle_quantize(cfg, bits)
+        assert ref["s_dec"] == 1.0
+        assert_quant_equal(out, ref, PLAIN, cnt)
+
+
+def test_e4m3_block_scale_ties_and_neighbours():
+    """Block amaxes 6 * m for every midpoint m between neighbouring E4M3 values
+    up to 448 (subnormals included) and the BF16 neighbours of 6 * m, with
+    s_enc,G = 1 (one block holds 2688 = 6 * 448): s = RN(amax / 6) = m exactly,
+    so every tie of the block-scale encode (App. B.2, RNE) is exercised, in
+    both the rowwise and the colwise kernels."""
+    e4 = torch.arange(0, 0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mids = (e4[:-1] + e4[1:]) / 2
+    amax = f32_to_bf16_bits((6.0 * mids).astype(np.float32))
+    assert np.array_equal(bf16_bits_to_f32(amax).astype(np.float64), 6.0 * mids)   # exact in BF16
+    amax = np.concatenate([amax, amax + 1, amax - 1])
+    amax = amax[(amax > 0) & (bf16_bits_to_f32(amax) <= 2688.0)]
+    rng = np.random.default_rng(4)
+    rows = np.zeros((amax.size + 1, 16), dtype=np.float32)
+    rows[0, 0] = 2688.0
+    a = bf16_bits_to_f32(amax)
+    rows[1:, 0] = a
+    rows[1:, 1:] = a[:, None] * rng.uniform(-1.0, 1.0, (amax.size, 15))
+    nrow = -(-rows.shape[0] // 16) * 16                            # whole 16-row tiles for the colwise case
+    rows = np.concatenate([rows, np.zeros((nrow - rows.shape[0], 16), np.float32)])
+    bits = f32_to_bf16_bits(rows)
+    for orient in (fb.FP4_ORIENT_ROWWISE, fb.FP4_ORIENT_COLWISE):
+        src = bits if orient == fb.FP4_ORIENT_ROWWISE else np.ascontiguousarray(bits.T)
+        cfg = fb.QuantConfig(layout=PLAIN, orient=orient)
+        out, _, cnt = gpu_quantize(cfg, src)
+        ref = oracle_quantize(cfg, src)
         assert ref["s_dec"] == 1.0
         assert_quant_equal(out, ref, PLAIN, cnt)
 
