@@ -12,25 +12,29 @@
 //   warp 0      : TMA producer -- A/B code tiles (128-byte swizzled rows of 256
 //                 FP4 values) and the tiles' scale chunks (1-D bulk copies) into
 //                 a STAGES-deep shared-memory ring guarded by mbarriers;
-//   warp 6      : one lane copies each stage's scale chunks into tensor memory
-//                 (eight tcgen05.cp.32x128b.warpx4) and commits them to a
-//                 per-stage barrier;
-//   warp 1      : allocates tensor memory and one lane issues, per stage, four
-//                 tcgen05.mma kind::mxf4nvf4 (K = 64 each), then commits the
-//                 stage back to the producer. Measured on GB300, a single thread
-//                 issuing the scale copies as well spent ~90 % of its time issuing
-//                 and left the tensor pipe ~80 % idle, so the copies live on their
-//                 own warp;
-//   warps 2-5   : epilogue -- tcgen05.ld the FP32 accumulator (each warp owns
-//                 its 32-lane quadrant), scale by alpha, store BF16 / FP32.
+//   warp 1      : allocates tensor memory; one lane issues, per stage, four
+//                 tcgen05.mma kind::mxf4nvf4 (M = 128, N = BN, K = 64 each) and
+//                 commits the stage back to the producer;
+//   warp 2      : one lane copies each stage's scale chunks into tensor memory
+//                 (tcgen05.cp.32x128b.warpx4) and commits them to a per-stage
+//                 barrier (measured on GB300: with the copies on the MMA thread
+//                 as well, that thread was the bottleneck);
+//   warps 3..   : epilogue -- BN / 32 warps; warp w reads TMEM lane quadrant
+//                 w % 4 and 128 of the BN accumulator columns (tcgen05.ld),
+//                 scales by alpha and stores BF16 / FP32.
+// Measured on GB300: a kind::mxf4nvf4 MMA with M = 128 takes about the same
+// time for N = 128 and N = 256, so BN = 256 tiles (one 256-column accumulator)
+// double the work per instruction; BN = 128 tiles (two accumulators) remain for
+// N not divisible by 256.
 // K is accumulated in chunks of 1024 values (CHUNK_STAGES stages): each chunk
-// starts a fresh accumulator in one of two tensor-memory buffers, and the
-// epilogue adds the chunk partials in FP32 registers with round-to-nearest.
-// Measured on GB300, one accumulator carried over K = 8192 drifts toward zero
-// (every out-of-bound output was smaller in magnitude than the exact sum), a
-// bias that grows with the number of MMAs folded into the accumulator; chunking
-// bounds it by the chunk length instead of K, and the two buffers let the
-// epilogue fold chunk c while the MMAs of chunk c+1 (or of the next tile) run.
+// starts a fresh accumulator and the epilogue adds the chunk partials in FP32
+// registers with round-to-nearest. Measured on GB300, one accumulator carried
+// over K = 8192 drifts toward zero (every out-of-bound output was smaller in
+// magnitude than the exact sum), a bias that grows with the number of MMAs
+// folded into the accumulator; chunking bounds it by the chunk length instead
+// of K. With two buffers (BN = 128) the epilogue folds chunk c while the MMAs of
+// chunk c+1 run; with one (BN = 256) the MMAs of the next chunk wait for the
+// fold, but not for the output stores of a finished tile.
 // Every mbarrier wait is bounded (see tcgen05.cuh).
 #include <cstdint>
 #include <cstring>
@@ -75,6 +79,10 @@ struct NvCfg {
     static constexpr int SF_TMEM_BASE = NUM_ACC * BN;
     static constexpr int TMEM_COLS = 512;
     static_assert(SF_TMEM_BASE + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory budget");
+    static constexpr int EPI_WARPS = BN / 32;      // 4 lane quadrants x (BN / 128) column halves
+    static constexpr int EPI_COLS = 128;           // accumulator columns per epilogue warp
+    static constexpr int FIRST_EPI_WARP = 3;
+    static constexpr int THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS);
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -83,7 +91,6 @@ struct NvCfg {
     static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
-    static constexpr int THREADS = 224;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -115,7 +122,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int a = 0; a < Cfg::NUM_ACC; ++a) {
             tc::mbar_init(accf_bar(a), 1);
-            tc::mbar_init(acce_bar(a), 4);
+            tc::mbar_init(acce_bar(a), Cfg::EPI_WARPS);
         }
         tc::mbar_init(drain_bar, 1);
         for (int s = 0; s < Cfg::STAGES; ++s) tc::mbar_init(sf_bar(s), 1);
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const bool last = kb % Cfg::CHUNK_STAGES == Cfg::CHUNK_STAGES - 1 || kb == num_k - 1;
                     const int buf = (int)(chunk % Cfg::NUM_ACC);
                     if (first) {
-                        // the epilogue must have drained this buffer's previous chunk
+                        // the epilogue must have read this buffer's previous chunk
                         if (!tc::mbar_wait(acce_bar(buf), ((chunk / Cfg::NUM_ACC) & 1u) ^ 1u, p.status)) {
                             ok = false;
                             break;
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc::commit(drain_bar);
             tc::mbar_wait(drain_bar, 0, p.status);
         }
-    } else if (warp == 6) {
+    } else if (warp == 2) {
         // ------------------------------------------------------------ scale copies
         if (lane == 0) {
             uint32_t it = 0;
@@ -253,15 +260,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // the TMEM lane quadrant this warp may access
+        const int half = (warp - Cfg::FIRST_EPI_WARP) >> 2;  // which 128 of the BN columns
         const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
         const int nchunks = (num_k + Cfg::CHUNK_STAGES - 1) / Cfg::CHUNK_STAGES;
         uint32_t chunk = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
             const int64_t mb = tile % num_m, nb = tile / num_m;
-            float acc[Cfg::BN];
+            float acc[Cfg::EPI_COLS];
 #pragma unroll
-            for (int c = 0; c < Cfg::BN; ++c) acc[c] = 0.0f;
+            for (int c = 0; c < Cfg::EPI_COLS; ++c) acc[c] = 0.0f;
             for (int ch = 0; ch < nchunks; ++ch, ++chunk) {
                 const int buf = (int)(chunk % Cfg::NUM_ACC);
                 if (!tc::mbar_wait(accf_bar(buf), (chunk / Cfg::NUM_ACC) & 1u, p.status)) {
@@ -269,9 +277,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * Cfg::BN);
+                const uint32_t t_row =
+                    tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * Cfg::BN + half * Cfg::EPI_COLS);
 #pragma unroll
-                for (int c = 0; c < Cfg::BN; c += 32) {
+                for (int c = 0; c < Cfg::EPI_COLS; c += 32) {
                     uint32_t r[32];
                     tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
                     tc::tmem_ld_wait();
@@ -284,11 +293,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             if (!ok) break;
             const int64_t m = mb * Cfg::BM + q * 32 + lane;
-            const int64_t n0 = nb * Cfg::BN;
+            const int64_t n0 = nb * Cfg::BN + half * Cfg::EPI_COLS;
             if (OUT32) {
                 float* dst = static_cast<float*>(p.d) + m * p.N + n0;
 #pragma unroll
-                for (int v = 0; v < Cfg::BN / 4; ++v) {
+                for (int v = 0; v < Cfg::EPI_COLS / 4; ++v) {
                     float4 o = make_float4(__fmul_rn(acc[4 * v + 0], alpha), __fmul_rn(acc[4 * v + 1], alpha),
                                            __fmul_rn(acc[4 * v + 2], alpha), __fmul_rn(acc[4 * v + 3], alpha));
                     if (p.accumulate) {
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             } else {
                 uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
 #pragma unroll
-                for (int v = 0; v < Cfg::BN / 8; ++v) {
+                for (int v = 0; v < Cfg::EPI_COLS / 8; ++v) {
                     uint32_t w[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -378,13 +387,18 @@ cudaError_t run_nvfp4(const GemmJob& j, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-using NvDefault = NvCfg<128, 6>;
+using NvWide = NvCfg<256, 4>;    // N % 256 == 0
+using NvNarrow = NvCfg<128, 6>;  // N % 128 == 0
 
 }  // namespace
 
 cudaError_t launch_gemm_nvfp4(const GemmJob& j, cudaStream_t st) {
-    if (j.out_fp32) return run_nvfp4<NvDefault, true>(j, st);
-    return run_nvfp4<NvDefault, false>(j, st);
+    if (j.N % 256 == 0) {
+        if (j.out_fp32) return run_nvfp4<NvWide, true>(j, st);
+        return run_nvfp4<NvWide, false>(j, st);
+    }
+    if (j.out_fp32) return run_nvfp4<NvNarrow, true>(j, st);
+    return run_nvfp4<NvNarrow, false>(j, st);
 }
 
 }  // namespace fp4bs

@@ -43,7 +43,9 @@ def _check(c_gpu, c_ref, s, bf16):
                              f"gpu {c_gpu.reshape(-1)[i]}, ref {c_ref.reshape(-1)[i]}, tol {tol.reshape(-1)[i]}")
 
 
-SHAPES = [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (1280, 1152, 768)]
+# N % 256 == 0 runs 128 x 256 tiles, other N 128 x 128 tiles; K = 1280 ends in a
+# partial accumulator chunk
+SHAPES = [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (1280, 1152, 768), (640, 1024, 1280)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -58,9 +60,10 @@ def test_gemm_nvfp4_full_output(M, N, K, out32):
     _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
 
 
-def test_gemm_nvfp4_persistent_wrap_sampled():
-    # more output tiles than SMs: each CTA loops over several tiles and both accumulators
-    M, N, K = 2048, 2048, 512
+@pytest.mark.parametrize("M,N,K", [(4096, 2048, 512), (2048, 2176, 1280)])
+def test_gemm_nvfp4_persistent_wrap_sampled(M, N, K):
+    # more output tiles than SMs (256 tiles of 128 x 256; 272 of 128 x 128): each
+    # CTA loops over several tiles and accumulator chunks
     ra, a = _operand(33, M, K, "normal")
     rb, b = _operand(34, N, K, "log_normal_1e-4_2")
     d = torch.empty((M, N), dtype=torch.float32, device="cuda")
