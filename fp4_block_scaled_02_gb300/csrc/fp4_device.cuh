@@ -150,12 +150,14 @@ __device__ __forceinline__ float e4m3_decode_hw(uint32_t code) {
 template <>
 struct ScaleFmt<kFmtE4M3> {
     static constexpr float kMax = 448.0f;
+    static constexpr uint32_t kMaxCode = 0x7Eu;
     __device__ static __forceinline__ uint32_t encode(float s) { return e4m3_encode_hw(s); }
     __device__ static __forceinline__ float decode(uint32_t c) { return e4m3_decode_hw(c & 0x7Fu); }
 };
 template <>
 struct ScaleFmt<kFmtUE5M3> {
     static constexpr float kMax = 114688.0f;
+    static constexpr uint32_t kMaxCode = 0xFEu;
     __device__ static __forceinline__ uint32_t encode(float s) { return scale_encode_m3<15, 0xFEu>(s, kMax); }
     __device__ static __forceinline__ float decode(uint32_t c) { return scale_decode_m3<15>(c); }
 };
@@ -178,6 +180,56 @@ __device__ __forceinline__ float exp2_exact(int k) {
     return __uint_as_float(1u << (k + 149));
 }
 
+// RN(a / 6) in binary32 with one multiply and two fused multiply-adds:
+// q0 = RN(a * y) with y = RN(1/6), r = RN(a - 6 q0) (exact), q1 = RN(q0 + r * y).
+// Checked exhaustively against the correctly rounded quotient over whole
+// binades (normal binades all behave alike, being exact scalings of one
+// another); below 2^-120 the quotient approaches the subnormal range, where
+// the IEEE division is used instead.
+__device__ __forceinline__ float div6_rn(float a) {
+    if (!(a >= 0x1p-120f)) return __fdiv_rn(a, 6.0f);
+    const float y = 0x1.555556p-3f;
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-6.0f, q0, a);
+    return __fmaf_rn(r, y, q0);
+}
+
+// Max |x| of 16 BF16 values held as 8 words, and whether any of them is +-0,
+// with the packed BF16 magnitude max/min (max/min.xorsign.abs.bf16x2: the
+// magnitude of the result is max/min(|a|, |b|); its sign is discarded here).
+__device__ __forceinline__ float amax_bf16x16(const uint32_t w[8], bool& any_zero) {
+    uint32_t mx = w[0], mn = w[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+        asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(mx) : "r"(w[i]));
+        asm("min.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(mn) : "r"(w[i]));
+    }
+    mx &= 0x7FFF7FFFu;
+    mn &= 0x7FFF7FFFu;
+    any_zero = (mn & 0xFFFFu) == 0u || (mn >> 16) == 0u;
+    return __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16);
+}
+
+// Max |v| of 16 FP32 values, and whether any of them is +-0.
+__device__ __forceinline__ float amax_f32x16(const float v[16], bool& any_zero) {
+    float mx = 0.0f, mn = fabsf(v[0]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        mx = fmaxf(mx, fabsf(v[i]));
+        mn = fminf(mn, fabsf(v[i]));
+    }
+    any_zero = mn == 0.0f;
+    return mx;
+}
+
+// Number of zero-magnitude codes among the 16 nibbles of two code words.
+__device__ __forceinline__ uint32_t zero_mag_count16(uint32_t lo, uint32_t hi) {
+    const uint32_t a = lo & 0x77777777u, b = hi & 0x77777777u;
+    const uint32_t na = (a | (a >> 1) | (a >> 2)) & 0x11111111u;
+    const uint32_t nb = (b | (b >> 1) | (b >> 2)) & 0x11111111u;
+    return 16u - (uint32_t)__popc(na | (nb << 1));
+}
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3",
 // SC'11): ten rounds of the multiply-xor bijection on a 4 x 32-bit counter with
@@ -185,8 +237,12 @@ __device__ __forceinline__ float exp2_exact(int k) {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        // one 32 x 32 -> 64-bit multiply gives both halves of each product
+        unsigned long long p0, p1;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
         c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;

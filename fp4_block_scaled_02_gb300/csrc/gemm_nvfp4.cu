@@ -62,19 +62,36 @@ struct GemmParams {
     int* status;
 };
 
-template <int BN_, int STAGES_>
+// 256-bit global store (sm_100+), 32-byte aligned destination.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                             uint32_t f, uint32_t g, uint32_t h) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+                 "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
+
+// K values accumulated in tensor memory before the epilogue folds them into
+// FP32 registers (compile-time overridable for accuracy studies)
+#ifndef FP4_GEMM_CHUNK_K
+#define FP4_GEMM_CHUNK_K 1024
+#endif
+
+template <int BN_, int STAGES_, int KSTEPS_, int EPI_ROW_BYTES_>
 struct NvCfg {
     static constexpr int BM = 128, BN = BN_, STAGES = STAGES_;
-    static constexpr int BK = 256;                 // FP4 values per stage = 128 bytes per row
-    static constexpr int CHUNK_STAGES = 4;         // K values per accumulator chunk = 1024
-    static constexpr int A_BYTES = BM * 128;
-    static constexpr int B_BYTES = BN * 128;
-    static constexpr int SFA_BYTES = BM * 16;      // 16 scale blocks of 16 per row per stage
-    static constexpr int SFB_BYTES = BN * 16;
+    static constexpr int KSTEPS = KSTEPS_;         // MMAs (K = 64 each) per stage: 2 or 4
+    static constexpr int BK = 64 * KSTEPS;         // FP4 values per stage
+    static constexpr int ROW_BYTES = BK / 2;       // 64 or 128 bytes per operand row: the swizzle width
+    static constexpr uint64_t SWIZZLE = ROW_BYTES == 128 ? tc::kSwizzle128B : tc::kSwizzle64B;
+    static constexpr int CHUNK_STAGES = FP4_GEMM_CHUNK_K / BK;  // stages per accumulator chunk
+    static constexpr int A_BYTES = BM * ROW_BYTES;
+    static constexpr int B_BYTES = BN * ROW_BYTES;
+    static constexpr int SFA_BYTES = (BM / 128) * 512 * KSTEPS;  // one 512-byte chunk per 128 rows per MMA
+    static constexpr int SFB_BYTES = (BN / 128) * 512 * KSTEPS;
     static constexpr uint32_t TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int NUM_ACC = (BN <= 128) ? 2 : 1;
-    static constexpr int SF_COLS_A = 16;           // 4 MMAs x 4 columns
-    static constexpr int SF_COLS_B = 4 * (BN / 32);  // 4 MMAs x (BN / 32) columns
+    static constexpr int SF_COLS_A = 4 * KSTEPS;           // KSTEPS MMAs x 4 columns
+    static constexpr int SF_COLS_B = KSTEPS * (BN / 32);   // KSTEPS MMAs x (BN / 32) columns
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
     static constexpr int SF_TMEM_BASE = NUM_ACC * BN;
     static constexpr int TMEM_COLS = 512;
@@ -87,7 +104,13 @@ struct NvCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    // output staging: one 32-row x EPI_ROW_BYTES box per epilogue warp, swizzled
+    // with the box row width (128 or 32 bytes)
+    static constexpr int EPI_ROW_BYTES = EPI_ROW_BYTES_;
+    static constexpr int EPI_BOX_BYTES = 32 * EPI_ROW_BYTES;
+    static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
+    static_assert(OFF_EPI % 1024 == 0, "staging boxes must be 1024-byte aligned");
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BOX_BYTES;
     static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
@@ -97,7 +120,7 @@ struct NvCfg {
 template <class Cfg, bool OUT32>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                      const GemmParams p) {
+                      const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -130,6 +153,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tc::mbar_init_fence();
         tc::prefetch_tmap(&tmap_a);
         tc::prefetch_tmap(&tmap_b);
+        tc::prefetch_tmap(&tmap_d);
     }
     if (warp == 1) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -155,17 +179,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         break;
                     }
                     tc::mbar_arrive_expect_tx(full_bar(s), Cfg::TX);
-                    tc::tma_load_2d(sb + Cfg::OFF_A + s * Cfg::A_BYTES, &tmap_a, kb * 128, (int32_t)(mb * Cfg::BM),
-                                    full_bar(s));
-                    tc::tma_load_2d(sb + Cfg::OFF_B + s * Cfg::B_BYTES, &tmap_b, kb * 128, (int32_t)(nb * Cfg::BN),
-                                    full_bar(s));
+                    tc::tma_load_2d(sb + Cfg::OFF_A + s * Cfg::A_BYTES, &tmap_a, kb * Cfg::ROW_BYTES,
+                                    (int32_t)(mb * Cfg::BM), full_bar(s));
+                    tc::tma_load_2d(sb + Cfg::OFF_B + s * Cfg::B_BYTES, &tmap_b, kb * Cfg::ROW_BYTES,
+                                    (int32_t)(nb * Cfg::BN), full_bar(s));
                     tc::bulk_load(sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
-                                  p.a_scales + 512 * (mb * chunks_k + 4 * kb), Cfg::SFA_BYTES, full_bar(s));
+                                  p.a_scales + 512 * (mb * chunks_k + Cfg::KSTEPS * kb), Cfg::SFA_BYTES, full_bar(s));
 #pragma unroll
                     for (int h = 0; h < Cfg::BN / 128; ++h)
-                        tc::bulk_load(sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + 2048 * h,
-                                      p.b_scales + 512 * ((nb * (Cfg::BN / 128) + h) * chunks_k + 4 * kb), 2048,
-                                      full_bar(s));
+                        tc::bulk_load(sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + 512 * Cfg::KSTEPS * h,
+                                      p.b_scales + 512 * ((nb * (Cfg::BN / 128) + h) * chunks_k + Cfg::KSTEPS * kb),
+                                      512 * Cfg::KSTEPS, full_bar(s));
                 }
             }
         }
@@ -205,10 +229,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t a_s = sb + Cfg::OFF_A + s * Cfg::A_BYTES;
                     const uint32_t b_s = sb + Cfg::OFF_B + s * Cfg::B_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        tc::mma_mxf4nvf4(d_tmem, tc::kmajor_sw128_desc(a_s + 32 * kk),
-                                         tc::kmajor_sw128_desc(b_s + 32 * kk), IDESC, sfa_t + 4 * kk,
-                                         sfb_t + (Cfg::BN / 32) * kk, (!first || kk != 0) ? 1u : 0u);
+                    for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
+                        tc::mma_mxf4nvf4(d_tmem, tc::kmajor_swizzled_desc(a_s + 32 * kk, Cfg::ROW_BYTES, Cfg::SWIZZLE),
+                                         tc::kmajor_swizzled_desc(b_s + 32 * kk, Cfg::ROW_BYTES, Cfg::SWIZZLE), IDESC,
+                                         sfa_t + 4 * kk, sfb_t + (Cfg::BN / 32) * kk, (!first || kk != 0) ? 1u : 0u);
                     }
                     tc::commit(empty_bar(s));
                     if (last) {
@@ -243,12 +267,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t sfa_s = sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
                     const uint32_t sfb_s = sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
+                    for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
                         tc::cp_32x128b_warpx4(sfa_t + 4 * kk, tc::scale_chunk_desc(sfa_s + 512 * kk));
 #pragma unroll
                         for (int h = 0; h < Cfg::BN / 128; ++h)
                             tc::cp_32x128b_warpx4(sfb_t + (Cfg::BN / 32) * kk + 4 * h,
-                                                  tc::scale_chunk_desc(sfb_s + 2048 * h + 512 * kk));
+                                                  tc::scale_chunk_desc(sfb_s + 512 * Cfg::KSTEPS * h + 512 * kk));
                     }
                     tc::commit(sf_bar(s));
                 }
@@ -261,6 +285,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // the TMEM lane quadrant this warp may access
         const int half = (warp - Cfg::FIRST_EPI_WARP) >> 2;  // which 128 of the BN columns
+        uint8_t* ebox = smem + Cfg::OFF_EPI + (warp - Cfg::FIRST_EPI_WARP) * Cfg::EPI_BOX_BYTES;
+        const uint32_t ebox_s = sb + Cfg::OFF_EPI + (uint32_t)((warp - Cfg::FIRST_EPI_WARP) * Cfg::EPI_BOX_BYTES);
         const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
         const int nchunks = (num_k + Cfg::CHUNK_STAGES - 1) / Cfg::CHUNK_STAGES;
         uint32_t chunk = 0;
@@ -285,7 +311,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c + i] = __fadd_rn(acc[c + i], __uint_as_float(r[i]));
+                    for (int i = 0; i < 32; i += 2)
+                        f2_unpack(f2_add(f2_pack(acc[c + i], acc[c + i + 1]),
+                                         f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1]))),
+                                  acc[c + i], acc[c + i + 1]);
                 }
                 tc::fence_before_sync();
                 __syncwarp();
@@ -294,36 +323,74 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (!ok) break;
             const int64_t m = mb * Cfg::BM + q * 32 + lane;
             const int64_t n0 = nb * Cfg::BN + half * Cfg::EPI_COLS;
-            if (OUT32) {
-                float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+            if (!p.accumulate) {
+                // stage 32 rows x EPI_ROW_BYTES per box in shared memory (row =
+                // lane; 16-byte chunk c at c ^ (address bits 7.. of the row): the
+                // box-width swizzle, so the eight lanes of each store phase hit
+                // distinct banks) and write the box with one TMA store; the buffer
+                // is refilled once the previous store has read it
+                const int32_t y = (int32_t)(mb * Cfg::BM + q * 32);
+                constexpr int CHUNKS = Cfg::EPI_ROW_BYTES / 16;
+                constexpr int BOX_COLS = OUT32 ? 4 * CHUNKS : 8 * CHUNKS;
+                const int sw = ((lane * Cfg::EPI_ROW_BYTES) >> 7) & (CHUNKS - 1);
 #pragma unroll
-                for (int v = 0; v < Cfg::EPI_COLS / 4; ++v) {
-                    float4 o = make_float4(__fmul_rn(acc[4 * v + 0], alpha), __fmul_rn(acc[4 * v + 1], alpha),
-                                           __fmul_rn(acc[4 * v + 2], alpha), __fmul_rn(acc[4 * v + 3], alpha));
-                    if (p.accumulate) {
-                        const float4 old = reinterpret_cast<const float4*>(dst)[v];
-                        o.x = __fadd_rn(o.x, old.x);
-                        o.y = __fadd_rn(o.y, old.y);
-                        o.z = __fadd_rn(o.z, old.z);
-                        o.w = __fadd_rn(o.w, old.w);
+                for (int bx = 0; bx < Cfg::EPI_COLS / BOX_COLS; ++bx) {
+                    if (lane == 0) tc::bulk_wait_group_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        uint4 o;
+                        if (OUT32) {
+                            const float* a = acc + BOX_COLS * bx + 4 * c;
+                            o = make_uint4(__float_as_uint(__fmul_rn(a[0], alpha)), __float_as_uint(__fmul_rn(a[1], alpha)),
+                                           __float_as_uint(__fmul_rn(a[2], alpha)), __float_as_uint(__fmul_rn(a[3], alpha)));
+                        } else {
+                            const float* a = acc + BOX_COLS * bx + 8 * c;
+                            uint32_t w[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const __nv_bfloat162 h =
+                                    __floats2bfloat162_rn(__fmul_rn(a[2 * k], alpha), __fmul_rn(a[2 * k + 1], alpha));
+                                w[k] = *reinterpret_cast<const uint32_t*>(&h);
+                            }
+                            o = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                        *reinterpret_cast<uint4*>(ebox + lane * Cfg::EPI_ROW_BYTES + ((c ^ sw) << 4)) = o;
                     }
-                    reinterpret_cast<float4*>(dst)[v] = o;
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::tma_store_2d(&tmap_d, ebox_s, (int32_t)(n0 + BOX_COLS * bx), y);
+                        tc::bulk_commit_group();
+                    }
                 }
             } else {
-                uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
+                // D += alpha * sum (FP32 only): each lane reads and writes its own
+                // row with 256-bit accesses (whole 32-byte sectors)
+                float* dst = static_cast<float*>(p.d) + m * p.N + n0;
 #pragma unroll
                 for (int v = 0; v < Cfg::EPI_COLS / 8; ++v) {
-                    uint32_t w[4];
+                    float o[8];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(acc[8 * v + 2 * k], alpha),
-                                                                       __fmul_rn(acc[8 * v + 2 * k + 1], alpha));
-                        w[k] = *reinterpret_cast<const uint32_t*>(&h);
-                    }
-                    reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int k = 0; k < 8; ++k) o[k] = __fmul_rn(acc[8 * v + k], alpha);
+                    const float4 a0 = reinterpret_cast<const float4*>(dst)[2 * v];
+                    const float4 a1 = reinterpret_cast<const float4*>(dst)[2 * v + 1];
+                    o[0] = __fadd_rn(o[0], a0.x);
+                    o[1] = __fadd_rn(o[1], a0.y);
+                    o[2] = __fadd_rn(o[2], a0.z);
+                    o[3] = __fadd_rn(o[3], a0.w);
+                    o[4] = __fadd_rn(o[4], a1.x);
+                    o[5] = __fadd_rn(o[5], a1.y);
+                    o[6] = __fadd_rn(o[6], a1.z);
+                    o[7] = __fadd_rn(o[7], a1.w);
+                    st_global_v8(dst + 8 * v, __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                                 __float_as_uint(o[3]), __float_as_uint(o[4]), __float_as_uint(o[5]),
+                                 __float_as_uint(o[6]), __float_as_uint(o[7]));
                 }
             }
         }
+        // every TMA store this warp issued has completed before the CTA exits
+        if (lane == 0) tc::bulk_wait_group0();
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -355,40 +422,91 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 // 2-D byte-matrix tensor map (rows x row_bytes, row-major) with a box of
-// box_rows x 128 bytes and 128-byte swizzling: each box row is one swizzle atom
-// row of a K-major tcgen05 operand.
-bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+// box_rows x box_bytes (128 or 64) and the swizzle of that width: each box row
+// is one swizzle atom row of a K-major tcgen05 operand.
+bool make_tmap_u8_swizzled(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows,
+                           int box_bytes) {
     EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr) return false;
+    if (fn == nullptr || (box_bytes != 128 && box_bytes != 64)) return false;
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+    return make_tmap_u8_swizzled(map, base, rows, row_bytes, box_rows, 128);
+}
+
+// 2-D BF16 matrix (rows x cols, row-major), unswizzled box_rows x box_cols tiles.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 namespace {
 
+// Output tensor map: rows x cols row-major BF16 or FP32, box of 32 rows x
+// row_bytes (128 or 32) with the swizzle of that width (the epilogue's staging
+// layout).
+bool make_tmap_out(CUtensorMap* map, void* base, int64_t rows, int64_t cols, bool fp32, int row_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr || (row_bytes != 128 && row_bytes != 32)) return false;
+    const cuuint64_t esz = fp32 ? 4 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+    cuuint32_t box[2] = {(cuuint32_t)(row_bytes / esz), 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <class Cfg, bool OUT32>
 cudaError_t run_nvfp4(const GemmJob& j, cudaStream_t st) {
-    CUtensorMap ta, tb;
-    if (!make_tmap_u8_sw128(&ta, j.a_codes, j.M, j.K / 2, Cfg::BM)) return cudaErrorInvalidValue;
-    if (!make_tmap_u8_sw128(&tb, j.b_codes, j.N, j.K / 2, Cfg::BN)) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, td;
+    if (!make_tmap_u8_swizzled(&ta, j.a_codes, j.M, j.K / 2, Cfg::BM, Cfg::ROW_BYTES)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8_swizzled(&tb, j.b_codes, j.N, j.K / 2, Cfg::BN, Cfg::ROW_BYTES)) return cudaErrorInvalidValue;
+    if (!make_tmap_out(&td, j.d, j.M, j.N, OUT32, Cfg::EPI_ROW_BYTES)) return cudaErrorInvalidValue;
     GemmParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status};
     auto kern = gemm_nvfp4_kernel<Cfg, OUT32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (j.M / Cfg::BM) * (j.N / Cfg::BN);
     const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, p);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, td, p);
     return cudaGetLastError();
 }
 
-using NvWide = NvCfg<256, 4>;    // N % 256 == 0
-using NvNarrow = NvCfg<128, 6>;  // N % 128 == 0
+// ring depth, MMAs per stage and output staging box width (compile-time
+// overridable for tuning)
+#ifndef FP4_GEMM_WIDE_STAGES
+#define FP4_GEMM_WIDE_STAGES 4
+#define FP4_GEMM_WIDE_KSTEPS 4
+#define FP4_GEMM_WIDE_EPI 32
+#endif
+#ifndef FP4_GEMM_NARROW_STAGES
+#define FP4_GEMM_NARROW_STAGES 6
+#define FP4_GEMM_NARROW_KSTEPS 4
+#define FP4_GEMM_NARROW_EPI 32
+#endif
+using NvWide = NvCfg<256, FP4_GEMM_WIDE_STAGES, FP4_GEMM_WIDE_KSTEPS, FP4_GEMM_WIDE_EPI>;            // N % 256 == 0
+using NvNarrow = NvCfg<128, FP4_GEMM_NARROW_STAGES, FP4_GEMM_NARROW_KSTEPS, FP4_GEMM_NARROW_EPI>;  // N % 128 == 0
 
 }  // namespace
 

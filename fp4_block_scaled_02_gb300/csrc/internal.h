@@ -85,5 +85,8 @@ cudaError_t launch_gemm_ue5m3(const GemmJob& job, cudaStream_t stream);
 // 2-D byte-matrix TMA descriptor with 128-byte rows per box row and 128-byte
 // swizzling (defined in gemm_nvfp4.cu).
 bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows);
+// 2-D BF16 matrix tensor map with unswizzled box_rows x box_cols tiles (defined
+// in gemm_nvfp4.cu).
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols);
 
 }  // namespace fp4bs

@@ -22,6 +22,7 @@
 
 #include "fp4_device.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace fp4bs {
 
@@ -136,70 +137,65 @@ __device__ __forceinline__ uint32_t sign_nibbles8(const float* v) {
     return s;
 }
 
-// Max |x| and the number of zeros (either sign) of 16 BF16 values held as 8
-// words, computed on the bit patterns (|x| of a BF16 orders like its low 15 bits).
-__device__ __forceinline__ float amax_bf16x16(const uint32_t w[8], uint32_t& nzero) {
-    uint32_t m = 0u, z = 0u;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t a = w[i] & 0x7FFF7FFFu;
-        m = __vmaxu2(m, a);
-        z += (uint32_t)__popc(__vcmpeq2(a, 0u));
-    }
-    nzero = z >> 4;
-    return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
-}
-
-__device__ __forceinline__ float amax_f32x16(const float v[16], uint32_t& nzero) {
-    float m = 0.0f;
-    uint32_t z = 0u;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        m = fmaxf(m, fabsf(v[i]));
-        z += (__float_as_uint(v[i]) << 1) == 0u ? 1u : 0u;
-    }
-    nzero = z;
-    return m;
+// Local encode scale per block-scale code (App. B.2-B.3), one table per
+// operand and CTA: s_enc,L(c) = RN(1 / RN(decode(c) * s_dec,G)) depends only on
+// the code c once the tensor scale is known. Unused codes hold 0.
+template <int FMT>
+__device__ __forceinline__ void fill_enc_table(float* tab, float s_dec) {
+    using F = ScaleFmt<FMT>;
+    for (int c = threadIdx.x; c < 256; c += blockDim.x)
+        tab[c] = (c == 0 || (uint32_t)c > F::kMaxCode) ? 0.0f : __frcp_rn(__fmul_rn(F::decode((uint32_t)c), s_dec));
 }
 
 // Quantize one 1x16 block (App. B.2-B.3): scale in the block format (RNE,
 // satfinite), local encode scale, E2M1 codes packed into two 32-bit words
 // (element i in nibble i). The block's values are w_i = sign_i * pre * v[i]:
-// plain blocks pass pre = 1 and zero sign masks; RHT blocks pass the raw
-// Hadamard butterfly in v, pre = 1/4 and the sign vector as nibble masks
-// (bit 3 of nibble i), so the normalisation and the signs fold into the
-// element scale and the code sign bits. amax_b is max |w_i| and nzero the
-// number of zero w_i. Folding is exact: pre * v[i] is exact, and so is
-// pre * s_enc,L except below 2^-124, where the two products are taken apart.
-// `g0` is the SR group of element 0. Event counts: scale saturation and
-// underflow (when count_scale); element saturation, counted per element only
-// when the scaled block amax exceeds 6 (rounding is monotone, so otherwise no
-// element can); element underflow = zero-magnitude codes minus zero inputs.
-template <int FMT, bool SR>
-__device__ __forceinline__ uint32_t quantize_block16(const float v[16], float amax_b, uint32_t nzero, float pre,
-                                                     uint32_t smask_lo, uint32_t smask_hi, float s_enc, float s_dec,
-                                                     uint64_t g0, const QParams& q, uint32_t& lo, uint32_t& hi,
-                                                     Counts& cnt, bool count_scale) {
+// plain blocks (RHT false) take v as is; RHT blocks pass the raw Hadamard
+// butterfly in v with pre = 1/4 and the sign vector as nibble masks (bit 3 of
+// nibble i), so the normalisation and the signs fold into the element scale
+// and the code sign bits. Folding is exact: pre * v[i] is exact, and so is
+// pre * s_enc,L unless s_enc,L < 2^-124, where the two products are taken
+// apart. vmax is max |v[i]|, any_zero whether some v[i] is +-0; enc_tab holds
+// s_enc,L per scale code (fill_enc_table). `g0` is the SR group of element 0.
+// Event counts: scale saturation and underflow; element saturation, counted
+// per element only when the scaled block max exceeds 6 (rounding is monotone,
+// so otherwise no element can); element underflow = zero-magnitude codes minus
+// zero inputs.
+template <int FMT, bool SR, bool RHT>
+__device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vmax, bool any_zero,
+                                                     const float* enc_tab, float s_enc, uint64_t g0, const QParams& q,
+                                                     uint32_t smask_lo, uint32_t smask_hi, uint32_t& lo, uint32_t& hi,
+                                                     Counts& cnt) {
     using F = ScaleFmt<FMT>;
-    const float s = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const float amax_b = RHT ? __fmul_rn(vmax, 0.25f) : vmax;
+    const float s = __fmul_rn(div6_rn(amax_b), s_enc);
     const uint32_t sc = F::encode(s);
-    if (count_scale) cnt.ssat += s > F::kMax ? 1u : 0u;
+    cnt.ssat += s > F::kMax ? 1u : 0u;
+    uint32_t nzero = 0u;
+    if (any_zero) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) nzero += v[i] == 0.0f ? 1u : 0u;
+    }
     if (sc == 0u) {
-        if (count_scale) cnt.sunder += amax_b > 0.0f ? 1u : 0u;
+        cnt.sunder += amax_b > 0.0f ? 1u : 0u;
         cnt.eunder += 16u - nzero;
         lo = sign_nibbles8(v) ^ smask_lo;
         hi = sign_nibbles8(v + 8) ^ smask_hi;
         return 0u;
     }
-    const float s_enc_l = __frcp_rn(__fmul_rn(F::decode(sc), s_dec));
+    const float enc_l = enc_tab[sc];
     float x[16];
-    if (pre == 1.0f || s_enc_l >= 0x1p-124f) {
-        scale16(v, __fmul_rn(pre, s_enc_l), x);
+    float xmax;
+    if (!RHT || enc_l >= 0x1p-124f) {
+        const float m = RHT ? __fmul_rn(enc_l, 0.25f) : enc_l;
+        scale16(v, m, x);
+        xmax = __fmul_rn(vmax, m);
     } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(__fmul_rn(v[i], pre), s_enc_l);
+        for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(__fmul_rn(v[i], 0.25f), enc_l);
+        xmax = __fmul_rn(amax_b, enc_l);
     }
-    if (__fmul_rn(amax_b, s_enc_l) > 6.0f) {
+    if (xmax > 6.0f) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[i]);
     }
@@ -212,9 +208,11 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float am
         lo = e2m1_rne_x8(x);
         hi = e2m1_rne_x8(x + 8);
     }
-    lo ^= smask_lo;
-    hi ^= smask_hi;
-    cnt.eunder += zero_mag_count8(lo) + zero_mag_count8(hi) - nzero;
+    if (RHT) {
+        lo ^= smask_lo;
+        hi ^= smask_hi;
+    }
+    cnt.eunder += zero_mag_count16(lo, hi) - nzero;
     return sc;
 }
 
@@ -222,26 +220,27 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float am
 // K1: tensor amax partials (App. B.1: one extra pass over the tensor).
 
 // Plain amax over all elements: max of |bf16| as 16-bit integers (BF16 bit
-// patterns of non-negative values order like their values).
-__global__ void __launch_bounds__(kThreads) amax_plain_kernel(const uint4* __restrict__ in, int64_t n_vec,
-                                                              float* __restrict__ partials) {
+// patterns of non-negative values order like their values). Each thread issues
+// eight 16-byte loads before reducing them, so a resident CTA keeps 32 KB of
+// reads in flight.
+constexpr int kAmaxVec = 8;
+
+__global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __restrict__ in, int64_t n_vec,
+                                                                 float* __restrict__ partials) {
     uint32_t m = 0u;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n_vec; i += 4 * stride) {
-        uint4 a = __ldg(in + i), b = __ldg(in + i + stride), c = __ldg(in + i + 2 * stride),
-              d = __ldg(in + i + 3 * stride);
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
-                                 __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
-                                 __vmaxu2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(c.x & 0x7FFF7FFFu, c.y & 0x7FFF7FFFu),
-                                 __vmaxu2(c.z & 0x7FFF7FFFu, c.w & 0x7FFF7FFFu)));
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(d.x & 0x7FFF7FFFu, d.y & 0x7FFF7FFFu),
-                                 __vmaxu2(d.z & 0x7FFF7FFFu, d.w & 0x7FFF7FFFu)));
+    for (; i + (kAmaxVec - 1) * stride < n_vec; i += kAmaxVec * stride) {
+        uint4 v[kAmaxVec];
+#pragma unroll
+        for (int k = 0; k < kAmaxVec; ++k) v[k] = __ldg(in + i + k * stride);
+#pragma unroll
+        for (int k = 0; k < kAmaxVec; ++k)
+            m = __vmaxu2(m, __vmaxu2(__vmaxu2(v[k].x & 0x7FFF7FFFu, v[k].y & 0x7FFF7FFFu),
+                                     __vmaxu2(v[k].z & 0x7FFF7FFFu, v[k].w & 0x7FFF7FFFu)));
     }
     for (; i < n_vec; i += stride) {
-        uint4 a = __ldg(in + i);
+        const uint4 a = __ldg(in + i);
         m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
                                  __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
     }
@@ -288,44 +287,61 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
 // ----------------------------------------------------------------------------
 // K2: rowwise 1x16 quantizer (activations X for Fprop, gradients dY for Dgrad).
 // Flat block index b covers rows x cols/16; block b's elements are the 16
-// consecutive inputs at 16 b, its codes the 8 bytes at 8 b.
+// consecutive inputs at 16 b, its codes the 8 bytes at 8 b. A warp takes 64
+// consecutive blocks per step (lane l: blocks base + l and base + 32 + l), with
+// all four 16-byte loads issued before either block is converted.
 template <int FMT, bool SR, bool TCL>
 __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
+    __shared__ float enc_tab[256];
     float s_enc, s_dec;
     if (!cta_tensor_scale(q, s_enc, s_dec)) return;
+    fill_enc_table<FMT>(enc_tab, s_dec);
+    __syncthreads();
     const int64_t nb_row = q.cols / 16;
     const int64_t nblk = q.rows * nb_row;
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     Counts cnt;
-    for (int64_t base = warp * 32; base < nblk; base += nwarps * 32) {
-        const int64_t b = base + lane;
-        const bool active = b < nblk;
-        uint32_t sc = 0u;
-        if (active) {
-            const uint4 a = ldg16(q.in + 16 * b), c = ldg16(q.in + 16 * b + 8);
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-            uint32_t nzero;
-            const float amax_b = amax_bf16x16(w, nzero);
-            float v[16];
-            unpack16(a, c, v);
-            uint32_t lo, hi;
-            sc = quantize_block16<FMT, SR>(v, amax_b, nzero, 1.0f, 0u, 0u, s_enc, s_dec, (uint64_t)(2 * b), q, lo, hi, cnt,
-                                           true);
-            *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
-        }
-        if (TCL) {
-            // lanes 4k..4k+3 hold the four adjacent scale bytes of one row
-            uint32_t w = sc << (8 * (lane & 3));
-            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
-            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
-            if (active && (lane & 3) == 0) {
-                const int64_t r = b / nb_row, j = b % nb_row;
-                *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(r, j, nb_row)) = w;
+    for (int64_t base = warp * 64; base < nblk; base += nwarps * 64) {
+        uint4 in[2][2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t b = base + 32 * u + lane;
+            if (b < nblk) {
+                in[u][0] = ldg16(q.in + 16 * b);
+                in[u][1] = ldg16(q.in + 16 * b + 8);
             }
-        } else if (active) {
-            q.scales[b] = (uint8_t)sc;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t b = base + 32 * u + lane;
+            const bool active = b < nblk;
+            uint32_t sc = 0u;
+            if (active) {
+                const uint4 a = in[u][0], c = in[u][1];
+                const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+                bool any_zero;
+                const float vmax = amax_bf16x16(w, any_zero);
+                float v[16];
+                unpack16(a, c, v);
+                uint32_t lo, hi;
+                sc = quantize_block16<FMT, SR, false>(v, vmax, any_zero, enc_tab, s_enc, (uint64_t)(2 * b), q, 0u, 0u,
+                                                      lo, hi, cnt);
+                *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
+            }
+            if (TCL) {
+                // lanes 4k..4k+3 hold the four adjacent scale bytes of one row
+                uint32_t w = sc << (8 * (lane & 3));
+                w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+                w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+                if (active && (lane & 3) == 0) {
+                    const int64_t r = b / nb_row, j = b % nb_row;
+                    *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(r, j, nb_row)) = w;
+                }
+            } else if (active) {
+                q.scales[b] = (uint8_t)sc;
+            }
         }
     }
     flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
@@ -340,9 +356,12 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
 // four lanes of a channel write 32 contiguous code bytes and four adjacent
 // scale bytes.
 template <int FMT, bool SR, bool RHT, bool TCL>
-__global__ void __launch_bounds__(kThreads) quantize_cols_kernel(QParams q) {
+__global__ void __launch_bounds__(kThreads, 2) quantize_cols_kernel(QParams q) {
+    __shared__ float enc_tab[256];
     float s_enc, s_dec;
     if (!cta_tensor_scale(q, s_enc, s_dec)) return;
+    fill_enc_table<FMT>(enc_tab, s_dec);
+    __syncthreads();
     const int64_t T = q.rows, C = q.cols;
     const int64_t ug = C / 4, uj = T / 16;
     const int64_t wg_count = (ug + 7) / 8, wj_count = (uj + 3) / 4;
@@ -384,11 +403,11 @@ __global__ void __launch_bounds__(kThreads) quantize_cols_kernel(QParams q) {
                 const int64_t c = 4 * g + 2 * pr + ln;
                 uint32_t lo = 0u, hi = 0u, sc = 0u;
                 if (active) {
-                    uint32_t nzero;
-                    const float amax_v = amax_f32x16(v, nzero);
-                    sc = quantize_block16<FMT, SR>(v, RHT ? __fmul_rn(amax_v, 0.25f) : amax_v, nzero,
-                                                  RHT ? 0.25f : 1.0f, smask_lo, smask_hi, s_enc, s_dec,
-                                                  (uint64_t)((c * T + 16 * j) >> 3), q, lo, hi, cnt, true);
+                    bool any_zero;
+                    const float vmax = amax_f32x16(v, any_zero);
+                    sc = quantize_block16<FMT, SR, RHT>(v, vmax, any_zero, enc_tab, s_enc,
+                                                        (uint64_t)((c * T + 16 * j) >> 3), q, smask_lo, smask_hi, lo,
+                                                        hi, cnt);
                     *reinterpret_cast<uint2*>(q.codes + c * (T / 2) + 8 * j) = make_uint2(lo, hi);
                 }
                 if (TCL) {
@@ -668,20 +687,35 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __r
 constexpr int kDualTT = 64;    // tokens per tile
 constexpr int kDualTC = 128;   // channels per tile
 
-// The conversion pass. A CTA stages a 64-token x 128-channel tile of X in
-// shared memory (the next tile's loads are in flight while this one is
-// converted); each thread then converts two rowwise blocks (16 consecutive
-// channels of one token, two 128-bit shared loads each) and one colwise pair
-// (16 tokens of two adjacent channels, sixteen 32-bit shared loads), so a warp
-// reads 32 consecutive channel pairs of one token row per load and never
-// conflicts on a bank. T % 128 == 0 and C % 128 == 0.
+constexpr int kDualStages = 3;                       // tiles in flight per CTA
+constexpr int kDualTileBytes = kDualTT * kDualTC * 2;  // 16 KB of BF16
+constexpr int kDualSmemBytes = kDualStages * kDualTileBytes + 1024;
+
+// The conversion pass. A CTA walks 64-token x 128-channel tiles of X; one
+// thread keeps kDualStages tiles in flight with TMA loads into a shared-memory
+// ring (an mbarrier per stage), and all threads convert the current tile: two
+// rowwise blocks each (16 consecutive channels of one token, two 128-bit shared
+// loads) and one colwise pair (16 tokens of two adjacent channels, sixteen
+// 32-bit shared loads, so a warp reads 32 consecutive channel pairs of one token
+// row per load and never conflicts on a bank). T % 128 == 0, C % 128 == 0.
 template <int FMT, bool SR_ROW, bool SR_COL, bool RHT>
-__global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QParams qc) {
-    __shared__ __align__(16) uint16_t tile[kDualTT * kDualTC];
+__global__ void __launch_bounds__(kThreads, 2)
+    quantize_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams qr, QParams qc) {
+    extern __shared__ uint8_t dual_smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dual_smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ float tab_r[256], tab_c[256];
+    __shared__ __align__(8) uint64_t full_bar[kDualStages];
     float se_r, sd_r, se_c, sd_c;
     if (!cta_tensor_scale(qr, se_r, sd_r)) return;
     __syncthreads();
     if (!cta_tensor_scale(qc, se_c, sd_c)) return;
+    fill_enc_table<FMT>(tab_r, sd_r);
+    fill_enc_table<FMT>(tab_c, sd_c);
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kDualStages; ++k) tc::mbar_init(tc::smem_u32(&full_bar[k]), 1);
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
     const int64_t T = qr.rows, C = qr.cols;
     const int64_t tiles_c = C / kDualTC, ntiles = (T / kDualTT) * tiles_c;
     const int tid = threadIdx.x, lane = tid & 31;
@@ -690,26 +724,24 @@ __global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QPa
     if (RHT) rht_sign_masks(signs, smask_lo, smask_hi);
     const int64_t nb_row = C / 16, nb_col = T / 16;
     Counts cr, cc;
-    uint4 pre[4];
-    auto load_tile = [&](int64_t t) {
+    auto issue = [&](int64_t t, int s) {
         const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = tid + kThreads * i;  // 16-byte chunk q: row q / 16, chunk q % 16
-            pre[i] = ldg16(qr.in + (t0 + (q >> 4)) * C + c0 + 8 * (q & 15));
-        }
+        const uint32_t bar = tc::smem_u32(&full_bar[s]);
+        tc::mbar_arrive_expect_tx(bar, kDualTileBytes);
+        tc::tma_load_2d(tc::smem_u32(ring + s * kDualTileBytes), &tmap_x, (int32_t)c0, (int32_t)t0, bar);
     };
-    int64_t t = blockIdx.x;
-    if (t < ntiles) load_tile(t);
-    for (; t < ntiles; t += gridDim.x) {
-        __syncthreads();  // the previous tile's readers are done
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = tid + kThreads * i;
-            *reinterpret_cast<uint4*>(&tile[(q >> 4) * kDualTC + 8 * (q & 15)]) = pre[i];
+    if (tid == 0) {
+        tc::prefetch_tmap(&tmap_x);
+        for (int k = 0; k < kDualStages; ++k) {
+            const int64_t tk = blockIdx.x + (int64_t)k * gridDim.x;
+            if (tk < ntiles) issue(tk, k);
         }
-        __syncthreads();
-        if (t + gridDim.x < ntiles) load_tile(t + gridDim.x);
+    }
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = (int)(it % kDualStages);
+        const bool ok = tc::mbar_wait(tc::smem_u32(&full_bar[s]), (it / kDualStages) & 1u, qr.status);
+        const uint16_t* tile = reinterpret_cast<const uint16_t*>(ring + s * kDualTileBytes);
         const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
         // rowwise: blocks k = tid and tid + 256 of the tile's 64 x 8 blocks
 #pragma unroll
@@ -718,15 +750,14 @@ __global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QPa
             const uint4 a = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b]);
             const uint4 c = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b + 8]);
             const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-            uint32_t nzero;
-            const float amax_b = amax_bf16x16(w, nzero);
+            bool any_zero;
+            const float vmax = amax_bf16x16(w, any_zero);
             float v[16];
             unpack16(a, c, v);
             const int64_t row = t0 + r, j = (c0 >> 4) + b, bg = row * nb_row + j;
             uint32_t lo, hi;
-            const uint32_t sc =
-                quantize_block16<FMT, SR_ROW>(v, amax_b, nzero, 1.0f, 0u, 0u, se_r, sd_r, (uint64_t)(2 * bg), qr, lo, hi,
-                                              cr, true);
+            const uint32_t sc = quantize_block16<FMT, SR_ROW, false>(v, vmax, any_zero, tab_r, se_r, (uint64_t)(2 * bg),
+                                                                     qr, 0u, 0u, lo, hi, cr);
             *reinterpret_cast<uint2*>(qr.codes + 8 * bg) = make_uint2(lo, hi);
             uint32_t ww = sc << (8 * (lane & 3));
             ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 1);
@@ -753,16 +784,23 @@ __global__ void __launch_bounds__(kThreads) quantize_dual_kernel(QParams qr, QPa
                     f2_unpack(pv[tt], a, b);
                     v[tt] = ch ? b : a;
                 }
-                uint32_t nzero;
-                const float amax_v = amax_f32x16(v, nzero);
+                bool any_zero;
+                const float vmax = amax_f32x16(v, any_zero);
                 const int64_t c = c0 + 2 * cp + ch;
                 uint32_t lo, hi;
-                const uint32_t sc = quantize_block16<FMT, SR_COL>(
-                    v, RHT ? __fmul_rn(amax_v, 0.25f) : amax_v, nzero, RHT ? 0.25f : 1.0f, smask_lo, smask_hi, se_c,
-                    sd_c, (uint64_t)((c * T + 16 * jg) >> 3), qc, lo, hi, cc, true);
+                const uint32_t sc = quantize_block16<FMT, SR_COL, RHT>(v, vmax, any_zero, tab_c, se_c,
+                                                                       (uint64_t)((c * T + 16 * jg) >> 3), qc,
+                                                                       smask_lo, smask_hi, lo, hi, cc);
                 *reinterpret_cast<uint2*>(qc.codes + c * (T / 2) + 8 * jg) = make_uint2(lo, hi);
                 qc.scales[tc_scale_offset(c, jg, nb_col)] = (uint8_t)sc;
             }
+        }
+        // every thread is done reading stage s (and every wait succeeded):
+        // refill it with the tile kDualStages steps ahead
+        if (!__syncthreads_and(ok)) break;
+        if (tid == 0) {
+            const int64_t tn = t + (int64_t)kDualStages * gridDim.x;
+            if (tn < ntiles) issue(tn, s);
         }
     }
     flush_counters(qr.counters, cr.esat, cr.eunder, cr.ssat, cr.sunder);
@@ -838,7 +876,7 @@ int amax_grid(const QuantJob& j) {
         return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
     }
     const int64_t nvec = j.rows * j.cols / 8;
-    int g = grid_for((nvec + 3) / 4, 8);
+    int g = grid_for((nvec + kAmaxVec - 1) / kAmaxVec, 4);
     return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
 }
 
@@ -946,7 +984,15 @@ cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStr
     const int64_t ntiles = (jr.rows / kDualTT) * (jr.cols / kDualTC);
     const int64_t cap = (int64_t)num_sms() * 2;
     const int grid = (int)(ntiles < cap ? ntiles : cap);
-#define FP4_DUAL(FMT, SR, RHT) quantize_dual_kernel<FMT, SR, SR, RHT><<<grid, kThreads, 0, st>>>(qr, qc)
+    CUtensorMap tmap_x;
+    if (!make_tmap_bf16_2d(&tmap_x, jr.in, jr.rows, jr.cols, kDualTT, kDualTC)) return cudaErrorInvalidValue;
+#define FP4_DUAL(FMT, SR, RHT)                                                                                   \
+    do {                                                                                                         \
+        auto kern = quantize_dual_kernel<FMT, SR, SR, RHT>;                                                      \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDualSmemBytes); \
+        if (e != cudaSuccess) return e;                                                                          \
+        kern<<<grid, kThreads, kDualSmemBytes, st>>>(tmap_x, qr, qc);                                            \
+    } while (0)
     if (jr.scale_fmt == kFmtE4M3) {
         if (jr.sr) { if (jc.rht) FP4_DUAL(kFmtE4M3, true, true); else FP4_DUAL(kFmtE4M3, true, false); }
         else { if (jc.rht) FP4_DUAL(kFmtE4M3, false, true); else FP4_DUAL(kFmtE4M3, false, false); }

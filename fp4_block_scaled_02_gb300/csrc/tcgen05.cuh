@@ -81,6 +81,23 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
+// Tiled 2-D store shared -> global through a tensor map (bulk-group completion):
+// x is the innermost coordinate (elements; x * element size a multiple of 16
+// bytes), the source box lies in shared memory laid out as the map's swizzle
+// mode requires (128-byte swizzle: 1024-byte aligned).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading its
+// shared-memory source (the buffer may be rewritten) ...
+__device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... or has completed entirely.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -159,6 +176,7 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 // stride byte offsets (all >> 4), version 1 at bit 46, swizzle mode at 61-63.
 constexpr uint64_t kSwizzleNone = 0;
 constexpr uint64_t kSwizzle128B = 2;
+constexpr uint64_t kSwizzle64B = 4;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint64_t swizzle) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
@@ -167,6 +185,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // K-major operand tile whose rows are 128-byte swizzle atoms (8 rows = 1024 B).
 __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t addr) { return smem_desc(addr, 16, 1024, kSwizzle128B); }
+
+// K-major operand tile with row_bytes-wide swizzle atoms (128 or 64 bytes; 8
+// rows per atom, so the stride between 8-row groups is 8 * row_bytes).
+__device__ __forceinline__ uint64_t kmajor_swizzled_desc(uint32_t addr, int row_bytes, uint64_t swizzle) {
+    return smem_desc(addr, 16, 8u * (uint32_t)row_bytes, swizzle);
+}
 
 // 32 rows x 16 bytes, unswizzled and contiguous: the source of a block-scale copy.
 __device__ __forceinline__ uint64_t scale_chunk_desc(uint32_t addr) { return smem_desc(addr, 0, 128, kSwizzleNone); }
