@@ -26,13 +26,15 @@
 // time for N = 128 and N = 256, so BN = 256 tiles (one 256-column accumulator)
 // double the work per instruction; BN = 128 tiles (two accumulators) remain for
 // N not divisible by 256.
-// K is accumulated in chunks of 1024 values (CHUNK_STAGES stages): each chunk
+// K is accumulated in chunks of 2048 values (CHUNK_STAGES stages): each chunk
 // starts a fresh accumulator and the epilogue adds the chunk partials in FP32
-// registers with round-to-nearest. Measured on GB300, one accumulator carried
-// over K = 8192 drifts toward zero (every out-of-bound output was smaller in
-// magnitude than the exact sum), a bias that grows with the number of MMAs
-// folded into the accumulator; chunking bounds it by the chunk length instead
-// of K. With two buffers (BN = 128) the epilogue folds chunk c while the MMAs of
+// registers with round-to-nearest. Measured on GB300 with all-positive
+// products at K = 8192 (the worst case for a one-sided bias), the largest
+// error relative to the 2^-20 * sum |a b| bound is 0.19 for 1024- and
+// 2048-value chunks with no sign preference, 0.40 for 4096 with nearly every
+// output too small in magnitude, and 1.48 (out of bound) for one accumulator
+// over all of K: the tensor-core accumulator drifts toward zero as more MMAs
+// fold into it, and chunking bounds that by the chunk length instead of K. With two buffers (BN = 128) the epilogue folds chunk c while the MMAs of
 // chunk c+1 run; with one (BN = 256) the MMAs of the next chunk wait for the
 // fold, but not for the output stores of a finished tile.
 // Every mbarrier wait is bounded (see tcgen05.cuh).
@@ -73,7 +75,7 @@ __device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, ui
 // K values accumulated in tensor memory before the epilogue folds them into
 // FP32 registers (compile-time overridable for accuracy studies)
 #ifndef FP4_GEMM_CHUNK_K
-#define FP4_GEMM_CHUNK_K 1024
+#define FP4_GEMM_CHUNK_K 2048
 #endif
 
 template <int BN_, int STAGES_, int KSTEPS_, int EPI_ROW_BYTES_>
@@ -443,17 +445,20 @@ bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_
     return make_tmap_u8_swizzled(map, base, rows, row_bytes, box_rows, 128);
 }
 
-// 2-D BF16 matrix (rows x cols, row-major), unswizzled box_rows x box_cols tiles.
-bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols) {
+// 2-D BF16 matrix (rows x cols, row-major), box_rows x box_cols tiles, optionally
+// with the 128-byte swizzle (box_cols * 2 == 128 then).
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols,
+                       bool swizzle128) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
+    if (swizzle128 && box_cols * 2 != 128) return false;
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -85,8 +85,9 @@ cudaError_t launch_gemm_ue5m3(const GemmJob& job, cudaStream_t stream);
 // 2-D byte-matrix TMA descriptor with 128-byte rows per box row and 128-byte
 // swizzling (defined in gemm_nvfp4.cu).
 bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows);
-// 2-D BF16 matrix tensor map with unswizzled box_rows x box_cols tiles (defined
-// in gemm_nvfp4.cu).
-bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols);
+// 2-D BF16 matrix tensor map with box_rows x box_cols tiles, unswizzled or with
+// the 128-byte swizzle (defined in gemm_nvfp4.cu).
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols,
+                       bool swizzle128 = false);
 
 }  // namespace fp4bs

@@ -517,6 +517,175 @@ __global__ void __launch_bounds__(kThreads) quantize_2d_kernel(QParams q) {
     flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
 }
 
+// K4b: the same 2D quantizer for N % 64 == 0 and K % 128 == 0, fed by TMA. A CTA
+// walks 64 x 128 tiles of W (kept kTileStages deep in a shared ring, each tile
+// two 64 x 64 boxes with the 128-byte swizzle); a group of 8 lanes owns one
+// 16 x 16 block: lane l converts rows l and l + 8 of W (the block amax is a
+// 3-step shuffle max over the group) and columns 2l and 2l + 1 as rows of W^T,
+// converting the same values with the same scale, so quantize(W)^T ==
+// quantize(W^T) holds by construction. Counters follow W.
+constexpr int kTileStages = 3;
+constexpr int k2dTileBytes = 64 * 128 * 2;
+constexpr int k2dSmemBytes = kTileStages * k2dTileBytes + 1024;
+
+// Byte offset of element (r, c) of a staged 64 x 128 BF16 tile: half c / 64,
+// 128-byte row r, 16-byte chunk ((c % 64) / 8) XOR (r % 8).
+__device__ __forceinline__ uint32_t tile2d_offset(int r, int c) {
+    return (uint32_t)((c >> 6) * 8192 + r * 128 + (((((c & 63) >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1));
+}
+
+template <int FMT, bool TCL_W, bool TCL_WT>
+__global__ void __launch_bounds__(kThreads, 2)
+    quantize_2d_tile_kernel(const __grid_constant__ CUtensorMap tmap_w, QParams q) {
+    extern __shared__ uint8_t tile2d_smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tile2d_smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ float tab[256];
+    __shared__ __align__(8) uint64_t full_bar[kTileStages];
+    float s_enc, s_dec;
+    if (!cta_tensor_scale(q, s_enc, s_dec)) return;
+    fill_enc_table<FMT>(tab, s_dec);
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kTileStages; ++k) tc::mbar_init(tc::smem_u32(&full_bar[k]), 1);
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
+    using F = ScaleFmt<FMT>;
+    const int64_t N = q.rows, K = q.cols, tiles_k = K / 128, ntiles = (N / 64) * tiles_k;
+    const int64_t tk_count = K / 16, tn_count = N / 16;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, l = lane & 7;
+    const int bn = warp >> 1, bk = 4 * (warp & 1) + (lane >> 3);  // this group's block in the tile
+    auto issue = [&](int64_t t, int s) {
+        const int64_t n0 = (t / tiles_k) * 64, k0 = (t % tiles_k) * 128;
+        const uint32_t bar = tc::smem_u32(&full_bar[s]);
+        tc::mbar_arrive_expect_tx(bar, k2dTileBytes);
+        tc::tma_load_2d(tc::smem_u32(ring + s * k2dTileBytes), &tmap_w, (int32_t)k0, (int32_t)n0, bar);
+        tc::tma_load_2d(tc::smem_u32(ring + s * k2dTileBytes + 8192), &tmap_w, (int32_t)(k0 + 64), (int32_t)n0, bar);
+    };
+    if (tid == 0) {
+        tc::prefetch_tmap(&tmap_w);
+        for (int k = 0; k < kTileStages; ++k) {
+            const int64_t tk = blockIdx.x + (int64_t)k * gridDim.x;
+            if (tk < ntiles) issue(tk, k);
+        }
+    }
+    Counts cnt;
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = (int)(it % kTileStages);
+        const bool ok = tc::mbar_wait(tc::smem_u32(&full_bar[s]), (it / kTileStages) & 1u, q.status);
+        const uint8_t* tile = ring + s * k2dTileBytes;
+        const int64_t n0 = (t / tiles_k) * 64, k0 = (t % tiles_k) * 128;
+        // ---- W rows 16 bn + l and 16 bn + l + 8 of the block
+        uint32_t w[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = 16 * bn + l + 8 * h;
+            const uint4 a = *reinterpret_cast<const uint4*>(tile + tile2d_offset(r, 16 * bk));
+            const uint4 c = *reinterpret_cast<const uint4*>(tile + tile2d_offset(r, 16 * bk + 8));
+            w[h][0] = a.x; w[h][1] = a.y; w[h][2] = a.z; w[h][3] = a.w;
+            w[h][4] = c.x; w[h][5] = c.y; w[h][6] = c.z; w[h][7] = c.w;
+        }
+        bool z0, z1;
+        float amax = fmaxf(amax_bf16x16(w[0], z0), amax_bf16x16(w[1], z1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+        float v[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[h][2 * i] = bf16_lo(w[h][i]);
+                v[h][2 * i + 1] = bf16_hi(w[h][i]);
+            }
+        uint32_t nzero = 0u;  // zeros among this lane's 32 values of W
+        if (z0 || z1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) nzero += v[h][i] == 0.0f ? 1u : 0u;
+        }
+        const float sval = __fmul_rn(div6_rn(amax), s_enc);
+        const uint32_t sc = F::encode(sval);
+        if (l == 0) {
+            cnt.ssat += sval > F::kMax ? 1u : 0u;
+            cnt.sunder += (sc == 0u && amax > 0.0f) ? 1u : 0u;
+        }
+        const float enc_l = tab[sc];
+        uint32_t cw[2][2];
+        if (sc == 0u) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                cw[h][0] = sign_nibbles8(v[h]);
+                cw[h][1] = sign_nibbles8(v[h] + 8);
+            }
+            cnt.eunder += 32u - nzero;
+        } else {
+            float x[2][16];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                scale16(v[h], enc_l, x[h]);
+                cw[h][0] = e2m1_rne_x8(x[h]);
+                cw[h][1] = e2m1_rne_x8(x[h] + 8);
+            }
+            if (__fmul_rn(amax, enc_l) > 6.0f) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[h][i]);
+            }
+            cnt.eunder += zero_mag_count16(cw[0][0], cw[0][1]) + zero_mag_count16(cw[1][0], cw[1][1]) - nzero;
+        }
+        if (q.codes != nullptr) {
+            const int64_t jb = (k0 >> 4) + bk;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t n = n0 + 16 * bn + l + 8 * h;
+                *reinterpret_cast<uint2*>(q.codes + n * (K / 2) + (k0 + 16 * bk) / 2) = make_uint2(cw[h][0], cw[h][1]);
+                q.scales[TCL_W ? tc_scale_offset(n, jb, tk_count) : n * tk_count + jb] = (uint8_t)sc;
+            }
+        }
+        // ---- W^T rows k = 16 bk + 2 l and + 1: columns of the block, 16 values along n
+        if (q.codes_t != nullptr) {
+            float c0[16], c1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t ww = *reinterpret_cast<const uint32_t*>(tile + tile2d_offset(16 * bn + i, 16 * bk + 2 * l));
+                c0[i] = bf16_lo(ww);
+                c1[i] = bf16_hi(ww);
+            }
+            uint32_t tw[2][2];
+            if (sc == 0u) {
+                tw[0][0] = sign_nibbles8(c0);
+                tw[0][1] = sign_nibbles8(c0 + 8);
+                tw[1][0] = sign_nibbles8(c1);
+                tw[1][1] = sign_nibbles8(c1 + 8);
+            } else {
+                float x[16];
+                scale16(c0, enc_l, x);
+                tw[0][0] = e2m1_rne_x8(x);
+                tw[0][1] = e2m1_rne_x8(x + 8);
+                scale16(c1, enc_l, x);
+                tw[1][0] = e2m1_rne_x8(x);
+                tw[1][1] = e2m1_rne_x8(x + 8);
+            }
+            const int64_t jb = (n0 >> 4) + bn;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t k = k0 + 16 * bk + 2 * l + h;
+                *reinterpret_cast<uint2*>(q.codes_t + k * (N / 2) + (n0 + 16 * bn) / 2) = make_uint2(tw[h][0], tw[h][1]);
+                q.scales_t[TCL_WT ? tc_scale_offset(k, jb, tn_count) : k * tn_count + jb] = (uint8_t)sc;
+            }
+        }
+        if (!__syncthreads_and(ok)) break;
+        if (tid == 0) {
+            const int64_t tn = t + (int64_t)kTileStages * gridDim.x;
+            if (tn < ntiles) issue(tn, s);
+        }
+    }
+    flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
+}
+
 // ----------------------------------------------------------------------------
 // K5: MXFP4 1x32 rowwise quantizer (section A3, App. B.4): UE8M0 scale = the
 // power of two that rounds amax_B / 6 up, value scaled by 2^-e exactly, RNE.
@@ -838,6 +1007,25 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
             lwt = j.layout_t;
         }
         const bool a = lw == FP4_LAYOUT_TCGEN05, b = lwt == FP4_LAYOUT_TCGEN05;
+        CUtensorMap tmap_w;
+        if (j.rows % 64 == 0 && j.cols % 128 == 0 && make_tmap_bf16_2d(&tmap_w, j.in, j.rows, j.cols, 64, 64, true)) {
+            const int64_t ntiles = (j.rows / 64) * (j.cols / 128);
+            const int64_t cap = (int64_t)num_sms() * 2;
+            const int g2 = (int)(ntiles < cap ? ntiles : cap);
+#define FP4_2D_TILE(TA, TB)                                                                                          \
+    do {                                                                                                            \
+        auto kern = quantize_2d_tile_kernel<FMT, TA, TB>;                                                           \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, k2dSmemBytes);      \
+        if (e != cudaSuccess) return e;                                                                             \
+        kern<<<g2, kThreads, k2dSmemBytes, st>>>(tmap_w, p);                                                        \
+    } while (0)
+            if (a && b) FP4_2D_TILE(true, true);
+            else if (a) FP4_2D_TILE(true, false);
+            else if (b) FP4_2D_TILE(false, true);
+            else FP4_2D_TILE(false, false);
+#undef FP4_2D_TILE
+            return cudaGetLastError();
+        }
         if (a && b) quantize_2d_kernel<FMT, true, true><<<grid, kThreads, 0, st>>>(p);
         else if (a) quantize_2d_kernel<FMT, true, false><<<grid, kThreads, 0, st>>>(p);
         else if (b) quantize_2d_kernel<FMT, false, true><<<grid, kThreads, 0, st>>>(p);

@@ -66,7 +66,10 @@ def test_colwise_1x16_with_rht(case):
     assert_quant_equal(out, oracle_quantize(cfg, bits), layout, cnt)
 
 
-@pytest.mark.parametrize("shape,layout", [((384, 256), TC), ((256, 512), TC), ((48, 80), PLAIN)])
+# N % 64 == 0 and K % 128 == 0 run the TMA-fed tile kernel, other shapes the
+# half-warp-per-block kernel
+@pytest.mark.parametrize("shape,layout", [((384, 256), TC), ((256, 512), TC), ((128, 256), PLAIN), ((48, 80), PLAIN),
+                                          ((256, 144), PLAIN)])
 @pytest.mark.parametrize("orient", [fb.FP4_ORIENT_ROWWISE, fb.FP4_ORIENT_COLWISE])
 def test_weights_2d_both_orientations(shape, layout, orient):
     bits = random_bf16(13, shape, "weight")
@@ -82,6 +85,24 @@ def test_weights_2d_both_orientations(shape, layout, orient):
     ua = np.stack([a & 0xF, a >> 4], axis=-1).reshape(a.shape[0], -1)
     ub = np.stack([b & 0xF, b >> 4], axis=-1).reshape(b.shape[0], -1)
     assert np.array_equal(ua.T, ub)
+
+
+def test_weights_2d_zero_tiny_and_huge_blocks():
+    """Whole 16 x 16 blocks of zeros (scale code 0), blocks of tiny values whose
+    E4M3 scale underflows, and one huge block saturating the other blocks'
+    scales to 448 through a large tensor amax, on the tile kernel's shapes."""
+    rng = np.random.default_rng(21)
+    x = rng.normal(0.0, 0.02, (256, 512)).astype(np.float32)
+    x[0:16, 0:16] = 0.0
+    x[16:32, 32:48] = 0.0
+    x[32:48, 16:32] *= 1e-30
+    x[64:80, 128:144] *= 1e4
+    bits = f32_to_bf16_bits(x)
+    for layout in (TC, PLAIN):
+        cfg = fb.QuantConfig(block=fb.FP4_BLOCK_16x16, layout=layout, emit_transpose=True)
+        out, out_t, cnt = gpu_quantize(cfg, bits, with_transpose=True)
+        assert_quant_equal(out, oracle_quantize(cfg, bits), layout, cnt)
+        assert_quant_equal(out_t, oracle_quantize(cfg, bits, colwise=True), layout)
 
 
 @pytest.mark.parametrize("shape,layout", [((256, 512), TC), ((384, 128), TC), ((10, 64), PLAIN), ((3, 96), PLAIN)])
