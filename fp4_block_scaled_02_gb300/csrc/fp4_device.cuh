@@ -222,12 +222,13 @@ __device__ __forceinline__ float amax_f32x16(const float v[16], bool& any_zero) 
     return mx;
 }
 
-// Number of zero-magnitude codes among the 16 nibbles of two code words.
+// Number of zero-magnitude codes among the 16 nibbles of two code words: a
+// magnitude m <= 7 plus 7 reaches bit 3 of its nibble iff m != 0 (no carry
+// leaves the nibble).
 __device__ __forceinline__ uint32_t zero_mag_count16(uint32_t lo, uint32_t hi) {
-    const uint32_t a = lo & 0x77777777u, b = hi & 0x77777777u;
-    const uint32_t na = (a | (a >> 1) | (a >> 2)) & 0x11111111u;
-    const uint32_t nb = (b | (b >> 1) | (b >> 2)) & 0x11111111u;
-    return 16u - (uint32_t)__popc(na | (nb << 1));
+    const uint32_t na = ((lo & 0x77777777u) + 0x77777777u) & 0x88888888u;
+    const uint32_t nb = ((hi & 0x77777777u) + 0x77777777u) & 0x88888888u;
+    return 16u - (uint32_t)__popc(na | (nb >> 1));
 }
 
 // ---------------------------------------------------------------------------

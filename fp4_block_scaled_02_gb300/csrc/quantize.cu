@@ -892,6 +892,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t smask_lo = 0u, smask_hi = 0u;
     if (RHT) rht_sign_masks(signs, smask_lo, smask_hi);
     const int64_t nb_row = C / 16, nb_col = T / 16;
+    // Per-thread parts of the output offsets (the tile's parts are added per tile;
+    // t0 is a multiple of 64 and c0 of 128, so tile and thread parts separate).
+    // Rowwise blocks (r, b) and (r + 32, b); tensor-core scale offset of row
+    // t0 + r, block c0/16 + b = tile part + 512 (b / 4) + 16 (r % 32) + 4 (r / 32) + b % 4.
+    const int r_row = tid >> 3, b_row = tid & 7;
+    const int64_t code_row_thr = 8 * (int64_t)r_row * nb_row + 8 * b_row;  // + 256 nb_row for r + 32
+    const uint32_t sc_row_thr = 512u * (b_row >> 2) + 16u * (r_row & 31) + (b_row & 3);
+    // Colwise pair: channels c0 + 2 cp + ch, token block t0/16 + jb.
+    const int cp = tid & 63, jb = tid >> 6;
     Counts cr, cc;
     auto issue = [&](int64_t t, int s) {
         const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
@@ -912,30 +921,32 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool ok = tc::mbar_wait(tc::smem_u32(&full_bar[s]), (it / kDualStages) & 1u, qr.status);
         const uint16_t* tile = reinterpret_cast<const uint16_t*>(ring + s * kDualTileBytes);
         const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
-        // rowwise: blocks k = tid and tid + 256 of the tile's 64 x 8 blocks
+        // rowwise: blocks (r, b) and (r + 32, b) of the tile's 64 x 8 blocks
+        const int64_t code_row_tile = 8 * t0 * nb_row + (c0 >> 1);
+        const int64_t sc_row_tile = 512 * ((t0 >> 7) * (nb_row >> 2) + (c0 >> 6)) + ((t0 & 64) >> 3);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int k = tid + kThreads * i, r = k >> 3, b = k & 7;
-            const uint4 a = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b]);
-            const uint4 c = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b + 8]);
+            const int r = r_row + 32 * i;
+            const uint4 a = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b_row]);
+            const uint4 c = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b_row + 8]);
             const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
             bool any_zero;
             const float vmax = amax_bf16x16(w, any_zero);
             float v[16];
             unpack16(a, c, v);
-            const int64_t row = t0 + r, j = (c0 >> 4) + b, bg = row * nb_row + j;
+            const int64_t code_off = code_row_tile + code_row_thr + 256 * i * nb_row;  // = 8 * block index
             uint32_t lo, hi;
-            const uint32_t sc = quantize_block16<FMT, SR_ROW, false>(v, vmax, any_zero, tab_r, se_r, (uint64_t)(2 * bg),
-                                                                     qr, 0u, 0u, lo, hi, cr);
-            *reinterpret_cast<uint2*>(qr.codes + 8 * bg) = make_uint2(lo, hi);
+            const uint32_t sc = quantize_block16<FMT, SR_ROW, false>(v, vmax, any_zero, tab_r, se_r,
+                                                                     (uint64_t)(code_off >> 2), qr, 0u, 0u, lo, hi, cr);
+            *reinterpret_cast<uint2*>(qr.codes + code_off) = make_uint2(lo, hi);
             uint32_t ww = sc << (8 * (lane & 3));
             ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 1);
             ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 2);
-            if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(qr.scales + tc_scale_offset(row, j, nb_row)) = ww;
+            if ((lane & 3) == 0)
+                *reinterpret_cast<uint32_t*>(qr.scales + sc_row_tile + sc_row_thr + 4u * i) = ww;
         }
         // colwise: channel pair cp, token block jb
         {
-            const int cp = tid & 63, jb = tid >> 6;
             f2 pv[16];
 #pragma unroll
             for (int tt = 0; tt < 16; ++tt) {
@@ -943,7 +954,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 pv[tt] = f2_pack(bf16_lo(w), bf16_hi(w));
             }
             if (RHT) wht16x2(pv);
-            const int64_t jg = (t0 >> 4) + jb;
+            const int64_t code_col_tile = c0 * (T >> 1) + (t0 >> 1) + 8 * jb;
+            const int64_t sc_col_tile = 512 * ((c0 >> 7) * (nb_col >> 2) + (t0 >> 6)) + jb;
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
                 float v[16];
@@ -955,13 +967,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 bool any_zero;
                 const float vmax = amax_f32x16(v, any_zero);
-                const int64_t c = c0 + 2 * cp + ch;
+                const int cc_local = 2 * cp + ch;  // channel within the tile
+                const int64_t code_off = code_col_tile + (int64_t)cc_local * (T >> 1);  // = 8 * block index
                 uint32_t lo, hi;
                 const uint32_t sc = quantize_block16<FMT, SR_COL, RHT>(v, vmax, any_zero, tab_c, se_c,
-                                                                       (uint64_t)((c * T + 16 * jg) >> 3), qc,
-                                                                       smask_lo, smask_hi, lo, hi, cc);
-                *reinterpret_cast<uint2*>(qc.codes + c * (T / 2) + 8 * jg) = make_uint2(lo, hi);
-                qc.scales[tc_scale_offset(c, jg, nb_col)] = (uint8_t)sc;
+                                                                       (uint64_t)(code_off >> 2), qc, smask_lo,
+                                                                       smask_hi, lo, hi, cc);
+                *reinterpret_cast<uint2*>(qc.codes + code_off) = make_uint2(lo, hi);
+                qc.scales[sc_col_tile + 16 * (cc_local & 31) + 4 * (cc_local >> 5)] = (uint8_t)sc;
             }
         }
         // every thread is done reading stage s (and every wait succeeded):
