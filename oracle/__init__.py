@@ -106,7 +106,7 @@ def _p(a: np.ndarray):
 class OracleError(RuntimeError):
     def __init__(self, code: int):
         super().__init__({ERR_ARG: "invalid argument", ERR_SHAPE: "bad shape",
-                          ERR_STATE: "held-amax state invalid on a non-refresh step"}.get(code, str(code)))
+                          ERR_STATE: "held-amax state error (reserved)"}.get(code, str(code)))
         self.code = code
 
 
@@ -123,8 +123,8 @@ def e2m1_rne(v: float) -> int:
     return lib().orc_e2m1_rne(v)
 
 
-def e2m1_sr(v: float, r16: int) -> int:
-    return lib().orc_e2m1_sr(v, r16)
+def e2m1_sr(v: float, r: int) -> int:
+    return lib().orc_e2m1_sr(v, r)
 
 
 def scale_encode(fmt: int, s: float) -> int:

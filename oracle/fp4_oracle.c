@@ -164,15 +164,13 @@ uint8_t orc_e2m1_rne(float v) {
 
 /* Stochastic rounding ([NV] 4.4): round |v| to one of its two neighbouring E2M1
  * magnitudes lo <= |v| < hi, choosing hi with probability proportional to the
- * distance from lo. Reading of the random-bit contract: r16 is a uniform 16-bit
- * integer added to the fraction frac = (|v| - lo) / (hi - lo) taken to 16 bits,
- * and the carry out of the sum rounds up:
- *     up  iff  r16 + floor(frac * 2^16) >= 2^16,
- * so P(up) = floor(frac * 2^16) / 2^16, within 2^-16 of frac (the bits of the
- * fraction below 2^-16 are dropped, never rounded up). frac is exact in FP32
- * (Sterbenz lemma: hi <= 2 lo whenever lo > 0, and hi - lo is a power of two),
- * and so is frac * 2^16. |v| >= 6 saturates to 6; the code's sign bit is v's. */
-uint8_t orc_e2m1_sr(float v, uint32_t r16) {
+ * distance from lo. Reading of the random-bit contract: r is one uniform 32-bit
+ * Philox word and the value rounds up iff (float)(r >> 8) < frac * 2^24, where
+ * frac = (|v| - lo) / (hi - lo). frac is exact in FP32 (Sterbenz lemma:
+ * hi <= 2 lo whenever lo > 0, and hi - lo is a power of two), frac * 2^24 and
+ * the 24-bit integer are exact too, so P(up) = ceil(frac * 2^24) / 2^24, within
+ * 2^-24 of frac. |v| >= 6 saturates to 6; the code's sign bit is v's. */
+uint8_t orc_e2m1_sr(float v, uint32_t r) {
     float a = fabsf(v);
     uint8_t sign = signbit(v) ? 8 : 0;
     if (a >= 6.0f) return (uint8_t)(sign | 7);
@@ -181,8 +179,7 @@ uint8_t orc_e2m1_sr(float v, uint32_t r16) {
     float flo = (float)E2M1_MAG[lo];
     float fhi = (float)E2M1_MAG[lo + 1];
     float frac = (a - flo) / (fhi - flo);
-    uint32_t f16 = (uint32_t)floorf(frac * 65536.0f);
-    int up = (r16 & 0xFFFFu) + f16 >= 65536u;
+    int up = (float)(r >> 8) < frac * 16777216.0f;
     return (uint8_t)(sign | (lo + up));
 }
 
@@ -220,14 +217,14 @@ void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint3
 }
 
 /* Reading of the stochastic-rounding bits: element e (row-major linear index in
- * the quantized operand) takes the 16-bit half (e & 1) of word ((e >> 1) & 3) of
- * Philox(key = seed, counter = (lo32(e>>3), hi32(e>>3), tensor_id, lo32(step))). */
+ * the quantized operand) takes word (e & 3) of
+ * Philox(key = seed, counter = (lo32(e>>2), hi32(e>>2), tensor_id, lo32(step))). */
 uint32_t orc_sr_bits(uint64_t seed, uint32_t tensor_id, uint64_t step, uint64_t e) {
-    uint32_t ctr[4] = {(uint32_t)(e >> 3), (uint32_t)(e >> 35), tensor_id, (uint32_t)step};
+    uint32_t ctr[4] = {(uint32_t)(e >> 2), (uint32_t)(e >> 34), tensor_id, (uint32_t)step};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t w[4];
     orc_philox4x32_10(ctr, key, w);
-    return (w[(e >> 1) & 3] >> (16 * (e & 1))) & 0xFFFFu;
+    return w[e & 3];
 }
 
 /* ------------------------------------------------------------------------- */
@@ -341,7 +338,8 @@ float orc_global_encode_scale(float amax, float target_T) {
  * Tensor scale: MXFP4 has none ([NV] A3). Otherwise current scaling uses the
  * amax of this tensor; held scaling ([UE]: the amax is refreshed every
  * `refresh_every` steps and held in between) refreshes when
- * step % refresh_every == 0 and otherwise needs a valid held state. */
+ * step % refresh_every == 0 or when the held state is not valid yet, and
+ * otherwise uses the held amax. */
 int orc_quantize(int scale_fmt, int block, int sr, int colwise, int rht,
                  uint64_t seed, uint32_t tensor_id, uint64_t step,
                  int held, float target_T, uint32_t refresh_every,
@@ -369,13 +367,12 @@ int orc_quantize(int scale_fmt, int block, int sr, int colwise, int rht,
     if (scale_fmt != ORC_FMT_UE8M0) {
         if (held) {
             if (refresh_every == 0) return ORC_ERR_ARG;
-            if (step % refresh_every == 0) {
+            if (step % refresh_every == 0 || !*st_valid) {
                 amax_used = orc_tensor_amax(in, rows, cols, colwise, rht, seed);
                 *st_amax = amax_used;
                 *st_valid = 1;
                 *st_last = step;
             } else {
-                if (!*st_valid) return ORC_ERR_STATE;
                 amax_used = *st_amax;
             }
         } else {

@@ -174,8 +174,12 @@ def test_held_amax_refresh_rule(orc):
     x1 = f32_to_bf16_bits(bf16_bits_to_f32(x0) * np.float32(3.0))
     st = orc.HeldState()
     kw = dict(scale_fmt=orc.FMT_UE5M3, held=True, target_T=2048.0, refresh_every=50, sr=True, seed=2)
-    with pytest.raises(orc.OracleError):
-        orc.quantize(x0, step=7, state=orc.HeldState(), **kw)    # no refresh yet
+    # a state that is not valid yet refreshes on any step, like step 0 would
+    st7 = orc.HeldState()
+    q7 = orc.quantize(x0, step=7, state=st7, **kw)
+    cur7 = orc.quantize(x0, step=7, scale_fmt=orc.FMT_UE5M3, target_T=2048.0, sr=True, seed=2)
+    assert q7["s_dec"] == cur7["s_dec"] and np.array_equal(q7["codes"], cur7["codes"])
+    assert st7.valid[0] == 1 and st7.last[0] == 7
     q0 = orc.quantize(x0, step=0, state=st, **kw)
     cur = orc.quantize(x0, step=0, scale_fmt=orc.FMT_UE5M3, target_T=2048.0, sr=True, seed=2)
     assert np.array_equal(q0["codes"], cur["codes"]) and q0["s_dec"] == cur["s_dec"]
@@ -207,7 +211,7 @@ def test_sr_is_unbiased_over_a_million_draws(orc):
         lo = E2M1[E2M1 <= v].max()
         hi = E2M1[E2M1 > v].min()
         assert set(np.unique(vals)) <= {lo, hi}
-        bound = 5 * (hi - lo) / (2 * np.sqrt(n)) + (hi - lo) * 2.0 ** -16
+        bound = 5 * (hi - lo) / (2 * np.sqrt(n)) + (hi - lo) * 2.0 ** -24
         assert abs(vals.mean() - v) <= bound, (v, vals.mean())
     # RNE path draws nothing
     q1 = orc.quantize(bits, sr=False, seed=1)

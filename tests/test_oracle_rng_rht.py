@@ -60,12 +60,12 @@ def test_philox_matches_triton(orc):
 
 
 def test_sr_bits_index_contract(orc):
-    # element e uses 16-bit half (e & 1) of word ((e >> 1) & 3) of the Philox block e >> 3
+    # element e uses word (e & 3) of the Philox block e >> 2
     seed, tid, step = 0xDEADBEEF12345, 3, 77
-    for e in [0, 1, 2, 7, 8, 9, 1 << 33, (1 << 40) + 5]:
-        w = orc.philox4x32_10([(e >> 3) & 0xFFFFFFFF, (e >> 35) & 0xFFFFFFFF, tid, step & 0xFFFFFFFF],
+    for e in [0, 1, 2, 3, 4, 7, 8, 9, 1 << 33, (1 << 40) + 5]:
+        w = orc.philox4x32_10([(e >> 2) & 0xFFFFFFFF, (e >> 34) & 0xFFFFFFFF, tid, step & 0xFFFFFFFF],
                               [seed & 0xFFFFFFFF, seed >> 32])
-        assert orc.sr_bits(seed, tid, step, e) == (int(w[(e >> 1) & 3]) >> (16 * (e & 1))) & 0xFFFF
+        assert orc.sr_bits(seed, tid, step, e) == int(w[e & 3])
 
 
 def _kron_hadamard(n):
