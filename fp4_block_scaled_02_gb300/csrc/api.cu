@@ -12,8 +12,8 @@
 
 namespace fp4bs {
 
-// Per-device status word: bounded waits that time out and held-amax states
-// used before their first refresh record a code here (first error wins).
+// Per-device status word: bounded waits that time out record a code here
+// (first error wins).
 __device__ int g_device_status;
 
 namespace {
@@ -212,7 +212,7 @@ const char* fp4_status_string(fp4_status_t s) {
         case FP4_ERR_UNSUPPORTED: return "unsupported combination";
         case FP4_ERR_SHAPE: return "unsupported shape";
         case FP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
-        case FP4_ERR_STATE: return "held-amax state invalid on a non-refresh step";
+        case FP4_ERR_STATE: return "held-amax state error (reserved)";
         case FP4_ERR_CUDA: return "CUDA runtime error";
         case FP4_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case FP4_ERR_WORKSPACE: return "workspace missing or too small";

@@ -46,6 +46,7 @@ struct QParams {
     int held, refresh;
     float target_T;
     uint32_t tensor_id, step_lo, key0, key1;
+    uint32_t round_key[20];  // Philox key of round r: (key0 + r W0, key1 + r W1), W the Weyl constants
     uint64_t step;
     int* status;
 };
@@ -72,18 +73,16 @@ __device__ float cta_max(float v) {
 // (uniformly over the CTA) when a held state is needed but invalid.
 __device__ bool cta_tensor_scale(const QParams& q, float& s_enc, float& s_dec) {
     __shared__ float s_amax;
-    __shared__ int s_ok;
-    if (q.held && !q.refresh) {
-        if (threadIdx.x == 0) {
-            s_ok = q.state->valid;
-            s_amax = q.state->amax_held;
-        }
-        __syncthreads();
-        if (!s_ok) {
-            if (blockIdx.x == 0 && threadIdx.x == 0) record_status(q.status, kStatusState);
-            return false;
-        }
-    } else {
+    __shared__ int s_valid;
+    // held scaling refreshes on refresh steps and whenever the held state is
+    // not valid yet (the amax pass then ran; see the amax kernels' skip rule)
+    if (threadIdx.x == 0) {
+        s_valid = (q.held && !q.refresh) ? q.state->valid : 0;
+        s_amax = s_valid ? q.state->amax_held : 0.0f;
+    }
+    __syncthreads();
+    const bool use_held = s_valid != 0;
+    if (!use_held) {
         float m = 0.0f;
         for (int i = threadIdx.x; i < q.npartials; i += blockDim.x) m = fmaxf(m, q.partials[i]);
         m = cta_max(m);
@@ -96,7 +95,7 @@ __device__ bool cta_tensor_scale(const QParams& q, float& s_enc, float& s_dec) {
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (q.s_dec) *q.s_dec = s_dec;
         if (q.s_dec_t) *q.s_dec_t = s_dec;
-        if (q.held && q.refresh) {
+        if (q.held && !use_held) {
             q.state->amax_held = amax;
             q.state->valid = 1;
             q.state->last_refresh_step = q.step;
@@ -156,7 +155,8 @@ __device__ __forceinline__ void fill_enc_table(float* tab, float s_dec) {
 // and the code sign bits. Folding is exact: pre * v[i] is exact, and so is
 // pre * s_enc,L unless s_enc,L < 2^-124, where the two products are taken
 // apart. vmax is max |v[i]|, any_zero whether some v[i] is +-0; enc_tab holds
-// s_enc,L per scale code (fill_enc_table). `g0` is the SR group of element 0.
+// s_enc,L per scale code (fill_enc_table). `g0` = (index of element 0) / 4, the
+// first of the block's four SR groups.
 // Event counts: scale saturation and underflow; element saturation, counted
 // per element only when the scaled block max exceeds 6 (rounding is monotone,
 // so otherwise no element can); element underflow = zero-magnitude codes minus
@@ -200,10 +200,10 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vm
         for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[i]);
     }
     if (SR) {
-        const uint4 r0 = sr_group_bits(g0, q.tensor_id, q.step_lo, q.key0, q.key1);
-        const uint4 r1 = sr_group_bits(g0 + 1, q.tensor_id, q.step_lo, q.key0, q.key1);
-        lo = e2m1_sr_x8(x, r0);
-        hi = e2m1_sr_x8(x + 8, r1);
+        uint4 r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = sr_group_bits_rk(g0 + k, q.tensor_id, q.step_lo, q.round_key);
+        e2m1_sr_x16(x, r, lo, hi);
     } else {
         lo = e2m1_rne_x8(x);
         hi = e2m1_rne_x8(x + 8);
@@ -225,8 +225,16 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vm
 // reads in flight.
 constexpr int kAmaxVec = 8;
 
+// Held scaling on a non-refresh step: the pass is only needed while the held
+// state is not valid yet; with a valid state every CTA returns at once.
+__device__ __forceinline__ bool amax_pass_skipped(const fp4_amax_state_t* a, const fp4_amax_state_t* b) {
+    return a != nullptr && a->valid != 0 && (b == nullptr || b->valid != 0);
+}
+
 __global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __restrict__ in, int64_t n_vec,
-                                                                 float* __restrict__ partials) {
+                                                                 float* __restrict__ partials,
+                                                                 const fp4_amax_state_t* skip_if_valid) {
+    if (amax_pass_skipped(skip_if_valid, nullptr)) return;
     uint32_t m = 0u;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -254,7 +262,9 @@ __global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __
 // the max magnitude. The RHT's signs do not change magnitudes and its 1/4 is an
 // exact scaling, so the max is taken over the raw butterfly and scaled once.
 __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ in, int64_t T,
-                                                                 int64_t C, float* __restrict__ partials) {
+                                                                 int64_t C, float* __restrict__ partials,
+                                                                 const fp4_amax_state_t* skip_if_valid) {
+    if (amax_pass_skipped(skip_if_valid, nullptr)) return;
     const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     float m = 0.0f;
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
                 float v[16];
                 unpack16(a, c, v);
                 uint32_t lo, hi;
-                sc = quantize_block16<FMT, SR, false>(v, vmax, any_zero, enc_tab, s_enc, (uint64_t)(2 * b), q, 0u, 0u,
+                sc = quantize_block16<FMT, SR, false>(v, vmax, any_zero, enc_tab, s_enc, (uint64_t)(4 * b), q, 0u, 0u,
                                                       lo, hi, cnt);
                 *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
             }
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_cols_kernel(QParams q) {
                     bool any_zero;
                     const float vmax = amax_f32x16(v, any_zero);
                     sc = quantize_block16<FMT, SR, RHT>(v, vmax, any_zero, enc_tab, s_enc,
-                                                        (uint64_t)((c * T + 16 * j) >> 3), q, smask_lo, smask_hi, lo,
+                                                        (uint64_t)((c * T + 16 * j) >> 2), q, smask_lo, smask_hi, lo,
                                                         hi, cnt);
                     *reinterpret_cast<uint2*>(q.codes + c * (T / 2) + 8 * j) = make_uint2(lo, hi);
                 }
@@ -814,7 +824,10 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __r
 template <bool RHT>
 __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __restrict__ in, int64_t T, int64_t C,
                                                              float* __restrict__ partials_row,
-                                                             float* __restrict__ partials_col) {
+                                                             float* __restrict__ partials_col,
+                                                             const fp4_amax_state_t* skip_row,
+                                                             const fp4_amax_state_t* skip_col) {
+    if (amax_pass_skipped(skip_row, skip_col)) return;
     const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     uint32_t mr = 0u;
@@ -937,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int64_t code_off = code_row_tile + code_row_thr + 256 * i * nb_row;  // = 8 * block index
             uint32_t lo, hi;
             const uint32_t sc = quantize_block16<FMT, SR_ROW, false>(v, vmax, any_zero, tab_r, se_r,
-                                                                     (uint64_t)(code_off >> 2), qr, 0u, 0u, lo, hi, cr);
+                                                                     (uint64_t)(code_off >> 1), qr, 0u, 0u, lo, hi, cr);
             *reinterpret_cast<uint2*>(qr.codes + code_off) = make_uint2(lo, hi);
             uint32_t ww = sc << (8 * (lane & 3));
             ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 1);
@@ -971,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int64_t code_off = code_col_tile + (int64_t)cc_local * (T >> 1);  // = 8 * block index
                 uint32_t lo, hi;
                 const uint32_t sc = quantize_block16<FMT, SR_COL, RHT>(v, vmax, any_zero, tab_c, se_c,
-                                                                       (uint64_t)(code_off >> 2), qc, smask_lo,
+                                                                       (uint64_t)(code_off >> 1), qc, smask_lo,
                                                                        smask_hi, lo, hi, cc);
                 *reinterpret_cast<uint2*>(qc.codes + code_off) = make_uint2(lo, hi);
                 qc.scales[sc_col_tile + 16 * (cc_local & 31) + 4 * (cc_local >> 5)] = (uint8_t)sc;
@@ -1103,6 +1116,10 @@ QParams make_params(const QuantJob& j) {
     q.step_lo = (uint32_t)j.step;
     q.key0 = (uint32_t)j.seed;
     q.key1 = (uint32_t)(j.seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        q.round_key[2 * r] = q.key0 + (uint32_t)r * kPhiloxW0;
+        q.round_key[2 * r + 1] = q.key1 + (uint32_t)r * kPhiloxW1;
+    }
     q.status = j.status;
     return q;
 }
@@ -1111,9 +1128,8 @@ QParams make_params(const QuantJob& j) {
 
 int amax_partials_needed(const QuantJob& j) {
     if (j.scale_fmt == kFmtUE8M0) return 0;
-    if (j.held && !j.refresh) return 0;
     if (j.rows == 0 || j.cols == 0) return 0;
-    return amax_grid(j);
+    return amax_grid(j);  // held non-refresh steps too: the state may not be valid yet
 }
 
 cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
@@ -1130,9 +1146,10 @@ cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
     const int np = amax_partials_needed(j);
     q.npartials = np;
     if (np > 0) {
-        if (j.rht) amax_rht_cols_kernel<<<np, kThreads, 0, st>>>(j.in, j.rows, j.cols, j.partials);
+        const fp4_amax_state_t* skip = (j.held && !j.refresh) ? j.state : nullptr;
+        if (j.rht) amax_rht_cols_kernel<<<np, kThreads, 0, st>>>(j.in, j.rows, j.cols, j.partials, skip);
         else amax_plain_kernel<<<np, kThreads, 0, st>>>(reinterpret_cast<const uint4*>(j.in), j.rows * j.cols / 8,
-                                                         j.partials);
+                                                         j.partials, skip);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -1171,14 +1188,19 @@ int dual_amax_grid(const QuantJob& jc) {
 cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStream_t st) {
     if (jr.rows == 0 || jr.cols == 0) return cudaSuccess;
     QParams qr = make_params(jr), qc = make_params(jc);
-    const bool amax_pass = !(jr.held && !jr.refresh);
-    if (amax_pass) {
+    {
+        // held non-refresh steps: the pass runs only while a held state is not valid yet
+        const bool held_step = jr.held && !jr.refresh;
+        const fp4_amax_state_t* skip_r = held_step ? jr.state : nullptr;
+        const fp4_amax_state_t* skip_c = held_step ? jc.state : nullptr;
         const int np = dual_amax_grid(jc);
         qr.npartials = qc.npartials = np;
         if (jc.rht)
-            amax_dual_kernel<true><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials);
+            amax_dual_kernel<true><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
+                                                             skip_c);
         else
-            amax_dual_kernel<false><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials);
+            amax_dual_kernel<false><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
+                                                              skip_c);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -23,9 +23,8 @@
  *     passed as void*; NULL = legacy default stream) and the call returns before
  *     it completes. Argument checks run synchronously on the host first: a call
  *     that fails them returns an error and enqueues nothing.
- *   - Device-side errors (a bounded wait that timed out, a held-amax state that
- *     was never refreshed) are recorded in a per-device status word read by
- *     fp4_device_status().
+ *   - Device-side errors (a bounded wait that timed out) are recorded in a
+ *     per-device status word read by fp4_device_status().
  *   - Shapes: an operand is `rows x cols` with `cols` the dot-product dimension
  *     (K-major); BF16 inputs are row-major with leading dimension = cols.
  */
@@ -45,7 +44,7 @@ typedef enum {
     FP4_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination */
     FP4_ERR_SHAPE = 3,         /* dimension not a multiple the path needs */
     FP4_ERR_ALIGNMENT = 4,     /* pointer not 16-byte aligned */
-    FP4_ERR_STATE = 5,         /* held-amax state invalid on a non-refresh step */
+    FP4_ERR_STATE = 5,         /* reserved (an invalid held state now triggers a refresh) */
     FP4_ERR_CUDA = 6,          /* a CUDA runtime call failed */
     FP4_ERR_DEVICE_TIMEOUT = 7,/* a bounded device-side wait gave up */
     FP4_ERR_WORKSPACE = 8      /* workspace missing or too small */
@@ -65,7 +64,8 @@ typedef enum { FP4_BLOCK_1x16 = 0, FP4_BLOCK_16x16 = 1, FP4_BLOCK_1x32 = 2 } fp4
 typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_round_t;
 
 /* Tensor scale: per-call amax (App. B.1) or held amax refreshed when
- * step % refresh_every == 0 (UE5M3 page: refresh every 50 steps). */
+ * step % refresh_every == 0 or when the held state is not valid yet (UE5M3
+ * page: refresh every 50 steps); other steps use the held amax. */
 typedef enum { FP4_TSCALE_CURRENT = 0, FP4_TSCALE_HELD = 1 } fp4_tscale_t;
 
 /* ROWWISE: the operand is the input itself (blocks run along its columns).
@@ -137,9 +137,9 @@ size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t co
  *              for COLWISE); codes, scales and s_dec_global are written.
  *   out_t    : 16x16 with emit_transpose: the transposed operand (cols x rows)
  *              with the same codes and scales transposed (section 4.3); else NULL.
- *   state    : held-amax record (FP4_TSCALE_HELD), else NULL. On refresh steps it
- *              is written; on other steps it must be valid (else the device status
- *              becomes FP4_ERR_STATE and nothing is written).
+ *   state    : held-amax record (FP4_TSCALE_HELD), else NULL. Refresh steps, and
+ *              steps that find it not valid yet, compute the amax and write it;
+ *              other steps use it (their amax pass returns at once).
  *   counters : NULL or 4 device uint64: elem_sat, elem_underflow, scale_sat,
  *              scale_underflow; the call ADDS its counts (the caller zeroes).
  *   ws       : device workspace of fp4_workspace_bytes() bytes (any content).

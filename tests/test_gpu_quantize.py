@@ -133,15 +133,20 @@ def test_ue5m3_current_and_held_amax():
     assert_quant_equal(out, oracle_quantize(cfg, base), TC, cnt)
 
 
-def test_held_state_invalid_on_non_refresh_step_sets_status():
+def test_held_state_not_valid_refreshes_on_a_non_refresh_step():
+    # the held amax refreshes on step % 50 == 0 and also whenever the state is
+    # not valid yet; afterwards non-refresh steps hold it
     assert fb.fp4_device_status() == 0
     bits = random_bf16(16, (128, 64), "normal")
-    cfg = fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE5M3, tscale=fb.FP4_TSCALE_HELD, target_T=2048.0, step=7)
-    out, _, cnt = gpu_quantize(cfg, bits, state=fb.AmaxState())
-    assert fb.fp4_device_status() == fb._lib.FP4_ERR_STATE
-    assert fb.fp4_device_status() == 0          # reading clears it
-    assert np.all(out.codes.cpu().numpy() == 0xAA)   # nothing written
-    assert int(cnt.sum()) == 0
+    state, ostate = fb.AmaxState(), oracle.HeldState()
+    for step, factor in [(7, 1.0), (8, 100.0)]:
+        x = f32_to_bf16_bits(bf16_bits_to_f32(bits) * np.float32(factor))
+        cfg = fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE5M3, tscale=fb.FP4_TSCALE_HELD, target_T=2048.0, step=step)
+        out, _, cnt = gpu_quantize(cfg, x, state=state)
+        ref = oracle_quantize(cfg, x, state=ostate)
+        assert_quant_equal(out, ref, TC, cnt)
+        assert state.valid == 1 and state.last_refresh_step == 7 == int(ostate.last[0])
+    assert fb.fp4_device_status() == 0
 
 
 def test_current_scaling_nvfp4_large_values_and_zero_tensor():
