@@ -10,18 +10,23 @@
 // in BF16; a BF16 x BF16 tensor-core MMA with FP32 accumulation then computes
 // the same products the native path would.
 //
-// Design (one persistent CTA per SM, 128 x 128 output tiles, 320 threads):
-//   warp 0    : TMA producer -- raw FP4 code tiles (K = 256) and scale chunks;
-//   warps 2-5 : decode -- per K = 64 slice, each thread expands its row's
-//               16-byte code chunks into BF16 with byte-permute table lookups,
-//               multiplies by the block scale (packed BF16 multiply, exact) and
-//               writes the 128-byte-swizzled K-major layout the tensor core reads;
-//   warp 1    : one lane issues tcgen05.mma kind::f16 (K = 16) on each decoded
-//               slice and commits it back to the decoders;
-//   warps 6-9 : epilogue: each raw stage (K = 256) is one accumulator chunk in
-//               one of two tensor-memory buffers; the epilogue folds the chunk
-//               partials in FP32 registers with round-to-nearest (the same
-//               bias control as the NVFP4 kernel), then stores alpha * sum.
+// Design (one persistent CTA per SM, 128 x 128 output tiles, 704 threads):
+//   warp 0      : TMA producer -- raw FP4 code tiles (K = 256) and scale chunks;
+//   warps 2-17  : decode -- per K = 64 slice, each thread expands one 16-byte
+//                 raw chunk (32 values) of one operand row into BF16 with
+//                 byte-permute table lookups, multiplies by the block scale
+//                 (packed BF16 multiply, exact) and writes the 128-byte-swizzled
+//                 K-major layout the tensor core reads. Sixteen warps keep four
+//                 per scheduler: measured on GB300, four decode warps (one per
+//                 scheduler) left the MMA waiting for decoded data 66 % of the time;
+//   warp 1      : one lane issues tcgen05.mma kind::f16 (K = 16) on each decoded
+//                 slice and commits it back to the decoders;
+//   warps 18-21 : epilogue -- each raw stage (K = 256) is one accumulator chunk in
+//                 one of two tensor-memory buffers; the epilogue adds the chunk
+//                 to a running FP32 sum kept in a third tensor-memory region
+//                 (tcgen05.ld both, add with round-to-nearest, tcgen05.st), so no
+//                 accumulator lives in registers, and at the last chunk of a tile
+//                 stores alpha * (sum + chunk).
 #include <cstdint>
 
 #include <cuda.h>
@@ -48,6 +53,7 @@ struct EmuParams {
 
 struct EmuCfg {
     static constexpr int BM = 128, BN = 128, BK = 256;
+    static constexpr int DEC_WARPS = 16, FIRST_DEC_WARP = 2, EPI_WARPS = 4, FIRST_EPI_WARP = 18;
     static constexpr int RAW_STAGES = 3, DEC_STAGES = 3;
     static constexpr int RAW_A = BM * 128, RAW_B = BN * 128;     // FP4 codes, 128 B per row
     static constexpr int RAW_SFA = BM * 16, RAW_SFB = BN * 16;   // 16 scale blocks per row
@@ -63,8 +69,9 @@ struct EmuCfg {
     static constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * DEC_STAGES + 4 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int THREADS = 320;
-    static constexpr int TMEM_COLS = 256;  // two 128-column FP32 accumulators
+    static constexpr int THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS);
+    static constexpr int TMEM_COLS = 512;  // two 128-column chunk accumulators + the running sum
+    static constexpr int SUM_COL = 2 * BN;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -100,12 +107,12 @@ __device__ __forceinline__ __nv_bfloat162 ue5m3_bf16x2(uint32_t code) {
     return __nv_bfloat162(h, h);
 }
 
-// Decode one operand row's two 16-byte raw chunks (K = 64 values) of slice kk
-// into the swizzled BF16 row of the decoded tile.
-__device__ __forceinline__ void decode_row(const uint8_t* raw, const uint8_t* sf, uint8_t* dec, int r, int kk) {
+// Decode half h (one 16-byte raw chunk, 32 values) of an operand row's K = 64
+// slice kk into the swizzled BF16 row of the decoded tile.
+__device__ __forceinline__ void decode_half(const uint8_t* raw, const uint8_t* sf, uint8_t* dec, int r, int kk,
+                                            int h) {
     const int sw = r & 7;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    {
         const int cr = 2 * kk + h;  // raw 16-byte chunk: values 32 cr .. 32 cr + 31 of the 256
         const uint4 codes = *reinterpret_cast<const uint4*>(raw + r * 128 + ((cr ^ sw) << 4));
         const uint16_t s2 =
@@ -146,15 +153,15 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < C::RAW_STAGES; ++s) {
             tc::mbar_init(raw_full(s), 1);
-            tc::mbar_init(raw_empty(s), 4);
+            tc::mbar_init(raw_empty(s), C::DEC_WARPS);
         }
         for (int s = 0; s < C::DEC_STAGES; ++s) {
-            tc::mbar_init(dec_full(s), 4);
+            tc::mbar_init(dec_full(s), C::DEC_WARPS);
             tc::mbar_init(dec_empty(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(accf(a), 1);
-            tc::mbar_init(acce(a), 4);
+            tc::mbar_init(acce(a), C::EPI_WARPS);
         }
         tc::mbar_init(drain, 1);
         tc::mbar_init_fence();
@@ -195,9 +202,10 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
                 }
             }
         }
-    } else if (warp >= 2 && warp < 6) {
+    } else if (warp >= C::FIRST_DEC_WARP && warp < C::FIRST_DEC_WARP + C::DEC_WARPS) {
         // ------------------------------------------------------------ decoders
-        const int r = threadIdx.x - 64;  // operand row 0..127 of the tile
+        const int t = threadIdx.x - 32 * C::FIRST_DEC_WARP;  // 0 .. 511
+        const int op = t >> 8, h = (t >> 7) & 1, r = t & 127;  // operand (A/B), raw chunk half, row
         uint32_t it_raw = 0, it_dec = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -207,18 +215,16 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint8_t* raw_a = smem + C::OFF_RAW_A + rs * C::RAW_A;
-                const uint8_t* raw_b = smem + C::OFF_RAW_B + rs * C::RAW_B;
-                const uint8_t* sfa = smem + C::OFF_SFA + rs * C::RAW_SFA;
-                const uint8_t* sfb = smem + C::OFF_SFB + rs * C::RAW_SFB;
+                const uint8_t* raw = op ? smem + C::OFF_RAW_B + rs * C::RAW_B : smem + C::OFF_RAW_A + rs * C::RAW_A;
+                const uint8_t* sf = op ? smem + C::OFF_SFB + rs * C::RAW_SFB : smem + C::OFF_SFA + rs * C::RAW_SFA;
                 for (int kk = 0; kk < 4; ++kk, ++it_dec) {
                     const int ds = (int)(it_dec % C::DEC_STAGES);
                     if (!tc::mbar_wait(dec_empty(ds), ((it_dec / C::DEC_STAGES) & 1u) ^ 1u, p.status)) {
                         ok = false;
                         break;
                     }
-                    decode_row(raw_a, sfa, smem + C::OFF_DEC_A + ds * C::DEC_A, r, kk);
-                    decode_row(raw_b, sfb, smem + C::OFF_DEC_B + ds * C::DEC_B, r, kk);
+                    decode_half(raw, sf, op ? smem + C::OFF_DEC_B + ds * C::DEC_B : smem + C::OFF_DEC_A + ds * C::DEC_A,
+                                r, kk, h);
                     tc::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(dec_full(ds));
@@ -264,17 +270,16 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
             tc::commit(drain);
             tc::mbar_wait(drain, 0, p.status);
         }
-    } else {
-        // ------------------------------------------------------------ epilogue (warps 6-9)
-        const int q = warp & 3;
+    } else if (warp >= C::FIRST_EPI_WARP) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // the TMEM lane quadrant this warp may access
         const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t chunk = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
             const int64_t mb = tile % num_m, nb = tile / num_m;
-            float acc[C::BN];
-#pragma unroll
-            for (int c = 0; c < C::BN; ++c) acc[c] = 0.0f;
+            const int64_t m = mb * C::BM + q * 32 + lane;
             for (int kb = 0; kb < num_k; ++kb, ++chunk) {
                 const int buf = (int)(chunk & 1u);
                 if (!tc::mbar_wait(accf(buf), (chunk >> 1) & 1u, p.status)) {
@@ -282,50 +287,71 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::BN);
-#pragma unroll
+                const bool first = kb == 0, last = kb == num_k - 1;
+#pragma unroll 1
                 for (int c = 0; c < C::BN; c += 32) {
-                    uint32_t rr[32];
-                    tc::tmem_ld_32x32b_x32(t_row + (uint32_t)c, rr);
+                    uint32_t rc[32], rs[32];
+                    tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(buf * C::BN + c), rc);
+                    if (!first) tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(C::SUM_COL + c), rs);
                     tc::tmem_ld_wait();
+                    if (first) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c + i] = __fadd_rn(acc[c + i], __uint_as_float(rr[i]));
+                        for (int i = 0; i < 32; ++i) rs[i] = rc[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float a0, a1;
+                            f2_unpack(f2_add(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])),
+                                             f2_pack(__uint_as_float(rc[i]), __uint_as_float(rc[i + 1]))),
+                                      a0, a1);
+                            rs[i] = __float_as_uint(a0);
+                            rs[i + 1] = __float_as_uint(a1);
+                        }
+                    }
+                    if (!last) {
+                        tc::tmem_st_32x32b_x32(lane_base + (uint32_t)(C::SUM_COL + c), rs);
+                        continue;
+                    }
+                    // last chunk of the tile: alpha * sum to the output row m, columns n0 + c ..
+                    const int64_t n0 = nb * C::BN + c;
+                    if (OUT32) {
+                        float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+#pragma unroll
+                        for (int v = 0; v < 32; v += 4) {
+                            float4 o = make_float4(__fmul_rn(__uint_as_float(rs[v]), alpha),
+                                                   __fmul_rn(__uint_as_float(rs[v + 1]), alpha),
+                                                   __fmul_rn(__uint_as_float(rs[v + 2]), alpha),
+                                                   __fmul_rn(__uint_as_float(rs[v + 3]), alpha));
+                            if (p.accumulate) {
+                                const float4 old = *reinterpret_cast<const float4*>(dst + v);
+                                o.x = __fadd_rn(o.x, old.x);
+                                o.y = __fadd_rn(o.y, old.y);
+                                o.z = __fadd_rn(o.z, old.z);
+                                o.w = __fadd_rn(o.w, old.w);
+                            }
+                            *reinterpret_cast<float4*>(dst + v) = o;
+                        }
+                    } else {
+                        uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
+#pragma unroll
+                        for (int v = 0; v < 32; v += 8) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const __nv_bfloat162 hh =
+                                    __floats2bfloat162_rn(__fmul_rn(__uint_as_float(rs[v + 2 * k]), alpha),
+                                                          __fmul_rn(__uint_as_float(rs[v + 2 * k + 1]), alpha));
+                                w[k] = *reinterpret_cast<const uint32_t*>(&hh);
+                            }
+                            *reinterpret_cast<uint4*>(dst + v) = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
                 }
+                // the running sum is written before this warp's next loads of it
+                if (!last) tc::tmem_st_wait();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(acce(buf));
-            }
-            if (!ok) break;
-            const int64_t m = mb * C::BM + q * 32 + lane;
-            const int64_t n0 = nb * C::BN;
-            if (OUT32) {
-                float* dst = static_cast<float*>(p.d) + m * p.N + n0;
-#pragma unroll
-                for (int v = 0; v < C::BN / 4; ++v) {
-                    float4 o = make_float4(__fmul_rn(acc[4 * v + 0], alpha), __fmul_rn(acc[4 * v + 1], alpha),
-                                           __fmul_rn(acc[4 * v + 2], alpha), __fmul_rn(acc[4 * v + 3], alpha));
-                    if (p.accumulate) {
-                        const float4 old = reinterpret_cast<const float4*>(dst)[v];
-                        o.x = __fadd_rn(o.x, old.x);
-                        o.y = __fadd_rn(o.y, old.y);
-                        o.z = __fadd_rn(o.z, old.z);
-                        o.w = __fadd_rn(o.w, old.w);
-                    }
-                    reinterpret_cast<float4*>(dst)[v] = o;
-                }
-            } else {
-                uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
-#pragma unroll
-                for (int v = 0; v < C::BN / 8; ++v) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(acc[8 * v + 2 * k], alpha),
-                                                                       __fmul_rn(acc[8 * v + 2 * k + 1], alpha));
-                        w[k] = *reinterpret_cast<const uint32_t*>(&h);
-                    }
-                    reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
             }
         }
     }
