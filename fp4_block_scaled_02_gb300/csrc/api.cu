@@ -82,7 +82,9 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     if (mx != (p->block == FP4_BLOCK_1x32)) return FP4_ERR_INVALID_ARG;
     if (p->rht && (p->block != FP4_BLOCK_1x16 || p->orient != FP4_ORIENT_COLWISE)) return FP4_ERR_INVALID_ARG;
     if (mx && (p->round != FP4_ROUND_RNE || p->orient != FP4_ORIENT_ROWWISE)) return FP4_ERR_UNSUPPORTED;
-    if (p->block == FP4_BLOCK_16x16 && p->round != FP4_ROUND_RNE) return FP4_ERR_UNSUPPORTED;
+    // 16x16 with SR runs only on the TMA tile path: whole 64 x 128 input tiles
+    if (p->block == FP4_BLOCK_16x16 && p->round != FP4_ROUND_RNE && (rows % 64 != 0 || cols % 128 != 0))
+        return FP4_ERR_UNSUPPORTED;
     if (p->emit_transpose && p->block != FP4_BLOCK_16x16) return FP4_ERR_INVALID_ARG;
     if (p->emit_transpose && out_t == nullptr) return FP4_ERR_INVALID_ARG;
     const bool held = !mx && p->tscale == FP4_TSCALE_HELD;
@@ -323,8 +325,8 @@ fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int
     if (d == nullptr) return FP4_ERR_INVALID_ARG;
     if (!aligned16(d)) return FP4_ERR_ALIGNMENT;
     if (accumulate && !out_fp32) return FP4_ERR_INVALID_ARG;
-    if (a->scale_fmt != b->scale_fmt || a->block_k != 16 || b->block_k != 16) return FP4_ERR_UNSUPPORTED;
-    if (a->scale_fmt == FP4_SCALE_UE8M0) return FP4_ERR_UNSUPPORTED;
+    const int bs = a->scale_fmt == FP4_SCALE_UE8M0 ? 32 : 16;
+    if (a->scale_fmt != b->scale_fmt || a->block_k != bs || b->block_k != bs) return FP4_ERR_UNSUPPORTED;
     if (a->scale_layout != FP4_LAYOUT_TCGEN05 || b->scale_layout != FP4_LAYOUT_TCGEN05) return FP4_ERR_UNSUPPORTED;
     if (a->cols != b->cols) return FP4_ERR_SHAPE;
     if (a->rows % 128 != 0 || b->rows % 128 != 0 || a->cols % 256 != 0 || a->cols <= 0 || a->rows <= 0 ||
@@ -347,7 +349,7 @@ fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int
     j.status = device_status_ptr();
     if (j.status == nullptr) return FP4_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (a->scale_fmt == FP4_SCALE_E4M3) return from_cuda(launch_gemm_nvfp4(j, st));
+    if (a->scale_fmt != FP4_SCALE_UE5M3) return from_cuda(launch_gemm_nvfp4(j, st));  // NVFP4 and MXFP4
     return from_cuda(launch_gemm_ue5m3(j, st));
 }
 

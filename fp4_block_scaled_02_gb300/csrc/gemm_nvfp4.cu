@@ -6,7 +6,9 @@
 // multiplies each block's partial dot product by both decode scales and
 // accumulates in FP32; the global decode scales are applied to the output) and
 // section A3 (hardware support). Both operands are K-major packed E2M1 with
-// UE4M3 scales in the tensor-core scale-factor layout.
+// UE4M3 scales in the tensor-core scale-factor layout. The same kernel runs
+// MXFP4 operands (section A3: UE8M0 power-of-two scales, one per 32 values, no
+// tensor scale) with tcgen05.mma kind::mxf4 and alpha = 1.
 //
 // Design (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      : TMA producer -- A/B code tiles (128-byte swizzled rows of 256
@@ -78,9 +80,11 @@ __device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, ui
 #define FP4_GEMM_CHUNK_K 2048
 #endif
 
-template <int BN_, int STAGES_, int KSTEPS_, int EPI_ROW_BYTES_>
+template <int BN_, int STAGES_, int KSTEPS_, int EPI_ROW_BYTES_, bool MX_ = false>
 struct NvCfg {
     static constexpr int BM = 128, BN = BN_, STAGES = STAGES_;
+    // MX: MXFP4 operands (UE8M0 scales per 32 values, no tensor scale)
+    static constexpr bool MX = MX_;
     static constexpr int KSTEPS = KSTEPS_;         // MMAs (K = 64 each) per stage: 2 or 4
     static constexpr int BK = 64 * KSTEPS;         // FP4 values per stage
     static constexpr int ROW_BYTES = BK / 2;       // 64 or 128 bytes per operand row: the swizzle width
@@ -88,12 +92,17 @@ struct NvCfg {
     static constexpr int CHUNK_STAGES = FP4_GEMM_CHUNK_K / BK;  // stages per accumulator chunk
     static constexpr int A_BYTES = BM * ROW_BYTES;
     static constexpr int B_BYTES = BN * ROW_BYTES;
-    static constexpr int SFA_BYTES = (BM / 128) * 512 * KSTEPS;  // one 512-byte chunk per 128 rows per MMA
-    static constexpr int SFB_BYTES = (BN / 128) * 512 * KSTEPS;
+    // a 512-byte scale chunk holds 128 rows x 4 block scales: K = 64 (NVFP4) or
+    // K = 128 (MXFP4) values, i.e. one or two MMAs
+    static constexpr int SF_CHUNK_K = MX ? 128 : 64;
+    static constexpr int SF_CHUNKS = BK / SF_CHUNK_K;       // chunks per 128 rows per stage
+    static_assert(BK % SF_CHUNK_K == 0, "whole scale chunks per stage");
+    static constexpr int SFA_BYTES = (BM / 128) * 512 * SF_CHUNKS;
+    static constexpr int SFB_BYTES = (BN / 128) * 512 * SF_CHUNKS;
     static constexpr uint32_t TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int NUM_ACC = (BN <= 128) ? 2 : 1;
-    static constexpr int SF_COLS_A = 4 * KSTEPS;           // KSTEPS MMAs x 4 columns
-    static constexpr int SF_COLS_B = KSTEPS * (BN / 32);   // KSTEPS MMAs x (BN / 32) columns
+    static constexpr int SF_COLS_A = 4 * SF_CHUNKS;          // 4 columns per chunk
+    static constexpr int SF_COLS_B = SF_CHUNKS * (BN / 32);  // (BN / 32) columns per chunk
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
     static constexpr int SF_TMEM_BASE = NUM_ACC * BN;
     static constexpr int TMEM_COLS = 512;
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     const int64_t num_m = p.M / Cfg::BM, num_n = p.N / Cfg::BN, tiles = num_m * num_n;
     const int num_k = (int)(p.K / Cfg::BK);
-    const int64_t chunks_k = p.K / 64;  // scale chunks (128 rows x 64 values) along K
+    const int64_t chunks_k = p.K / Cfg::SF_CHUNK_K;  // scale chunks (128 rows x 4 block scales) along K
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -186,12 +195,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc::tma_load_2d(sb + Cfg::OFF_B + s * Cfg::B_BYTES, &tmap_b, kb * Cfg::ROW_BYTES,
                                     (int32_t)(nb * Cfg::BN), full_bar(s));
                     tc::bulk_load(sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
-                                  p.a_scales + 512 * (mb * chunks_k + Cfg::KSTEPS * kb), Cfg::SFA_BYTES, full_bar(s));
+                                  p.a_scales + 512 * (mb * chunks_k + Cfg::SF_CHUNKS * kb), Cfg::SFA_BYTES, full_bar(s));
 #pragma unroll
                     for (int h = 0; h < Cfg::BN / 128; ++h)
-                        tc::bulk_load(sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + 512 * Cfg::KSTEPS * h,
-                                      p.b_scales + 512 * ((nb * (Cfg::BN / 128) + h) * chunks_k + Cfg::KSTEPS * kb),
-                                      512 * Cfg::KSTEPS, full_bar(s));
+                        tc::bulk_load(sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + 512 * Cfg::SF_CHUNKS * h,
+                                      p.b_scales + 512 * ((nb * (Cfg::BN / 128) + h) * chunks_k + Cfg::SF_CHUNKS * kb),
+                                      512 * Cfg::SF_CHUNKS, full_bar(s));
                 }
             }
         }
@@ -232,9 +241,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t b_s = sb + Cfg::OFF_B + s * Cfg::B_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
-                        tc::mma_mxf4nvf4(d_tmem, tc::kmajor_swizzled_desc(a_s + 32 * kk, Cfg::ROW_BYTES, Cfg::SWIZZLE),
-                                         tc::kmajor_swizzled_desc(b_s + 32 * kk, Cfg::ROW_BYTES, Cfg::SWIZZLE), IDESC,
-                                         sfa_t + 4 * kk, sfb_t + (Cfg::BN / 32) * kk, (!first || kk != 0) ? 1u : 0u);
+                        const uint64_t da = tc::kmajor_swizzled_desc(a_s + 32 * kk, Cfg::ROW_BYTES, Cfg::SWIZZLE);
+                        const uint64_t db = tc::kmajor_swizzled_desc(b_s + 32 * kk, Cfg::ROW_BYTES, Cfg::SWIZZLE);
+                        const uint32_t acc_in = (!first || kk != 0) ? 1u : 0u;
+                        if (Cfg::MX) {
+                            // MMA kk reads scale bytes 2 (kk % 2) .. + 1 of chunk kk / 2
+                            const int c = kk >> 1;
+                            tc::mma_mxf4(d_tmem, da, db, tc::idesc_mxf4(Cfg::BM, Cfg::BN, 2u * (kk & 1)), sfa_t + 4 * c,
+                                         sfb_t + (Cfg::BN / 32) * c, acc_in);
+                        } else {
+                            tc::mma_mxf4nvf4(d_tmem, da, db, IDESC, sfa_t + 4 * kk, sfb_t + (Cfg::BN / 32) * kk, acc_in);
+                        }
                     }
                     tc::commit(empty_bar(s));
                     if (last) {
@@ -269,12 +286,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t sfa_s = sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
                     const uint32_t sfb_s = sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
-                        tc::cp_32x128b_warpx4(sfa_t + 4 * kk, tc::scale_chunk_desc(sfa_s + 512 * kk));
+                    for (int c = 0; c < Cfg::SF_CHUNKS; ++c) {
+                        tc::cp_32x128b_warpx4(sfa_t + 4 * c, tc::scale_chunk_desc(sfa_s + 512 * c));
 #pragma unroll
                         for (int h = 0; h < Cfg::BN / 128; ++h)
-                            tc::cp_32x128b_warpx4(sfb_t + (Cfg::BN / 32) * kk + 4 * h,
-                                                  tc::scale_chunk_desc(sfb_s + 512 * Cfg::KSTEPS * h + 512 * kk));
+                            tc::cp_32x128b_warpx4(sfb_t + (Cfg::BN / 32) * c + 4 * h,
+                                                  tc::scale_chunk_desc(sfb_s + 512 * Cfg::SF_CHUNKS * h + 512 * c));
                     }
                     tc::commit(sf_bar(s));
                 }
@@ -289,7 +306,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int half = (warp - Cfg::FIRST_EPI_WARP) >> 2;  // which 128 of the BN columns
         uint8_t* ebox = smem + Cfg::OFF_EPI + (warp - Cfg::FIRST_EPI_WARP) * Cfg::EPI_BOX_BYTES;
         const uint32_t ebox_s = sb + Cfg::OFF_EPI + (uint32_t)((warp - Cfg::FIRST_EPI_WARP) * Cfg::EPI_BOX_BYTES);
-        const float alpha = __fmul_rn(*p.a_sdec, *p.b_sdec);
+        const float alpha = Cfg::MX ? 1.0f : __fmul_rn(*p.a_sdec, *p.b_sdec);
         const int nchunks = (num_k + Cfg::CHUNK_STAGES - 1) / Cfg::CHUNK_STAGES;
         uint32_t chunk = 0;
         bool ok = true;
@@ -512,10 +529,16 @@ cudaError_t run_nvfp4(const GemmJob& j, cudaStream_t st) {
 #endif
 using NvWide = NvCfg<256, FP4_GEMM_WIDE_STAGES, FP4_GEMM_WIDE_KSTEPS, FP4_GEMM_WIDE_EPI>;            // N % 256 == 0
 using NvNarrow = NvCfg<128, FP4_GEMM_NARROW_STAGES, FP4_GEMM_NARROW_KSTEPS, FP4_GEMM_NARROW_EPI>;  // N % 128 == 0
+using MxWide = NvCfg<256, FP4_GEMM_WIDE_STAGES, FP4_GEMM_WIDE_KSTEPS, FP4_GEMM_WIDE_EPI, true>;
+using MxNarrow = NvCfg<128, FP4_GEMM_NARROW_STAGES, FP4_GEMM_NARROW_KSTEPS, FP4_GEMM_NARROW_EPI, true>;
 
 }  // namespace
 
 cudaError_t launch_gemm_nvfp4(const GemmJob& j, cudaStream_t st) {
+    if (j.scale_fmt == FP4_SCALE_UE8M0) {
+        if (j.N % 256 == 0) return j.out_fp32 ? run_nvfp4<MxWide, true>(j, st) : run_nvfp4<MxWide, false>(j, st);
+        return j.out_fp32 ? run_nvfp4<MxNarrow, true>(j, st) : run_nvfp4<MxNarrow, false>(j, st);
+    }
     if (j.N % 256 == 0) {
         if (j.out_fp32) return run_nvfp4<NvWide, true>(j, st);
         return run_nvfp4<NvWide, false>(j, st);

@@ -44,6 +44,7 @@ struct QParams {
     const float* partials;
     int npartials;
     int held, refresh;
+    int count_t;  // 16x16 with two outputs: the counters follow the transposed output
     float target_T;
     uint32_t tensor_id, step_lo, key0, key1;
     uint32_t round_key[20];  // Philox key of round r: (key0 + r W0, key1 + r W1), W the Weyl constants
@@ -544,7 +545,7 @@ __device__ __forceinline__ uint32_t tile2d_offset(int r, int c) {
     return (uint32_t)((c >> 6) * 8192 + r * 128 + (((((c & 63) >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1));
 }
 
-template <int FMT, bool TCL_W, bool TCL_WT>
+template <int FMT, bool SR, bool TCL_W, bool TCL_WT>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_2d_tile_kernel(const __grid_constant__ CUtensorMap tmap_w, QParams q) {
     extern __shared__ uint8_t tile2d_smem_raw[];
@@ -629,14 +630,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 cw[h][0] = sign_nibbles8(v[h]);
                 cw[h][1] = sign_nibbles8(v[h] + 8);
             }
-            cnt.eunder += 32u - nzero;
+            if (!q.count_t) cnt.eunder += 32u - nzero;
         } else {
             float x[2][16];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 scale16(v[h], enc_l, x[h]);
-                cw[h][0] = e2m1_rne_x8(x[h]);
-                cw[h][1] = e2m1_rne_x8(x[h] + 8);
+                if (SR) {
+                    // W element (n, k) has index n K + k
+                    const int64_t e0 = (n0 + 16 * bn + l + 8 * h) * K + k0 + 16 * bk;
+                    uint4 r[4];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        r[g] = sr_group_bits_rk((uint64_t)(e0 >> 2) + g, q.tensor_id, q.step_lo, q.round_key);
+                    e2m1_sr_x16(x[h], r, cw[h][0], cw[h][1]);
+                } else {
+                    cw[h][0] = e2m1_rne_x8(x[h]);
+                    cw[h][1] = e2m1_rne_x8(x[h] + 8);
+                }
             }
             if (__fmul_rn(amax, enc_l) > 6.0f) {
 #pragma unroll
@@ -644,7 +655,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[h][i]);
             }
-            cnt.eunder += zero_mag_count16(cw[0][0], cw[0][1]) + zero_mag_count16(cw[1][0], cw[1][1]) - nzero;
+            if (!q.count_t)
+                cnt.eunder += zero_mag_count16(cw[0][0], cw[0][1]) + zero_mag_count16(cw[1][0], cw[1][1]) - nzero;
         }
         if (q.codes != nullptr) {
             const int64_t jb = (k0 >> 4) + bk;
@@ -670,14 +682,27 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tw[0][1] = sign_nibbles8(c0 + 8);
                 tw[1][0] = sign_nibbles8(c1);
                 tw[1][1] = sign_nibbles8(c1 + 8);
+                if (q.count_t) cnt.eunder += 32u - nzero;  // the same values, transposed
             } else {
-                float x[16];
-                scale16(c0, enc_l, x);
-                tw[0][0] = e2m1_rne_x8(x);
-                tw[0][1] = e2m1_rne_x8(x + 8);
-                scale16(c1, enc_l, x);
-                tw[1][0] = e2m1_rne_x8(x);
-                tw[1][1] = e2m1_rne_x8(x + 8);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float x[16];
+                    scale16(hh ? c1 : c0, enc_l, x);
+                    if (SR) {
+                        // W^T element (k, n) has index k N + n
+                        const int64_t e0 = (k0 + 16 * bk + 2 * l + hh) * N + n0 + 16 * bn;
+                        uint4 r[4];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            r[g] = sr_group_bits_rk((uint64_t)(e0 >> 2) + g, q.tensor_id, q.step_lo, q.round_key);
+                        e2m1_sr_x16(x, r, tw[hh][0], tw[hh][1]);
+                    } else {
+                        tw[hh][0] = e2m1_rne_x8(x);
+                        tw[hh][1] = e2m1_rne_x8(x + 8);
+                    }
+                }
+                if (q.count_t)
+                    cnt.eunder += zero_mag_count16(tw[0][0], tw[0][1]) + zero_mag_count16(tw[1][0], tw[1][1]) - nzero;
             }
             const int64_t jb = (n0 >> 4) + bn;
 #pragma unroll
@@ -1018,6 +1043,7 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
         // the kernel's primary output is W (rowwise); for COLWISE the operand is
         // W^T, which the kernel writes through its transposed output
         QParams p = q;
+        p.count_t = j.colwise;  // the counters follow the requested operand
         int lw, lwt;
         if (j.colwise) {
             p.codes = j.codes_t;
@@ -1040,7 +1066,7 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
             const int g2 = (int)(ntiles < cap ? ntiles : cap);
 #define FP4_2D_TILE(TA, TB)                                                                                          \
     do {                                                                                                            \
-        auto kern = quantize_2d_tile_kernel<FMT, TA, TB>;                                                           \
+        auto kern = j.sr ? quantize_2d_tile_kernel<FMT, true, TA, TB> : quantize_2d_tile_kernel<FMT, false, TA, TB>;  \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, k2dSmemBytes);      \
         if (e != cudaSuccess) return e;                                                                             \
         kern<<<g2, kThreads, k2dSmemBytes, st>>>(tmap_w, p);                                                        \
@@ -1052,6 +1078,7 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
 #undef FP4_2D_TILE
             return cudaGetLastError();
         }
+        if (j.sr) return cudaErrorNotSupported;  // the half-warp kernel rounds to nearest only
         if (a && b) quantize_2d_kernel<FMT, true, true><<<grid, kThreads, 0, st>>>(p);
         else if (a) quantize_2d_kernel<FMT, true, false><<<grid, kThreads, 0, st>>>(p);
         else if (b) quantize_2d_kernel<FMT, false, true><<<grid, kThreads, 0, st>>>(p);

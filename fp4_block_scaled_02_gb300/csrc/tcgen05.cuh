@@ -146,6 +146,20 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d, uint64_t a, uint64_t b,
         : "memory");
 }
 
+// The same with UE8M0 scales, one per 32 values (kind::mxf4, MXFP4): each
+// 32-bit scale column holds four consecutive block scales of a row, of which
+// one MMA (K = 64) reads two, at the byte offset the instruction descriptor's
+// scale-factor ids select (0 or 2).
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
 // D (TMEM, FP32) (+)= A x B^T with BF16 operands from shared memory, K = 16.
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -214,6 +228,15 @@ __device__ __forceinline__ uint64_t scale_chunk_desc(uint32_t addr) { return sme
 // scales (bit 23 = 0), both K-major, dense, scale-factor ids 0.
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4: E2M1 A and B (type code 1), UE8M0
+// scales (bit 23 = 1), both K-major, dense; sf_id (0 or 2) is the byte offset of
+// the MMA's two scales in each 32-bit scale column, for A (bits 29-30) and B
+// (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sf_id) {
+    return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
 }
 
 // Instruction descriptor, kind::f16: FP32 accumulator (bits 4-5 = 1), BF16 A

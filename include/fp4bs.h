@@ -189,9 +189,12 @@ fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void
 /* Block-scaled GEMM D[M x N] = s_dec,G,A * s_dec,G,B * sum_k (a_mk s_A)(b_nk s_B)
  * with FP32 accumulation ("Pretraining LLMs with NVFP4", App. B.3; A3 hardware
  * support). A is M x K, B is N x K, both quantized, K-major, TCGEN05 scale
- * layout, same scale format and block 16. E4M3 runs natively (tcgen05
- * kind::mxf4nvf4); UE5M3 runs the software-emulated path (operands decoded to
- * BF16 in shared memory, tcgen05 kind::f16). M and N must be multiples of 128
+ * layout, same scale format. E4M3 (block 16) runs natively (tcgen05
+ * kind::mxf4nvf4); UE8M0 (MXFP4, block 32, section A3) runs natively too
+ * (tcgen05 kind::mxf4) with alpha = 1: MXFP4 has no tensor scale, so its
+ * s_dec_global is not read; UE5M3 (block 16) runs the software-emulated path
+ * (operands decoded to BF16 in shared memory, tcgen05 kind::f16). Mixed scale
+ * formats are FP4_ERR_UNSUPPORTED. M and N must be multiples of 128
  * and K of 256. Output row-major M x N: BF16 (out_fp32 == 0) or FP32; with
  * accumulate != 0 (FP32 only) D is added to the existing output. */
 fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32,

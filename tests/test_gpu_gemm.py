@@ -76,6 +76,50 @@ def test_gemm_nvfp4_persistent_wrap_sampled(M, N, K):
     _check(d.cpu().numpy()[ms, ns], c_ref, s, bf16=False)
 
 
+MX = fb.FP4_SCALE_UE8M0
+
+
+# MXFP4 ("Pretraining Large Language Models with NVFP4", A3): UE8M0 scales per
+# 32 values, tcgen05 kind::mxf4; N % 256 selects the tile width as for NVFP4 and
+# K = 2304 ends in a partial accumulator chunk
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (640, 1024, 2304)])
+@pytest.mark.parametrize("out32", [False, True])
+def test_gemm_mxfp4_full_output(M, N, K, out32):
+    ra, a = _operand(41, M, K, "student_t4", fmt=MX, block=fb.FP4_BLOCK_1x32)
+    rb, b = _operand(42, N, K, "log_normal_1e-4_2", fmt=MX, block=fb.FP4_BLOCK_1x32)
+    # MXFP4 has no tensor scale: whatever the s_dec words hold is not read
+    a.s_dec.fill_(7.0)
+    b.s_dec.fill_(-3.0)
+    d = torch.empty((M, N), dtype=torch.float32 if out32 else torch.bfloat16, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert fb.fp4_device_status() == 0
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], 1.0, rb["codes"], rb["scales"], 1.0,
+                           scale_fmt=oracle.FMT_UE8M0, bs=32)
+    _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
+
+
+def test_gemm_mxfp4_persistent_wrap_sampled():
+    M, N, K = 4096, 2048, 768
+    ra, a = _operand(43, M, K, "normal", fmt=MX, block=fb.FP4_BLOCK_1x32)
+    rb, b = _operand(44, N, K, "weight", fmt=MX, block=fb.FP4_BLOCK_1x32)
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert fb.fp4_device_status() == 0
+    rng = np.random.default_rng(1)
+    ms, ns = rng.integers(0, M, 4000), rng.integers(0, N, 4000)
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], 1.0, rb["codes"], rb["scales"], 1.0,
+                           scale_fmt=oracle.FMT_UE8M0, bs=32, pairs=(ms, ns))
+    _check(d.cpu().numpy()[ms, ns], c_ref, s, bf16=False)
+
+
+def test_gemm_mixed_scale_formats_are_rejected():
+    _, a = _operand(45, 128, 256, "normal")
+    _, b = _operand(46, 128, 256, "normal", fmt=MX, block=fb.FP4_BLOCK_1x32)
+    with pytest.raises(fb.Fp4Error) as e:
+        fb.fp4_gemm(a, b, torch.empty((128, 128), dtype=torch.float32, device="cuda"))
+    assert e.value.status == fb._lib.FP4_ERR_UNSUPPORTED
+
+
 def test_gemm_accumulate_fp32():
     M, N, K = 256, 256, 512
     ra, a = _operand(35, M, K, "normal")
@@ -324,3 +368,31 @@ def test_8b_mxfp4_side_by_side_counters():
             ref = oracle_quantize(cfg, bits)
             assert cnt.cpu().numpy().tolist() == ref["counters"].tolist(), (key, cfg.scale_fmt)
             assert np.array_equal(out.codes.cpu().numpy(), ref["codes"])
+
+
+def test_8b_mxfp4_fprop_full_size_sampled():
+    """The 8B up-projection (T = 8192, 4096 -> 21504) with X and W through the
+    MXFP4 1x32 quantizer on the GPU (bytes equal to the oracle's) and the
+    kind::mxf4 GEMM: sampled outputs of Y = X W^T within the bound."""
+    w = WORKLOADS["8b"]
+    inp = linear_inputs(w, 0)
+    cfg = fb.QuantConfig(scale_fmt=MX, block=fb.FP4_BLOCK_1x32)
+    ops, refs = [], []
+    for key in ("x", "w"):
+        bits = inp[key]
+        out = fb.QTensor.empty(bits.shape[0], bits.shape[1], MX)
+        fb.fp4_quantize(cfg, to_gpu_bf16(bits), out, ws=torch.empty(4096, dtype=torch.float32, device="cuda"))
+        ref = oracle_quantize(cfg, bits)
+        assert np.array_equal(out.codes.cpu().numpy(), ref["codes"]), key
+        assert np.array_equal(out.scales.cpu().numpy(), oracle.swizzle_scales(ref["scales"])), key
+        ops.append(out)
+        refs.append(ref)
+    T, N = inp["x"].shape[0], inp["w"].shape[0]
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    fb.fp4_linear_fprop(ops[0], ops[1], y)
+    assert fb.fp4_device_status() == 0
+    rng = np.random.default_rng(2)
+    ms, ns = rng.integers(0, T, 3000), rng.integers(0, N, 3000)
+    c_ref, s = oracle.gemm(refs[0]["codes"], refs[0]["scales"], 1.0, refs[1]["codes"], refs[1]["scales"], 1.0,
+                           scale_fmt=oracle.FMT_UE8M0, bs=32, pairs=(ms, ns))
+    _check(y.float().cpu().numpy()[ms, ns], c_ref, s, bf16=True)

@@ -105,6 +105,38 @@ def test_weights_2d_zero_tiny_and_huge_blocks():
         assert_quant_equal(out_t, oracle_quantize(cfg, bits, colwise=True), layout)
 
 
+# 2D scaling of gradients with SR (16x16 blocks on a gradient operand, in both
+# orientations): runs on the tile kernel's shapes; every element draws the word
+# of its own index in the operand it lands in, so the two outputs round apart
+@pytest.mark.parametrize("shape,layout,fmt", [((256, 512), TC, fb.FP4_SCALE_E4M3), ((192, 384), PLAIN, fb.FP4_SCALE_E4M3),
+                                              ((128, 256), TC, fb.FP4_SCALE_UE5M3)])
+@pytest.mark.parametrize("orient", [fb.FP4_ORIENT_ROWWISE, fb.FP4_ORIENT_COLWISE])
+def test_2d_blocks_with_stochastic_rounding(shape, layout, fmt, orient):
+    bits = random_bf16(24, shape, "log_normal_1e-4_2")
+    cfg = fb.QuantConfig(block=fb.FP4_BLOCK_16x16, scale_fmt=fmt, round=fb.FP4_ROUND_SR, layout=layout,
+                         emit_transpose=True, orient=orient, seed=6, tensor_id=9, step=41)
+    out, out_t, cnt = gpu_quantize(cfg, bits, with_transpose=True)
+    assert_quant_equal(out, oracle_quantize(cfg, bits), layout, cnt)
+    assert_quant_equal(out_t, oracle_quantize(cfg, bits, colwise=orient == fb.FP4_ORIENT_ROWWISE), layout)
+    # the scales are shared; the codes of the two outputs are independent draws
+    a = out.codes.cpu().numpy()
+    b = out_t.codes.cpu().numpy()
+    ua = np.stack([a & 0xF, a >> 4], axis=-1).reshape(a.shape[0], -1)
+    ub = np.stack([b & 0xF, b >> 4], axis=-1).reshape(b.shape[0], -1)
+    assert not np.array_equal(ua.T, ub)
+
+
+def test_2d_stochastic_rounding_needs_whole_tiles():
+    """16x16 with SR runs only where the input is whole 64 x 128 tiles."""
+    for shape in ((48, 256), (128, 80)):
+        x = to_gpu_bf16(random_bf16(25, shape, "normal"))
+        out = fb.QTensor.empty(*shape, layout=PLAIN)
+        cfg = fb.QuantConfig(block=fb.FP4_BLOCK_16x16, round=fb.FP4_ROUND_SR, layout=PLAIN)
+        with pytest.raises(fb.Fp4Error) as e:
+            fb.fp4_quantize(cfg, x, out, ws=new_ws())
+        assert e.value.status == fb._lib.FP4_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("shape,layout", [((256, 512), TC), ((384, 128), TC), ((10, 64), PLAIN), ((3, 96), PLAIN)])
 def test_mxfp4_1x32(shape, layout):
     bits = random_bf16(14, shape, "student_t4")

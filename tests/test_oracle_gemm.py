@@ -84,6 +84,30 @@ def test_gemm_exhaustive_code_pairs(orc):
             assert s[i, j] == abs(c[i, j])
 
 
+def test_gemm_mxfp4_block32_exact_rational(orc):
+    # MXFP4 ("Pretraining Large Language Models with NVFP4", A3): UE8M0 block
+    # scales are powers of two 2^(code - 127), one per 32 values; no tensor scale
+    rng = np.random.default_rng(23)
+    M, N, K = 6, 5, 96
+    ac = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    bc = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    asc = rng.integers(100, 150, size=(M, K // 32), dtype=np.uint8)
+    bsc = rng.integers(110, 140, size=(N, K // 32), dtype=np.uint8)
+    c, s = orc.gemm(ac, asc, 1.0, bc, bsc, 1.0, scale_fmt=orc.FMT_UE8M0, bs=32)
+
+    def val(codes, scales, r, k):
+        byte = int(codes[r, k // 2])
+        code = byte & 0xF if k % 2 == 0 else byte >> 4
+        return Fraction(_val(code)) * Fraction(2) ** (int(scales[r, k // 32]) - 127)
+
+    for m in range(M):
+        for n in range(N):
+            terms = [val(ac, asc, m, k) * val(bc, bsc, n, k) for k in range(K)]
+            exact, sabs = sum(terms), sum(abs(t) for t in terms)
+            assert abs(Fraction(c[m, n]) - exact) <= Fraction(2) ** -45 * sabs
+            assert Fraction(s[m, n]) == sabs or abs(Fraction(s[m, n]) - sabs) <= Fraction(2) ** -45 * sabs
+
+
 def test_gemm_zero_bound_means_zero(orc):
     ac = np.zeros((4, 16), dtype=np.uint8)
     c, s = orc.gemm(ac, np.zeros((4, 2), np.uint8), 1.0, ac, np.zeros((4, 2), np.uint8), 1.0)
