@@ -79,46 +79,42 @@ __device__ __forceinline__ uint32_t e2m1_sr_sw(float v, uint32_t r) {
 // when rh > fh; only rh == fh needs the low 8 bits. R = 0xFFFF - rh rounds up
 // iff rh < fh, R = 0x10000 - rh iff rh <= fh (rh >= 1), so two conversions
 // classify every element, and blocks holding a tie (or a draw with rh == 0,
-// where 0x10000 does not fit) take the software decision. Returns x0's code in
-// bits 0-3 and x1's in bits 4-7 (bits 8-15: don't care); rb holds R(x0) in its
-// low half and R(x1) in its high half.
-__device__ __forceinline__ uint32_t e2m1_sr_pair_hw(float x0, float x1, uint32_t rb) {
+// where 0x10000 does not fit) take the software decision. Returns x_lo's code
+// in nibble 0 and x_hi's in nibble 2 (nibbles 1 and 3 zero); rb holds R(x_lo)
+// in its low half and R(x_hi) in its high half.
+__device__ __forceinline__ uint32_t e2m1_sr_pair_hw(float x_lo, float x_hi, uint32_t rb) {
     const uint32_t rbits = __byte_perm(rb, 0u, 0x3120);
     uint16_t d;
     asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
         : "=h"(d)
-        : "f"(0.0f), "f"(x1), "f"(0.0f), "f"(x0), "r"(rbits));
-    const uint32_t t = d;
-    return t | (t >> 4);
-}
-
-// Four pair bytes (low byte of t0..t3) -> one code word.
-__device__ __forceinline__ uint32_t pack_pair_bytes(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3) {
-    return __byte_perm(__byte_perm(t0, t1, 0x0040u), __byte_perm(t2, t3, 0x0040u), 0x5410u);
+        : "f"(0.0f), "f"(x_hi), "f"(0.0f), "f"(x_lo), "r"(rbits));
+    return d;
 }
 
 // Sixteen SR codes (element i in nibble i of lo / hi); element i draws word
-// i & 3 of r[i >> 2].
+// i & 3 of r[i >> 2]. Each quad 4q .. 4q + 3 takes two conversions: (4q, 4q + 2)
+// into nibbles 0 and 2 and (4q + 1, 4q + 3) into nibbles 0 and 2 shifted up by
+// one nibble, so one add interleaves them into the quad's 16 bits.
 __device__ __forceinline__ void e2m1_sr_x16(const float x[16], const uint4 r[4], uint32_t& lo, uint32_t& hi) {
-    uint32_t ta[8], tb[8];
+    uint32_t qa[4], qb[4];
     uint32_t mn = __vimin3_u32(__vimin3_u32(r[0].x, r[0].y, r[0].z), __vimin3_u32(r[0].w, r[1].x, r[1].y),
                                __vimin3_u32(r[1].z, r[1].w, r[2].x));
     mn = __vimin3_u32(mn, __vimin3_u32(r[2].y, r[2].z, r[2].w), __vimin3_u32(r[3].x, r[3].y, min(r[3].z, r[3].w)));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4& q = r[j >> 1];
-        const uint32_t r0 = (j & 1) ? q.z : q.x, r1 = (j & 1) ? q.w : q.y;
-        const uint32_t wa = ~__byte_perm(r0, r1, 0x7632u);  // 0xFFFF - rh, per element half
+    for (int q = 0; q < 4; ++q) {
+        // 0xFFFF - rh per element half: (4q, 4q + 2) and (4q + 1, 4q + 3)
+        const uint32_t we = ~__byte_perm(r[q].x, r[q].z, 0x7632u);
+        const uint32_t wo = ~__byte_perm(r[q].y, r[q].w, 0x7632u);
         // 0x10000 - rh; a half with rh == 0 overflows into its neighbour, but any
         // such draw sends the block to the software decision below
-        const uint32_t wb = wa + 0x00010001u;
-        ta[j] = e2m1_sr_pair_hw(x[2 * j], x[2 * j + 1], wa);
-        tb[j] = e2m1_sr_pair_hw(x[2 * j], x[2 * j + 1], wb);
+        const uint32_t we1 = we + 0x00010001u, wo1 = wo + 0x00010001u;
+        qa[q] = e2m1_sr_pair_hw(x[4 * q], x[4 * q + 2], we) + 16u * e2m1_sr_pair_hw(x[4 * q + 1], x[4 * q + 3], wo);
+        qb[q] = e2m1_sr_pair_hw(x[4 * q], x[4 * q + 2], we1) + 16u * e2m1_sr_pair_hw(x[4 * q + 1], x[4 * q + 3], wo1);
     }
-    lo = pack_pair_bytes(ta[0], ta[1], ta[2], ta[3]);
-    hi = pack_pair_bytes(ta[4], ta[5], ta[6], ta[7]);
-    const uint32_t lob = pack_pair_bytes(tb[0], tb[1], tb[2], tb[3]);
-    const uint32_t hib = pack_pair_bytes(tb[4], tb[5], tb[6], tb[7]);
+    lo = __byte_perm(qa[0], qa[1], 0x5410u);
+    hi = __byte_perm(qa[2], qa[3], 0x5410u);
+    const uint32_t lob = __byte_perm(qb[0], qb[1], 0x5410u);
+    const uint32_t hib = __byte_perm(qb[2], qb[3], 0x5410u);
     if (((lo ^ lob) | (hi ^ hib)) != 0u || mn < 0x10000u) {
         lo = hi = 0u;
 #pragma unroll
@@ -317,29 +313,39 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
-// Philox4x32-10 with the ten round keys precomputed (rk[2r], rk[2r + 1] = the
-// key after r Weyl increments); passing them as kernel parameters lets every
-// round read its key straight from the parameter bank.
-__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk)[20]) {
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        unsigned long long p0, p1;
-        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
-        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
-        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
-        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
-        c = make_uint4(hi1 ^ c.y ^ rk[2 * round], lo1, hi0 ^ c.w ^ rk[2 * round + 1], lo0);
-    }
-    return c;
-}
-
 // Random bits for stochastic rounding: operand element e (row-major linear
 // index of the quantized operand) uses word (e & 3) of Philox(counter =
 // (lo32(e >> 2), hi32(e >> 2), tensor_id, lo32(step)), key = seed). One call
-// covers 4 consecutive elements; this returns the words for the group g = e >> 2.
-__device__ __forceinline__ uint4 sr_group_bits_rk(uint64_t g, uint32_t tensor_id, uint32_t step_lo,
-                                                  const uint32_t (&rk)[20]) {
-    return philox4x32_10_rk(make_uint4((uint32_t)g, (uint32_t)(g >> 32), tensor_id, step_lo), rk);
+// covers 4 consecutive elements. sr_block_bits returns the words of the four
+// groups g0 .. g0 + 3 of one 16-element block (g0 % 4 == 0, so the four
+// counters share hi32(g0)). Their first round multiplies the same third counter
+// word (tensor_id) and their second round the same first word, so those two
+// products are formed once per block; every other step is the plain round.
+__device__ __forceinline__ void sr_block_bits(uint64_t g0, uint32_t tensor_id, uint32_t step_lo,
+                                              const uint32_t (&rk)[20], uint4 r[4]) {
+    unsigned long long p;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(tensor_id), "r"(0xCD9E8D57u));
+    const uint32_t x1 = (uint32_t)(p >> 32) ^ (uint32_t)(g0 >> 32) ^ rk[0];  // round 1 output, word 0
+    const uint32_t y1k = (uint32_t)p ^ rk[2];                                // round 1 word 1, round 2 key folded
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(x1), "r"(0xD2511F53u));
+    const uint32_t z2k = (uint32_t)(p >> 32) ^ rk[3], w2 = (uint32_t)p;    // round 2 parts from word 0
+    const uint32_t sk = step_lo ^ rk[1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        unsigned long long p0, p1;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"((uint32_t)g0 + (uint32_t)i), "r"(0xD2511F53u));
+        const uint32_t z1 = (uint32_t)(p0 >> 32) ^ sk, w1 = (uint32_t)p0;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(z1), "r"(0xCD9E8D57u));
+        uint4 c = make_uint4((uint32_t)(p1 >> 32) ^ y1k, (uint32_t)p1, z2k ^ w1, w2);
+#pragma unroll
+        for (int round = 2; round < 10; ++round) {
+            asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
+            asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
+            c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk[2 * round], (uint32_t)p1,
+                           (uint32_t)(p0 >> 32) ^ c.w ^ rk[2 * round + 1], (uint32_t)p0);
+        }
+        r[i] = c;
+    }
 }
 
 // ---------------------------------------------------------------------------

@@ -202,8 +202,7 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vm
     }
     if (SR) {
         uint4 r[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) r[k] = sr_group_bits_rk(g0 + k, q.tensor_id, q.step_lo, q.round_key);
+        sr_block_bits(g0, q.tensor_id, q.step_lo, q.round_key, r);
         e2m1_sr_x16(x, r, lo, hi);
     } else {
         lo = e2m1_rne_x8(x);
@@ -640,9 +639,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     // W element (n, k) has index n K + k
                     const int64_t e0 = (n0 + 16 * bn + l + 8 * h) * K + k0 + 16 * bk;
                     uint4 r[4];
-#pragma unroll
-                    for (int g = 0; g < 4; ++g)
-                        r[g] = sr_group_bits_rk((uint64_t)(e0 >> 2) + g, q.tensor_id, q.step_lo, q.round_key);
+                    sr_block_bits((uint64_t)(e0 >> 2), q.tensor_id, q.step_lo, q.round_key, r);
                     e2m1_sr_x16(x[h], r, cw[h][0], cw[h][1]);
                 } else {
                     cw[h][0] = e2m1_rne_x8(x[h]);
@@ -692,9 +689,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         // W^T element (k, n) has index k N + n
                         const int64_t e0 = (k0 + 16 * bk + 2 * l + hh) * N + n0 + 16 * bn;
                         uint4 r[4];
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            r[g] = sr_group_bits_rk((uint64_t)(e0 >> 2) + g, q.tensor_id, q.step_lo, q.round_key);
+                        sr_block_bits((uint64_t)(e0 >> 2), q.tensor_id, q.step_lo, q.round_key, r);
                         e2m1_sr_x16(x, r, tw[hh][0], tw[hh][1]);
                     } else {
                         tw[hh][0] = e2m1_rne_x8(x);
