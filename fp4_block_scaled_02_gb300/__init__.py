@@ -23,7 +23,7 @@ from ._lib import (FP4_BLOCK_1x16, FP4_BLOCK_1x32, FP4_BLOCK_16x16, FP4_LAYOUT_P
                    FP4_SCALE_UE5M3, FP4_SCALE_UE8M0, FP4_TSCALE_CURRENT, FP4_TSCALE_HELD, Fp4Error)
 
 __all__ = ["QTensor", "QuantConfig", "AmaxState", "fp4_quantize", "fp4_quantize_dual", "fp4_dequantize", "fp4_gemm",
-           "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
+           "fp4_gemm_workspace_bytes", "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
            "fp4_workspace_bytes", "fp4_quantized_sizes", "Fp4Error", "Fp4Linear"]
 
 
@@ -159,11 +159,25 @@ def fp4_dequantize(t: QTensor, out: torch.Tensor, stream=None) -> None:
                                           _stream(stream)), "fp4_dequantize")
 
 
-def fp4_gemm(a: QTensor, b: QTensor, d: torch.Tensor, accumulate: bool = False, stream=None) -> None:
+def fp4_gemm_workspace_bytes(a: QTensor, b: QTensor) -> int:
+    da, db = a.desc(), b.desc()
+    return _lib.load().fp4_gemm_workspace_bytes(ctypes.byref(da), ctypes.byref(db))
+
+
+def fp4_gemm(a: QTensor, b: QTensor, d: torch.Tensor, accumulate: bool = False, stream=None,
+             ws: torch.Tensor | None = None) -> None:
+    """D = A B^T (fp4_gemm); with ``ws`` (fp4_gemm_workspace_bytes(a, b) bytes of
+    device memory) UE5M3 operands take the rebiased native path (fp4_gemm_ws)."""
     assert d.is_contiguous() and d.dtype in (torch.float32, torch.bfloat16)
     da, db = a.desc(), b.desc()
-    _lib.check(_lib.load().fp4_gemm(ctypes.byref(da), ctypes.byref(db), _ptr(d), int(d.dtype == torch.float32),
-                                    int(accumulate), _stream(stream)), "fp4_gemm")
+    L = _lib.load()
+    if ws is None:
+        _lib.check(L.fp4_gemm(ctypes.byref(da), ctypes.byref(db), _ptr(d), int(d.dtype == torch.float32),
+                              int(accumulate), _stream(stream)), "fp4_gemm")
+    else:
+        _lib.check(L.fp4_gemm_ws(ctypes.byref(da), ctypes.byref(db), _ptr(d), int(d.dtype == torch.float32),
+                                 int(accumulate), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+                   "fp4_gemm_ws")
 
 
 def fp4_linear_fprop(x: QTensor, w: QTensor, y: torch.Tensor, stream=None) -> None:
@@ -200,7 +214,8 @@ class Fp4Linear:
 
     scale_fmt E4M3 gives NVFP4 with current tensor scaling; UE5M3 gives the
     UE5M3 recipe (held amax refreshed every `refresh_every` steps with target T,
-    no RHT) on the emulated GEMM path."""
+    no RHT), whose GEMMs take the rebiased native path (fp4_gemm_ws) when
+    `ue5m3_native` is set, else the emulated one."""
     tokens: int
     k_in: int
     n_out: int
@@ -211,6 +226,7 @@ class Fp4Linear:
     target_T: float = 448.0
     held: bool = False
     refresh_every: int = 50
+    ue5m3_native: bool = True
     device: str = "cuda"
     bufs: dict = field(default_factory=dict)
 
@@ -228,6 +244,12 @@ class Fp4Linear:
                               device=dev)
         self.counters = torch.zeros((5, 4), dtype=torch.int64, device=dev)
         self.states = [AmaxState(dev) for _ in range(5)] if self.held else [None] * 5
+        self.gemm_ws = None
+        if f == FP4_SCALE_UE5M3 and self.ue5m3_native:
+            b = self.bufs
+            need = max(fp4_gemm_workspace_bytes(b["x"], b["w"]), fp4_gemm_workspace_bytes(b["dy"], b["wt"]),
+                       fp4_gemm_workspace_bytes(b["dyt"], b["xt"]))
+            self.gemm_ws = torch.empty(need, dtype=torch.uint8, device=dev)
 
     def _cfg(self, idx: int, step: int, **kw) -> QuantConfig:
         base = dict(scale_fmt=self.scale_fmt, target_T=self.target_T, seed=self.seed,
@@ -267,6 +289,11 @@ class Fp4Linear:
 
     def gemms(self, y: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor, stream=None):
         b = self.bufs
+        if self.gemm_ws is not None:
+            fp4_gemm(b["x"], b["w"], y, stream=stream, ws=self.gemm_ws)
+            fp4_gemm(b["dy"], b["wt"], dx, stream=stream, ws=self.gemm_ws)
+            fp4_gemm(b["dyt"], b["xt"], dw, stream=stream, ws=self.gemm_ws)
+            return
         fp4_linear_fprop(b["x"], b["w"], y, stream=stream)
         fp4_linear_dgrad(b["dy"], b["wt"], dx, stream=stream)
         fp4_linear_wgrad(b["dyt"], b["xt"], dw, stream=stream)

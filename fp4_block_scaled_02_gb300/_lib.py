@@ -34,7 +34,8 @@ FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05 = 0, 1
 
 EXPORTED = ["fp4_quantized_sizes", "fp4_workspace_bytes", "fp4_quantize", "fp4_dequantize", "fp4_gemm",
             "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
-            "fp4_status_string", "fp4_abi_version", "fp4_quantize_noalloc", "fp4_quantize_dual"]
+            "fp4_status_string", "fp4_abi_version", "fp4_quantize_noalloc", "fp4_quantize_dual",
+            "fp4_gemm_workspace_bytes", "fp4_gemm_ws"]
 
 
 class fp4_quant_params_t(ctypes.Structure):
@@ -89,6 +90,10 @@ def load() -> ctypes.CDLL:
             L.fp4_dequantize.restype = i32
             L.fp4_gemm.argtypes = [TP, TP, P, i32, i32, P]
             L.fp4_gemm.restype = i32
+            L.fp4_gemm_workspace_bytes.argtypes = [TP, TP]
+            L.fp4_gemm_workspace_bytes.restype = sz
+            L.fp4_gemm_ws.argtypes = [TP, TP, P, i32, i32, P, sz, P]
+            L.fp4_gemm_ws.restype = i32
             L.fp4_linear_fprop.argtypes = [TP, TP, P, P]
             L.fp4_linear_fprop.restype = i32
             L.fp4_linear_dgrad.argtypes = [TP, TP, P, P]

@@ -203,6 +203,61 @@ float* noalloc_scratch_ptr() {
 
 }  // namespace
 
+namespace {
+
+fp4_status_t prepare_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
+                          GemmJob& j) {
+    fp4_status_t s = check_operand(a);
+    if (s != FP4_OK) return s;
+    s = check_operand(b);
+    if (s != FP4_OK) return s;
+    if (d == nullptr) return FP4_ERR_INVALID_ARG;
+    if (!aligned16(d)) return FP4_ERR_ALIGNMENT;
+    if (accumulate && !out_fp32) return FP4_ERR_INVALID_ARG;
+    const int bs = a->scale_fmt == FP4_SCALE_UE8M0 ? 32 : 16;
+    if (a->scale_fmt != b->scale_fmt || a->block_k != bs || b->block_k != bs) return FP4_ERR_UNSUPPORTED;
+    if (a->scale_layout != FP4_LAYOUT_TCGEN05 || b->scale_layout != FP4_LAYOUT_TCGEN05) return FP4_ERR_UNSUPPORTED;
+    if (a->cols != b->cols) return FP4_ERR_SHAPE;
+    if (a->rows % 128 != 0 || b->rows % 128 != 0 || a->cols % 256 != 0 || a->cols <= 0 || a->rows <= 0 ||
+        b->rows <= 0)
+        return FP4_ERR_SHAPE;
+    j = GemmJob{};
+    j.a_codes = a->codes;
+    j.a_scales = a->scales;
+    j.a_sdec = a->s_dec_global;
+    j.b_codes = b->codes;
+    j.b_scales = b->scales;
+    j.b_sdec = b->s_dec_global;
+    j.M = a->rows;
+    j.N = b->rows;
+    j.K = a->cols;
+    j.scale_fmt = a->scale_fmt;
+    j.d = d;
+    j.out_fp32 = out_fp32 != 0;
+    j.accumulate = accumulate != 0;
+    j.status = device_status_ptr();
+    if (j.status == nullptr) return FP4_ERR_CUDA;
+    return FP4_OK;
+}
+
+// UE5M3 rebias workspace: per-tile "does not fit" bytes, per-row offsets of A
+// and B, rebiased scales of A and B (each part 16-byte aligned).
+struct RebiasLayout {
+    size_t off_a, off_b, sc_a, sc_b, total;
+};
+RebiasLayout rebias_layout(int64_t M, int64_t N, int64_t K) {
+    auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
+    RebiasLayout l{};
+    l.off_a = up16((size_t)(M / 128 + N / 128));
+    l.off_b = l.off_a + up16((size_t)M);
+    l.sc_a = l.off_b + up16((size_t)N);
+    l.sc_b = l.sc_a + up16((size_t)(M * (K / 16)));
+    l.total = l.sc_b + up16((size_t)(N * (K / 16)));
+    return l;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp4_abi_version(void) { return 1; }
@@ -316,41 +371,58 @@ fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void
     return from_cuda(launch_dequantize(j, static_cast<cudaStream_t>(stream)));
 }
 
+
 fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
                       void* stream) {
-    fp4_status_t s = check_operand(a);
+    GemmJob j;
+    fp4_status_t s = prepare_gemm(a, b, d, out_fp32, accumulate, j);
     if (s != FP4_OK) return s;
-    s = check_operand(b);
-    if (s != FP4_OK) return s;
-    if (d == nullptr) return FP4_ERR_INVALID_ARG;
-    if (!aligned16(d)) return FP4_ERR_ALIGNMENT;
-    if (accumulate && !out_fp32) return FP4_ERR_INVALID_ARG;
-    const int bs = a->scale_fmt == FP4_SCALE_UE8M0 ? 32 : 16;
-    if (a->scale_fmt != b->scale_fmt || a->block_k != bs || b->block_k != bs) return FP4_ERR_UNSUPPORTED;
-    if (a->scale_layout != FP4_LAYOUT_TCGEN05 || b->scale_layout != FP4_LAYOUT_TCGEN05) return FP4_ERR_UNSUPPORTED;
-    if (a->cols != b->cols) return FP4_ERR_SHAPE;
-    if (a->rows % 128 != 0 || b->rows % 128 != 0 || a->cols % 256 != 0 || a->cols <= 0 || a->rows <= 0 ||
-        b->rows <= 0)
-        return FP4_ERR_SHAPE;
-    GemmJob j{};
-    j.a_codes = a->codes;
-    j.a_scales = a->scales;
-    j.a_sdec = a->s_dec_global;
-    j.b_codes = b->codes;
-    j.b_scales = b->scales;
-    j.b_sdec = b->s_dec_global;
-    j.M = a->rows;
-    j.N = b->rows;
-    j.K = a->cols;
-    j.scale_fmt = a->scale_fmt;
-    j.d = d;
-    j.out_fp32 = out_fp32 != 0;
-    j.accumulate = accumulate != 0;
-    j.status = device_status_ptr();
-    if (j.status == nullptr) return FP4_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (a->scale_fmt != FP4_SCALE_UE5M3) return from_cuda(launch_gemm_nvfp4(j, st));  // NVFP4 and MXFP4
     return from_cuda(launch_gemm_ue5m3(j, st));
+}
+
+size_t fp4_gemm_workspace_bytes(const fp4_tensor_t* a, const fp4_tensor_t* b) {
+    if (a == nullptr || b == nullptr || a->scale_fmt != FP4_SCALE_UE5M3 || a->rows < 0 || b->rows < 0 ||
+        a->cols < 0)
+        return 0;
+    return rebias_layout(a->rows, b->rows, a->cols).total;
+}
+
+fp4_status_t fp4_gemm_ws(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
+                         void* ws, size_t ws_bytes, void* stream) {
+    GemmJob j;
+    fp4_status_t s = prepare_gemm(a, b, d, out_fp32, accumulate, j);
+    if (s != FP4_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (a->scale_fmt != FP4_SCALE_UE5M3) return from_cuda(launch_gemm_nvfp4(j, st));
+    const RebiasLayout l = rebias_layout(j.M, j.N, j.K);
+    if (ws == nullptr || ws_bytes < l.total) return FP4_ERR_WORKSPACE;
+    if (!aligned16(ws)) return FP4_ERR_ALIGNMENT;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    uint8_t* flags = w;
+    int8_t* a_off = reinterpret_cast<int8_t*>(w + l.off_a);
+    int8_t* b_off = reinterpret_cast<int8_t*>(w + l.off_b);
+    uint8_t* a_sc = w + l.sc_a;
+    uint8_t* b_sc = w + l.sc_b;
+    cudaError_t e = launch_rebias_ue5m3(j.a_scales, j.M, j.b_scales, j.N, j.K, a_sc, b_sc, a_off, b_off, flags, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    // native MMA on the rebiased scales, unless a row did not fit; then the
+    // emulated kernel (which reads the UE5M3 scales) runs instead
+    GemmJob jn = j;
+    jn.a_scales = a_sc;
+    jn.b_scales = b_sc;
+    jn.a_off = a_off;
+    jn.b_off = b_off;
+    jn.rb_flags = flags;
+    jn.rb_nflags = j.M / 128 + j.N / 128;
+    e = launch_gemm_nvfp4(jn, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    GemmJob je = j;
+    je.rb_flags = flags;
+    je.rb_nflags = jn.rb_nflags;
+    je.rb_emulated = 1;
+    return from_cuda(launch_gemm_ue5m3(je, st));
 }
 
 fp4_status_t fp4_linear_fprop(const fp4_tensor_t* x, const fp4_tensor_t* w, void* y_bf16, void* stream) {

@@ -64,6 +64,10 @@ struct GemmParams {
     int64_t M, N, K;
     int accumulate;
     int* status;
+    const int8_t* a_off;      // rebiased UE5M3: per-row power-of-two offsets of A and B
+    const int8_t* b_off;
+    const uint8_t* rb_flags;  // rebiased UE5M3: return at once when any of the rb_nflags bytes is set
+    int64_t rb_nflags;
 };
 
 // 256-bit global store (sm_100+), 32-byte aligned destination.
@@ -80,11 +84,14 @@ __device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, ui
 #define FP4_GEMM_CHUNK_K 2048
 #endif
 
-template <int BN_, int STAGES_, int KSTEPS_, int EPI_ROW_BYTES_, bool MX_ = false>
+template <int BN_, int STAGES_, int KSTEPS_, int EPI_ROW_BYTES_, bool MX_ = false, bool RB_ = false>
 struct NvCfg {
     static constexpr int BM = 128, BN = BN_, STAGES = STAGES_;
     // MX: MXFP4 operands (UE8M0 scales per 32 values, no tensor scale)
     static constexpr bool MX = MX_;
+    // RB: UE5M3 operands rebiased onto E4M3 scales; output (m, n) is scaled by
+    // 2^(a_off[m] + b_off[n]) before alpha
+    static constexpr bool RB = RB_;
     static constexpr int KSTEPS = KSTEPS_;         // MMAs (K = 64 each) per stage: 2 or 4
     static constexpr int BK = 64 * KSTEPS;         // FP4 values per stage
     static constexpr int ROW_BYTES = BK / 2;       // 64 or 128 bytes per operand row: the swizzle width
@@ -132,6 +139,9 @@ template <class Cfg, bool OUT32>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
+    // some row could not be rebiased: the emulated kernel takes this product
+    // (uniform across the grid, before any barrier or tensor memory is set up)
+    if (Cfg::RB && rb_any_flag(p.rb_flags, p.rb_nflags)) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -342,6 +352,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (!ok) break;
             const int64_t m = mb * Cfg::BM + q * 32 + lane;
             const int64_t n0 = nb * Cfg::BN + half * Cfg::EPI_COLS;
+            if (Cfg::RB) {
+                // undo the rebias: times 2^(a_off[m] + b_off[n]), a power of two,
+                // so each sum equals the one over the UE5M3-scaled products
+                const int om = p.a_off[m];
+                const uint4* bo = reinterpret_cast<const uint4*>(p.b_off + n0);  // same 128 bytes in every lane
+#pragma unroll
+                for (int v = 0; v < Cfg::EPI_COLS / 16; ++v) {
+                    const uint4 w = bo[v];
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int on = (int)(int8_t)(uint8_t)(ww[k >> 2] >> (8 * (k & 3)));
+                        acc[16 * v + k] = __fmul_rn(acc[16 * v + k], __int_as_float((127 + om + on) << 23));
+                    }
+                }
+            }
             if (!p.accumulate) {
                 // stage 32 rows x EPI_ROW_BYTES per box in shared memory (row =
                 // lane; 16-byte chunk c at c ^ (address bits 7.. of the row): the
@@ -505,7 +531,8 @@ cudaError_t run_nvfp4(const GemmJob& j, cudaStream_t st) {
     if (!make_tmap_u8_swizzled(&ta, j.a_codes, j.M, j.K / 2, Cfg::BM, Cfg::ROW_BYTES)) return cudaErrorInvalidValue;
     if (!make_tmap_u8_swizzled(&tb, j.b_codes, j.N, j.K / 2, Cfg::BN, Cfg::ROW_BYTES)) return cudaErrorInvalidValue;
     if (!make_tmap_out(&td, j.d, j.M, j.N, OUT32, Cfg::EPI_ROW_BYTES)) return cudaErrorInvalidValue;
-    GemmParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status};
+    GemmParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status,
+                 j.a_off, j.b_off, j.rb_flags, j.rb_nflags};
     auto kern = gemm_nvfp4_kernel<Cfg, OUT32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -531,10 +558,111 @@ using NvWide = NvCfg<256, FP4_GEMM_WIDE_STAGES, FP4_GEMM_WIDE_KSTEPS, FP4_GEMM_W
 using NvNarrow = NvCfg<128, FP4_GEMM_NARROW_STAGES, FP4_GEMM_NARROW_KSTEPS, FP4_GEMM_NARROW_EPI>;  // N % 128 == 0
 using MxWide = NvCfg<256, FP4_GEMM_WIDE_STAGES, FP4_GEMM_WIDE_KSTEPS, FP4_GEMM_WIDE_EPI, true>;
 using MxNarrow = NvCfg<128, FP4_GEMM_NARROW_STAGES, FP4_GEMM_NARROW_KSTEPS, FP4_GEMM_NARROW_EPI, true>;
+using RbWide = NvCfg<256, FP4_GEMM_WIDE_STAGES, FP4_GEMM_WIDE_KSTEPS, FP4_GEMM_WIDE_EPI, false, true>;
+using RbNarrow = NvCfg<128, FP4_GEMM_NARROW_STAGES, FP4_GEMM_NARROW_KSTEPS, FP4_GEMM_NARROW_EPI, false, true>;
+
+// ---------------------------------------------------------------- UE5M3 rebias
+// UE5M3 code (nonzero, not 0xFF) -> s = (1 + f / 8) * 2^E: normal codes carry
+// E = e - 15 and f = the mantissa; subnormal codes m / 8 * 2^-14 are normalised.
+__device__ __forceinline__ void ue5m3_normalize(uint32_t code, int& E, int& f) {
+    const int e = (int)(code >> 3), m = (int)(code & 7u);
+    if (e > 0) {
+        E = e - 15;
+        f = m;
+    } else {
+        const int top = 31 - __clz(m);  // 0, 1 or 2
+        E = top - 17;
+        f = (m << (3 - top)) & 7;
+    }
+}
+
+// One CTA per 128-row tile of A or B, kRbParts threads per row: thread
+// (part, t) owns row t of the tile in the chunks c = part mod kRbParts; the
+// row's four scales per 512-byte chunk sit at bytes 16 (t % 32) + 4 (t / 32)
+// .. + 3, so the 128 threads of a part read a chunk in one coalesced sweep.
+// Pass 1 finds the row's largest key 8 E + f and smallest E over its nonzero
+// scales; the offset o puts the largest scale at E4M3 exponent 8 (7 if its
+// mantissa is 7: 0x7F is not a number) and the row fits if the smallest then
+// stays normal (E - o >= -6). Pass 2 writes code ((E - o + 7) << 3) | f, 0 for 0.
+constexpr int kRbParts = 4;
+__global__ void __launch_bounds__(128 * kRbParts)
+    rebias_ue5m3_kernel(const uint8_t* __restrict__ a_sc, int64_t a_tiles, const uint8_t* __restrict__ b_sc,
+                        uint8_t* __restrict__ a_out, uint8_t* __restrict__ b_out, int8_t* __restrict__ a_off,
+                        int8_t* __restrict__ b_off, int64_t nchunks, uint8_t* __restrict__ flags) {
+    __shared__ int kmax_s[kRbParts][128], emin_s[kRbParts][128];
+    const bool is_a = blockIdx.x < a_tiles;
+    const int64_t rt = is_a ? blockIdx.x : blockIdx.x - a_tiles;
+    const uint8_t* src = (is_a ? a_sc : b_sc) + rt * nchunks * 512;
+    uint8_t* dst = (is_a ? a_out : b_out) + rt * nchunks * 512;
+    const int t = threadIdx.x & 127, part = threadIdx.x >> 7;
+    const int woff = 16 * (t & 31) + 4 * (t >> 5);
+    int kmax = -1024, emin = 1024;
+    bool bad = false;
+#pragma unroll 4
+    for (int64_t c = part; c < nchunks; c += kRbParts) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(src + c * 512 + woff);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t code = (w >> (8 * j)) & 0xFFu;
+            if (code == 0u) continue;
+            bad |= code == 0xFFu;
+            int E, f;
+            ue5m3_normalize(code, E, f);
+            kmax = max(kmax, 8 * E + f);
+            emin = min(emin, E);
+        }
+    }
+    kmax_s[part][t] = kmax;
+    emin_s[part][t] = emin;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kRbParts; ++q) {
+        kmax = max(kmax, kmax_s[q][t]);
+        emin = min(emin, emin_s[q][t]);
+    }
+    int o = 0;
+    if (kmax > -1024) {
+        const int emax = kmax >> 3;  // floor division: f = kmax & 7 is in 0..7
+        o = emax - ((kmax & 7) == 7 ? 7 : 8);
+        bad |= emin - o < -6;
+    }
+    if (part == 0) (is_a ? a_off : b_off)[rt * 128 + t] = (int8_t)o;
+    const int any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) flags[blockIdx.x] = any_bad ? 1 : 0;
+#pragma unroll 4
+    for (int64_t c = part; c < nchunks; c += kRbParts) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(src + c * 512 + woff);
+        uint32_t out = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t code = (w >> (8 * j)) & 0xFFu;
+            if (code == 0u || code == 0xFFu) continue;
+            int E, f;
+            ue5m3_normalize(code, E, f);
+            const int e4 = min(max(E - o + 7, 0), 15);  // in 1..15 when the row fits
+            out |= (uint32_t)((e4 << 3) | f) << (8 * j);
+        }
+        *reinterpret_cast<uint32_t*>(dst + c * 512 + woff) = out;
+    }
+}
 
 }  // namespace
 
+cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_t* b_scales, int64_t N, int64_t K,
+                                uint8_t* a_out, uint8_t* b_out, int8_t* a_off, int8_t* b_off, uint8_t* flags,
+                                cudaStream_t st) {
+    const int64_t tiles = M / 128 + N / 128;
+    if (tiles <= 0 || tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    rebias_ue5m3_kernel<<<(unsigned)tiles, 128 * kRbParts, 0, st>>>(a_scales, M / 128, b_scales, a_out, b_out,
+                                                                    a_off, b_off, K / 64, flags);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_nvfp4(const GemmJob& j, cudaStream_t st) {
+    if (j.a_off != nullptr) {
+        if (j.N % 256 == 0) return j.out_fp32 ? run_nvfp4<RbWide, true>(j, st) : run_nvfp4<RbWide, false>(j, st);
+        return j.out_fp32 ? run_nvfp4<RbNarrow, true>(j, st) : run_nvfp4<RbNarrow, false>(j, st);
+    }
     if (j.scale_fmt == FP4_SCALE_UE8M0) {
         if (j.N % 256 == 0) return j.out_fp32 ? run_nvfp4<MxWide, true>(j, st) : run_nvfp4<MxWide, false>(j, st);
         return j.out_fp32 ? run_nvfp4<MxNarrow, true>(j, st) : run_nvfp4<MxNarrow, false>(j, st);

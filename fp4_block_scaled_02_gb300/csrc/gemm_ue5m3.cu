@@ -49,6 +49,8 @@ struct EmuParams {
     int64_t M, N, K;
     int accumulate;
     int* status;
+    const uint8_t* rb_flags;  // nullable: return at once when none of the rb_nflags bytes is set
+    int64_t rb_nflags;
 };
 
 struct EmuCfg {
@@ -132,6 +134,8 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
     gemm_ue5m3_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const EmuParams p) {
     using C = EmuCfg;
+    // the rebiased native kernel took this product (uniform across the grid)
+    if (p.rb_flags != nullptr && !rb_any_flag(p.rb_flags, p.rb_nflags)) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -368,7 +372,8 @@ cudaError_t run_emu(const GemmJob& j, cudaStream_t st) {
     CUtensorMap ta, tb;
     if (!make_tmap_u8_sw128(&ta, j.a_codes, j.M, j.K / 2, EmuCfg::BM)) return cudaErrorInvalidValue;
     if (!make_tmap_u8_sw128(&tb, j.b_codes, j.N, j.K / 2, EmuCfg::BN)) return cudaErrorInvalidValue;
-    EmuParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status};
+    EmuParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status,
+                j.rb_emulated ? j.rb_flags : nullptr, j.rb_nflags};
     auto kern = gemm_ue5m3_kernel<OUT32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, EmuCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -78,9 +78,33 @@ struct GemmJob {
     int out_fp32;
     int accumulate;
     int* status;
+    // UE5M3 operands rebiased onto E4M3 scales (launch_rebias_ue5m3): the scale
+    // pointers above hold the E4M3 bytes and a_off / b_off the per-row power-of-
+    // two offsets. rb_flags[0 .. rb_nflags) are the rebias pass's per-tile
+    // "does not fit" bytes: the rebiased kernel returns at once if any is set,
+    // the emulated kernel (rb_emulated) if none is.
+    const int8_t* a_off;
+    const int8_t* b_off;
+    const uint8_t* rb_flags;
+    int64_t rb_nflags;
+    int rb_emulated;
 };
 cudaError_t launch_gemm_nvfp4(const GemmJob& job, cudaStream_t stream);
 cudaError_t launch_gemm_ue5m3(const GemmJob& job, cudaStream_t stream);
+// Rewrite the UE5M3 block scales of A (M rows) and B (N rows), tensor-core
+// layout with K / 16 scales per row, as E4M3 scales times a per-row power of
+// two: s = e4m3_out * 2^off[row] exactly. flags[t] (one byte per 128-row tile,
+// A's tiles first, M / 128 + N / 128 in all) is set to 1 if a row of tile t
+// has scales spanning more binades than E4M3 holds, else to 0.
+cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_t* b_scales, int64_t N, int64_t K,
+                                uint8_t* a_out, uint8_t* b_out, int8_t* a_off, int8_t* b_off, uint8_t* flags,
+                                cudaStream_t stream);
+// Any of the n bytes at f nonzero (every thread of the calling warp gets the answer).
+__device__ __forceinline__ bool rb_any_flag(const uint8_t* f, int64_t n) {
+    bool any = false;
+    for (int64_t i = threadIdx.x & 31; i < n; i += 32) any |= f[i] != 0;
+    return __any_sync(0xFFFFFFFFu, any) != 0;
+}
 
 // 2-D byte-matrix TMA descriptor with 128-byte rows per box row and 128-byte
 // swizzling (defined in gemm_nvfp4.cu).

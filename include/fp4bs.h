@@ -200,6 +200,26 @@ fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void
 fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32,
                       int accumulate, void* stream);
 
+/* fp4_gemm with a caller workspace, which gives UE5M3 operands the exact fast
+ * path (no tensor core reads UE5M3 scales, "UE5M3 block scales" abstract; the
+ * rebias is this library's design): a first kernel rewrites every row's UE5M3
+ * block scales as E4M3 scales times one power of two per row,
+ * s = e4m3 * 2^o_row exactly, the native kind::mxf4nvf4 GEMM runs on the E4M3
+ * scales and multiplies output (m, n) by 2^(o_m + o_n) before alpha, which
+ * gives the same sum as the UE5M3-scaled products. If some row's nonzero scales
+ * span more than E4M3's 15 binades, the emulated kernel computes the product
+ * instead; the choice is made on the device (no host synchronisation), and the
+ * kernel not chosen returns at once. ws: device, 16-byte aligned, at least
+ * fp4_gemm_workspace_bytes(a, b) bytes (about (M + N) * K / 16), owned by the
+ * caller, overwritten, not to be shared by calls in flight at the same time.
+ * Too small or NULL: FP4_ERR_WORKSPACE. Other scale formats ignore ws and run
+ * exactly as fp4_gemm. After the stream has run the call, byte t of ws
+ * (t < M / 128 + N / 128, A's 128-row tiles first) is 1 if tile t held a row
+ * that did not fit and 0 otherwise: all zero means the native kernel ran. */
+size_t fp4_gemm_workspace_bytes(const fp4_tensor_t* a, const fp4_tensor_t* b);
+fp4_status_t fp4_gemm_ws(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
+                         void* ws, size_t ws_bytes, void* stream);
+
 /* The three GEMMs of a linear layer Y = X W^T (section 4.1, Fig. 5):
  *   Fprop: Y[T x N]  = X[T x K]   . W[N x K]^T     (x rowwise, w 16x16), BF16 out
  *   Dgrad: dX[T x K] = dY[T x N]  . Wt[K x N]^T    (dy rowwise, wt = W^T operand), BF16 out

@@ -221,7 +221,81 @@ def test_gemm_ue5m3_emulated_full_output(M, N, K, out32):
     _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
 
 
-def test_gemm_ue5m3_wide_scale_range_sampled():
+def _ws_for(a, b):
+    return torch.zeros(fb.fp4_gemm_workspace_bytes(a, b), dtype=torch.uint8, device="cuda")
+
+
+def _took_native(ws, a, b) -> bool:
+    """The rebias pass leaves one zero byte per 128-row tile at the start of the
+    workspace when every row of the tile fit."""
+    return int(ws[: a.rows // 128 + b.rows // 128].sum().item()) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1280, 1152, 768), (512, 1024, 2304)])
+@pytest.mark.parametrize("out32", [False, True])
+def test_gemm_ue5m3_rebiased_native_full_output(M, N, K, out32):
+    """UE5M3 operands on the native MMA after the per-row rebias onto E4M3."""
+    ra, a = _operand(41, M, K, "log_normal_1e-4_2", fmt=UE, target_T=2048.0)
+    rb, b = _operand(42, N, K, "student_t4", fmt=UE, target_T=448.0)
+    d = torch.empty((M, N), dtype=torch.float32 if out32 else torch.bfloat16, device="cuda")
+    ws = _ws_for(a, b)
+    fb.fp4_gemm(a, b, d, ws=ws)
+    assert fb.fp4_device_status() == 0
+    assert _took_native(ws, a, b)
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                           scale_fmt=oracle.FMT_UE5M3)
+    _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
+
+
+def _set_row(scales, r, codes):
+    scales[r, :] = np.resize(np.array(codes, dtype=np.uint8), scales.shape[1])
+
+
+def test_gemm_ue5m3_rebias_edges_and_fallback():
+    """Rows at the edge of what one E4M3 offset covers: the largest scale with
+    mantissa 7 (placed at E4M3 exponent 7) and the smallest 13 binades below;
+    mantissa <= 6 (exponent 8) with the smallest 14 binades below; UE5M3
+    subnormal scales. All fit and run natively. One more binade in a single row
+    sends the whole product to the emulated kernel. Both give the oracle's sums."""
+    M, N, K = 256, 256, 512
+    ra, _ = _operand(45, M, K, "normal", fmt=UE)
+    rb, _ = _operand(46, N, K, "weight", fmt=UE)
+    sa, sb = ra["scales"].copy(), rb["scales"].copy()
+    _set_row(sa, 0, [0xA7, 0x38, 0x60, 0x80, 0x00])   # E 5 (f 7) .. -8
+    _set_row(sa, 130, [0xA6, 0x30, 0x99])              # E 5 (f 6) .. -9
+    _set_row(sb, 7, [0x50, 0x01, 0x03, 0x07, 0x0F])    # E -5 .. -17 (subnormals)
+    _set_row(sb, 255, [0x00])                          # all-zero row
+    for fallback in (False, True):
+        if fallback:
+            _set_row(sa, 9, [0xA7, 0x30])              # 14 binades under a mantissa-7 maximum
+        ra2, rb2 = dict(ra, scales=sa), dict(rb, scales=sb)
+        a, b = upload_operand(ra2, M, K, UE), upload_operand(rb2, N, K, UE)
+        for out32 in (False, True):
+            d = torch.empty((M, N), dtype=torch.float32 if out32 else torch.bfloat16, device="cuda")
+            ws = _ws_for(a, b)
+            fb.fp4_gemm(a, b, d, ws=ws)
+            assert fb.fp4_device_status() == 0
+            assert _took_native(ws, a, b) == (not fallback)
+            c_ref, s = oracle.gemm(ra2["codes"], sa, ra2["s_dec"], rb2["codes"], sb, rb2["s_dec"],
+                                   scale_fmt=oracle.FMT_UE5M3)
+            _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
+
+
+def test_gemm_ue5m3_workspace_checks():
+    _, a = _operand(47, 128, 256, "normal", fmt=UE)
+    _, b = _operand(48, 128, 256, "normal", fmt=UE)
+    need = fb.fp4_gemm_workspace_bytes(a, b)
+    assert need >= 2 * 128 * 256 // 16
+    d = torch.empty((128, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(fb.Fp4Error) as e:
+        fb.fp4_gemm(a, b, d, ws=torch.empty(need - 16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == fb._lib.FP4_ERR_WORKSPACE
+    _, c = _operand(49, 128, 256, "normal")
+    assert fb.fp4_gemm_workspace_bytes(c, c) == 0  # NVFP4 needs none
+
+
+@pytest.mark.parametrize("native", [False, True])
+def test_gemm_ue5m3_wide_scale_range_sampled(native):
     # scales spread over many binades: a x10^3 drift against a held amax
     # saturates some blocks and drives others toward the UE5M3 subnormals
     M, N, K = 1024, 1024, 1024
@@ -237,7 +311,8 @@ def test_gemm_ue5m3_wide_scale_range_sampled():
     a = upload_operand(ra, M, K, UE)
     rb, b = _operand(44, N, K, "weight", fmt=UE)
     d = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    fb.fp4_gemm(a, b, d)
+    fb.fp4_gemm(a, b, d, ws=_ws_for(a, b) if native else None)
+    assert fb.fp4_device_status() == 0
     rng = np.random.default_rng(2)
     ms, ns = rng.integers(0, M, 3000), rng.integers(0, N, 3000)
     c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
@@ -245,10 +320,10 @@ def test_gemm_ue5m3_wide_scale_range_sampled():
     _check(d.cpu().numpy()[ms, ns], c_ref, s, bf16=False)
 
 
-@pytest.mark.parametrize("T_target", [448.0, 2048.0])
-def test_ue5m3_periodic_scaling_sweep_steps(T_target):
+@pytest.mark.parametrize("T_target,native", [(448.0, False), (2048.0, False), (448.0, True), (2048.0, True)])
+def test_ue5m3_periodic_scaling_sweep_steps(T_target, native):
     """Sweep workload (4096 -> 4096, T = 8192): held amax refreshed every 50 steps,
-    UE5M3 scales, SR on gradients, no RHT, emulated GEMMs. Steps 0, 49, 50, 99
+    UE5M3 scales, SR on gradients, no RHT, emulated or rebiased native GEMMs. Steps 0, 49, 50, 99
     run in order on the GPU and the oracle; quantized bytes, counters and held
     state match exactly and sampled GEMM outputs meet the bound."""
     from workloads import sweep_dy
@@ -256,7 +331,8 @@ def test_ue5m3_periodic_scaling_sweep_steps(T_target):
     lin = w.linears[0]
     inp = linear_inputs(w, 0)
     T, K, N = lin.tokens, lin.k_in, lin.n_out
-    L = fb.Fp4Linear(T, K, N, scale_fmt=UE, rht=False, held=True, target_T=T_target, seed=w.sr_seed)
+    L = fb.Fp4Linear(T, K, N, scale_fmt=UE, rht=False, held=True, target_T=T_target, seed=w.sr_seed,
+                     ue5m3_native=native)
     x, wt = to_gpu_bf16(inp["x"]), to_gpu_bf16(inp["w"])
     y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
     dx = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
