@@ -141,7 +141,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                       const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
     // some row could not be rebiased: the emulated kernel takes this product
     // (uniform across the grid, before any barrier or tensor memory is set up)
-    if (Cfg::RB && rb_any_flag(p.rb_flags, p.rb_nflags)) return;
+    if (Cfg::RB) {
+        pdl_wait();
+        if (rb_any_flag(p.rb_flags, p.rb_nflags)) return;
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,6 +179,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tc::prefetch_tmap(&tmap_b);
         tc::prefetch_tmap(&tmap_d);
     }
+    if (!Cfg::RB) pdl_wait();
+    pdl_trigger();
     if (warp == 1) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), Cfg::TMEM_COLS);
         tc::tmem_relinquish();
@@ -538,7 +543,7 @@ cudaError_t run_nvfp4(const GemmJob& j, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int64_t tiles = (j.M / Cfg::BM) * (j.N / Cfg::BN);
     const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, td, p);
+    (void)launch_pdl(kern, grid, Cfg::THREADS, Cfg::SMEM_BYTES, st, ta, tb, td, p);
     return cudaGetLastError();
 }
 
@@ -589,6 +594,7 @@ __global__ void __launch_bounds__(128 * kRbParts)
     rebias_ue5m3_kernel(const uint8_t* __restrict__ a_sc, int64_t a_tiles, const uint8_t* __restrict__ b_sc,
                         uint8_t* __restrict__ a_out, uint8_t* __restrict__ b_out, int8_t* __restrict__ a_off,
                         int8_t* __restrict__ b_off, int64_t nchunks, uint8_t* __restrict__ flags) {
+    pdl_begin();
     __shared__ int kmax_s[kRbParts][128], emin_s[kRbParts][128];
     const bool is_a = blockIdx.x < a_tiles;
     const int64_t rt = is_a ? blockIdx.x : blockIdx.x - a_tiles;
@@ -653,7 +659,7 @@ cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_
                                 cudaStream_t st) {
     const int64_t tiles = M / 128 + N / 128;
     if (tiles <= 0 || tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    rebias_ue5m3_kernel<<<(unsigned)tiles, 128 * kRbParts, 0, st>>>(a_scales, M / 128, b_scales, a_out, b_out,
+    (void)launch_pdl(rebias_ue5m3_kernel, (unsigned)tiles, 128 * kRbParts, 0, st, a_scales, M / 128, b_scales, a_out, b_out,
                                                                     a_off, b_off, K / 64, flags);
     return cudaGetLastError();
 }

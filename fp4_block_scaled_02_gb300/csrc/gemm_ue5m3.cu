@@ -135,7 +135,10 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
                       const EmuParams p) {
     using C = EmuCfg;
     // the rebiased native kernel took this product (uniform across the grid)
-    if (p.rb_flags != nullptr && !rb_any_flag(p.rb_flags, p.rb_nflags)) return;
+    if (p.rb_flags != nullptr) {
+        pdl_wait();
+        if (!rb_any_flag(p.rb_flags, p.rb_nflags)) return;
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,6 +175,8 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         tc::prefetch_tmap(&tmap_a);
         tc::prefetch_tmap(&tmap_b);
     }
+    if (p.rb_flags == nullptr) pdl_wait();
+    pdl_trigger();
     if (warp == 1) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
         tc::tmem_relinquish();
@@ -379,7 +384,7 @@ cudaError_t run_emu(const GemmJob& j, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int64_t tiles = (j.M / EmuCfg::BM) * (j.N / EmuCfg::BN);
     const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
-    kern<<<grid, EmuCfg::THREADS, EmuCfg::SMEM_BYTES, st>>>(ta, tb, p);
+    (void)launch_pdl(kern, grid, EmuCfg::THREADS, EmuCfg::SMEM_BYTES, st, ta, tb, p);
     return cudaGetLastError();
 }
 

@@ -3,12 +3,42 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "fp4bs.h"
 
 namespace fp4bs {
+
+// Programmatic dependent launch. Every kernel of the library is launched with
+// launch_pdl, so the stream may start it while the kernel before it is still
+// finishing; the kernel calls pdl_wait() before its first access to global
+// memory (and before it allocates tensor memory), which returns once the
+// previous grid has completed and its writes are visible, and then pdl_trigger()
+// so the next kernel can be scheduled onto SMs as they free up. Only on-chip
+// setup (shared memory, mbarrier init, tensor-map prefetch) may precede the wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // One quantizer launch, after validation. Operand shape is rows x cols of the
 // INPUT; `colwise` makes the operand its transpose.

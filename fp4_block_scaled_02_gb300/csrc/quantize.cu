@@ -234,6 +234,7 @@ __device__ __forceinline__ bool amax_pass_skipped(const fp4_amax_state_t* a, con
 __global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __restrict__ in, int64_t n_vec,
                                                                  float* __restrict__ partials,
                                                                  const fp4_amax_state_t* skip_if_valid) {
+    pdl_begin();
     if (amax_pass_skipped(skip_if_valid, nullptr)) return;
     uint32_t m = 0u;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __
 __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ in, int64_t T,
                                                                  int64_t C, float* __restrict__ partials,
                                                                  const fp4_amax_state_t* skip_if_valid) {
+    pdl_begin();
     if (amax_pass_skipped(skip_if_valid, nullptr)) return;
     const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
 // all four 16-byte loads issued before either block is converted.
 template <int FMT, bool SR, bool TCL>
 __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
+    pdl_begin();
     __shared__ float enc_tab[256];
     float s_enc, s_dec;
     if (!cta_tensor_scale(q, s_enc, s_dec)) return;
@@ -367,6 +370,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
 // scale bytes.
 template <int FMT, bool SR, bool RHT, bool TCL>
 __global__ void __launch_bounds__(kThreads, 2) quantize_cols_kernel(QParams q) {
+    pdl_begin();
     __shared__ float enc_tab[256];
     float s_enc, s_dec;
     if (!cta_tensor_scale(q, s_enc, s_dec)) return;
@@ -444,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_cols_kernel(QParams q) {
 // omitted (null codes pointer).
 template <int FMT, bool TCL_W, bool TCL_WT>
 __global__ void __launch_bounds__(kThreads) quantize_2d_kernel(QParams q) {
+    pdl_begin();
     float s_enc, s_dec;
     if (!cta_tensor_scale(q, s_enc, s_dec)) return;
     using F = ScaleFmt<FMT>;
@@ -547,6 +552,7 @@ __device__ __forceinline__ uint32_t tile2d_offset(int r, int c) {
 template <int FMT, bool SR, bool TCL_W, bool TCL_WT>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_2d_tile_kernel(const __grid_constant__ CUtensorMap tmap_w, QParams q) {
+    pdl_begin();
     extern __shared__ uint8_t tile2d_smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tile2d_smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ float tab[256];
@@ -721,6 +727,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // power of two that rounds amax_B / 6 up, value scaled by 2^-e exactly, RNE.
 template <bool TCL>
 __global__ void __launch_bounds__(kThreads) quantize_mx_rows_kernel(QParams q) {
+    pdl_begin();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (q.s_dec) *q.s_dec = 1.0f;
     }
@@ -791,6 +798,7 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __r
                                                               const uint8_t* __restrict__ scales,
                                                               const float* __restrict__ s_dec_p, int64_t rows,
                                                               int64_t cols, void* __restrict__ out) {
+    pdl_begin();
     const float s_dec = *s_dec_p;
     const int64_t nb_row = cols / BS, nblk = rows * nb_row;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -847,6 +855,7 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __r
                                                              float* __restrict__ partials_col,
                                                              const fp4_amax_state_t* skip_row,
                                                              const fp4_amax_state_t* skip_col) {
+    pdl_begin();
     if (amax_pass_skipped(skip_row, skip_col)) return;
     const int64_t ug = C / 4, uj = T / 16, units = ug * uj;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -903,6 +912,7 @@ constexpr int kDualSmemBytes = kDualStages * kDualTileBytes + 1024;
 template <int FMT, bool SR_ROW, bool SR_COL, bool RHT>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams qr, QParams qc) {
+    pdl_begin();
     extern __shared__ uint8_t dual_smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dual_smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ float tab_r[256], tab_c[256];
@@ -1064,7 +1074,7 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
         auto kern = j.sr ? quantize_2d_tile_kernel<FMT, true, TA, TB> : quantize_2d_tile_kernel<FMT, false, TA, TB>;  \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, k2dSmemBytes);      \
         if (e != cudaSuccess) return e;                                                                             \
-        kern<<<g2, kThreads, k2dSmemBytes, st>>>(tmap_w, p);                                                        \
+        (void)launch_pdl(kern, g2, kThreads, k2dSmemBytes, st, tmap_w, p);                                                        \
     } while (0)
             if (a && b) FP4_2D_TILE(true, true);
             else if (a) FP4_2D_TILE(true, false);
@@ -1074,26 +1084,26 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
             return cudaGetLastError();
         }
         if (j.sr) return cudaErrorNotSupported;  // the half-warp kernel rounds to nearest only
-        if (a && b) quantize_2d_kernel<FMT, true, true><<<grid, kThreads, 0, st>>>(p);
-        else if (a) quantize_2d_kernel<FMT, true, false><<<grid, kThreads, 0, st>>>(p);
-        else if (b) quantize_2d_kernel<FMT, false, true><<<grid, kThreads, 0, st>>>(p);
-        else quantize_2d_kernel<FMT, false, false><<<grid, kThreads, 0, st>>>(p);
+        if (a && b) (void)launch_pdl(quantize_2d_kernel<FMT, true, true>, grid, kThreads, 0, st, p);
+        else if (a) (void)launch_pdl(quantize_2d_kernel<FMT, true, false>, grid, kThreads, 0, st, p);
+        else if (b) (void)launch_pdl(quantize_2d_kernel<FMT, false, true>, grid, kThreads, 0, st, p);
+        else (void)launch_pdl(quantize_2d_kernel<FMT, false, false>, grid, kThreads, 0, st, p);
         return cudaGetLastError();
     }
     if (!j.colwise) {
         const int grid = grid_for(j.rows * (j.cols / 16), 8);
         if (j.sr) {
-            if (tcl) quantize_rows_kernel<FMT, true, true><<<grid, kThreads, 0, st>>>(q);
-            else quantize_rows_kernel<FMT, true, false><<<grid, kThreads, 0, st>>>(q);
+            if (tcl) (void)launch_pdl(quantize_rows_kernel<FMT, true, true>, grid, kThreads, 0, st, q);
+            else (void)launch_pdl(quantize_rows_kernel<FMT, true, false>, grid, kThreads, 0, st, q);
         } else {
-            if (tcl) quantize_rows_kernel<FMT, false, true><<<grid, kThreads, 0, st>>>(q);
-            else quantize_rows_kernel<FMT, false, false><<<grid, kThreads, 0, st>>>(q);
+            if (tcl) (void)launch_pdl(quantize_rows_kernel<FMT, false, true>, grid, kThreads, 0, st, q);
+            else (void)launch_pdl(quantize_rows_kernel<FMT, false, false>, grid, kThreads, 0, st, q);
         }
         return cudaGetLastError();
     }
     const int64_t wunits = ((j.cols / 4 + 7) / 8) * ((j.rows / 16 + 3) / 4);
     const int grid = grid_for(wunits * 32, 8);
-#define FP4_COLS(SR, RHT, TCL) quantize_cols_kernel<FMT, SR, RHT, TCL><<<grid, kThreads, 0, st>>>(q)
+#define FP4_COLS(SR, RHT, TCL) launch_pdl(quantize_cols_kernel<FMT, SR, RHT, TCL>, grid, kThreads, 0, st, q)
     if (j.sr) {
         if (j.rht) { if (tcl) FP4_COLS(true, true, true); else FP4_COLS(true, true, false); }
         else { if (tcl) FP4_COLS(true, false, true); else FP4_COLS(true, false, false); }
@@ -1160,8 +1170,8 @@ cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
 
     if (j.scale_fmt == kFmtUE8M0) {
         const int grid = grid_for(j.rows * (j.cols / 32), 8);
-        if (j.layout == FP4_LAYOUT_TCGEN05) quantize_mx_rows_kernel<true><<<grid, kThreads, 0, st>>>(q);
-        else quantize_mx_rows_kernel<false><<<grid, kThreads, 0, st>>>(q);
+        if (j.layout == FP4_LAYOUT_TCGEN05) (void)launch_pdl(quantize_mx_rows_kernel<true>, grid, kThreads, 0, st, q);
+        else (void)launch_pdl(quantize_mx_rows_kernel<false>, grid, kThreads, 0, st, q);
         return cudaGetLastError();
     }
     // pass 1 (current scaling, or a held-amax refresh step): amax partials
@@ -1169,8 +1179,8 @@ cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
     q.npartials = np;
     if (np > 0) {
         const fp4_amax_state_t* skip = (j.held && !j.refresh) ? j.state : nullptr;
-        if (j.rht) amax_rht_cols_kernel<<<np, kThreads, 0, st>>>(j.in, j.rows, j.cols, j.partials, skip);
-        else amax_plain_kernel<<<np, kThreads, 0, st>>>(reinterpret_cast<const uint4*>(j.in), j.rows * j.cols / 8,
+        if (j.rht) (void)launch_pdl(amax_rht_cols_kernel, np, kThreads, 0, st, j.in, j.rows, j.cols, j.partials, skip);
+        else (void)launch_pdl(amax_plain_kernel, np, kThreads, 0, st, reinterpret_cast<const uint4*>(j.in), j.rows * j.cols / 8,
                                                          j.partials, skip);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1187,11 +1197,11 @@ cudaError_t launch_dequantize(const DequantJob& j, cudaStream_t st) {
 #define FP4_DQ(FMT, BS)                                                                                           \
     do {                                                                                                          \
         if (tcl) {                                                                                                \
-            if (j.out_fp32) dequantize_kernel<FMT, BS, true, true><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
-            else dequantize_kernel<FMT, BS, true, false><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            if (j.out_fp32) (void)launch_pdl(dequantize_kernel<FMT, BS, true, true>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            else (void)launch_pdl(dequantize_kernel<FMT, BS, true, false>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
         } else {                                                                                                  \
-            if (j.out_fp32) dequantize_kernel<FMT, BS, false, true><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
-            else dequantize_kernel<FMT, BS, false, false><<<grid, kThreads, 0, st>>>(j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            if (j.out_fp32) (void)launch_pdl(dequantize_kernel<FMT, BS, false, true>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            else (void)launch_pdl(dequantize_kernel<FMT, BS, false, false>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
         }                                                                                                         \
     } while (0)
     if (j.scale_fmt == kFmtE4M3) FP4_DQ(kFmtE4M3, 16);
@@ -1218,10 +1228,10 @@ cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStr
         const int np = dual_amax_grid(jc);
         qr.npartials = qc.npartials = np;
         if (jc.rht)
-            amax_dual_kernel<true><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
+            (void)launch_pdl(amax_dual_kernel<true>, np, kThreads, 0, st, jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
                                                              skip_c);
         else
-            amax_dual_kernel<false><<<np, kThreads, 0, st>>>(jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
+            (void)launch_pdl(amax_dual_kernel<false>, np, kThreads, 0, st, jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
                                                               skip_c);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1236,7 +1246,7 @@ cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStr
         auto kern = quantize_dual_kernel<FMT, SR, SR, RHT>;                                                      \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDualSmemBytes); \
         if (e != cudaSuccess) return e;                                                                          \
-        kern<<<grid, kThreads, kDualSmemBytes, st>>>(tmap_x, qr, qc);                                            \
+        (void)launch_pdl(kern, grid, kThreads, kDualSmemBytes, st, tmap_x, qr, qc);                                            \
     } while (0)
     if (jr.scale_fmt == kFmtE4M3) {
         if (jr.sr) { if (jc.rht) FP4_DUAL(kFmtE4M3, true, true); else FP4_DUAL(kFmtE4M3, true, false); }
