@@ -20,10 +20,11 @@ import torch
 from . import _lib
 from ._lib import (FP4_BLOCK_1x16, FP4_BLOCK_1x32, FP4_BLOCK_16x16, FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05,
                    FP4_ORIENT_COLWISE, FP4_ORIENT_ROWWISE, FP4_ROUND_RNE, FP4_ROUND_SR, FP4_SCALE_E4M3,
-                   FP4_SCALE_UE5M3, FP4_SCALE_UE8M0, FP4_TSCALE_CURRENT, FP4_TSCALE_HELD, Fp4Error)
+                   FP4_SCALE_UE5M3, FP4_SCALE_UE8M0, FP4_TSCALE_CURRENT, FP4_TSCALE_GIVEN, FP4_TSCALE_HELD,
+                   Fp4Error)
 
 __all__ = ["QTensor", "QuantConfig", "AmaxState", "fp4_quantize", "fp4_quantize_dual", "fp4_dequantize", "fp4_gemm",
-           "fp4_gemm_workspace_bytes", "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
+           "fp4_gemm_workspace_bytes", "fp4_tensor_amax", "fp4_tensor_amax_dual", "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
            "fp4_workspace_bytes", "fp4_quantized_sizes", "Fp4Error", "Fp4Linear"]
 
 
@@ -152,6 +153,30 @@ def fp4_quantize_dual(cfg_row: QuantConfig, cfg_col: QuantConfig, x: torch.Tenso
     _lib.check(st, "fp4_quantize_dual")
 
 
+AMAX_WS_BYTES = 2 * 2048 * 4  # workspace of fp4_tensor_amax / fp4_tensor_amax_dual
+
+
+def fp4_tensor_amax(cfg: QuantConfig, x: torch.Tensor, out: AmaxState, ws: torch.Tensor, stream=None) -> None:
+    """Tensor amax of the operand `cfg` describes into `out` (fp4_tensor_amax in fp4bs.h), for a later
+    fp4_quantize with tscale FP4_TSCALE_GIVEN."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    p = cfg.params()
+    _lib.check(_lib.load().fp4_tensor_amax(ctypes.byref(p), _ptr(x), x.shape[0], x.shape[1], _ptr(out.buf),
+                                           _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+               "fp4_tensor_amax")
+
+
+def fp4_tensor_amax_dual(cfg_row: QuantConfig, cfg_col: QuantConfig, x: torch.Tensor, out_row: AmaxState,
+                         out_col: AmaxState, ws: torch.Tensor, stream=None) -> None:
+    """Rowwise and colwise operand amaxes of `x` from one read (fp4_tensor_amax_dual in fp4bs.h)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    pr, pc = cfg_row.params(), cfg_col.params()
+    _lib.check(_lib.load().fp4_tensor_amax_dual(ctypes.byref(pr), ctypes.byref(pc), _ptr(x), x.shape[0], x.shape[1],
+                                                _ptr(out_row.buf), _ptr(out_col.buf), _ptr(ws),
+                                                ws.numel() * ws.element_size(), _stream(stream)),
+               "fp4_tensor_amax_dual")
+
+
 def fp4_dequantize(t: QTensor, out: torch.Tensor, stream=None) -> None:
     assert out.is_contiguous() and out.dtype in (torch.float32, torch.bfloat16)
     d = t.desc()
@@ -215,7 +240,13 @@ class Fp4Linear:
     scale_fmt E4M3 gives NVFP4 with current tensor scaling; UE5M3 gives the
     UE5M3 recipe (held amax refreshed every `refresh_every` steps with target T,
     no RHT), whose GEMMs take the rebiased native path (fp4_gemm_ws) when
-    `ue5m3_native` is set, else the emulated one."""
+    `ue5m3_native` is set, else the emulated one.
+
+    With current scaling and `overlap_amax` set (and T, K, N multiples of 128),
+    the tensor amaxes of W and dY are computed on a second stream
+    (fp4_tensor_amax) while X is quantized on the caller's stream, and W and dY
+    are then quantized with those amaxes (FP4_TSCALE_GIVEN): the same bytes as
+    current scaling, with their amax passes off the critical path."""
     tokens: int
     k_in: int
     n_out: int
@@ -227,6 +258,7 @@ class Fp4Linear:
     held: bool = False
     refresh_every: int = 50
     ue5m3_native: bool = True
+    overlap_amax: bool = True
     device: str = "cuda"
     bufs: dict = field(default_factory=dict)
 
@@ -244,6 +276,13 @@ class Fp4Linear:
                               device=dev)
         self.counters = torch.zeros((5, 4), dtype=torch.int64, device=dev)
         self.states = [AmaxState(dev) for _ in range(5)] if self.held else [None] * 5
+        self.side = None
+        if self.overlap_amax and not self.held and T % 128 == 0 and K % 128 == 0 and N % 128 == 0:
+            self.side = torch.cuda.Stream(device=dev)
+            self.ws_side = torch.empty(AMAX_WS_BYTES // 4, dtype=torch.float32, device=dev)
+            self.given = [AmaxState(dev) for _ in range(5)]
+            self.ev_inputs = torch.cuda.Event()
+            self.ev_amax = torch.cuda.Event()
         self.gemm_ws = None
         if f == FP4_SCALE_UE5M3 and self.ue5m3_native:
             b = self.bufs
@@ -265,6 +304,9 @@ class Fp4Linear:
         b, c = self.bufs, self.counters
         rht = self.rht
         dual_ok = self.tokens % 128 == 0 and self.k_in % 128 == 0 and self.n_out % 128 == 0
+        if self.side is not None:
+            self._quantize_all_overlapped(x, w, dy, step, stream)
+            return
         if dual_ok:
             fp4_quantize_dual(self._cfg(0, step), self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x,
                               b["x"], b["xt"], self.states[0], self.states[1], c[0], c[1], ws=self.ws,
@@ -286,6 +328,29 @@ class Fp4Linear:
                          ws=self.ws, stream=stream)
             fp4_quantize(self._cfg(4, step, orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR), dy, b["dyt"],
                          state=self.states[4], counters=c[4], ws=self.ws, stream=stream)
+
+    def _quantize_all_overlapped(self, x, w, dy, step, stream):
+        b, c, g, rht = self.bufs, self.counters, self.given, self.rht
+        main = torch.cuda.current_stream() if stream is None else stream
+        self.ev_inputs.record(main)
+        self.side.wait_event(self.ev_inputs)
+        w_cfg = dict(block=FP4_BLOCK_16x16)
+        dy_r = dict(round=FP4_ROUND_SR)
+        dy_c = dict(orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR)
+        w.record_stream(self.side)  # read on the side stream: keep the allocator from reusing it early
+        dy.record_stream(self.side)
+        fp4_tensor_amax(self._cfg(2, step, **w_cfg), w, g[2], self.ws_side, stream=self.side)
+        fp4_tensor_amax_dual(self._cfg(3, step, **dy_r), self._cfg(4, step, **dy_c), dy, g[3], g[4], self.ws_side,
+                             stream=self.side)
+        self.ev_amax.record(self.side)
+        fp4_quantize_dual(self._cfg(0, step), self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x,
+                          b["x"], b["xt"], None, None, c[0], c[1], ws=self.ws, stream=main)
+        main.wait_event(self.ev_amax)
+        giv = dict(tscale=FP4_TSCALE_GIVEN)
+        fp4_quantize(self._cfg(2, step, emit_transpose=True, **w_cfg, **giv), w, b["w"], b["wt"], state=g[2],
+                     counters=c[2], stream=main)
+        fp4_quantize_dual(self._cfg(3, step, **dy_r, **giv), self._cfg(4, step, **dy_c, **giv), dy, b["dy"], b["dyt"],
+                          g[3], g[4], c[3], c[4], stream=main)
 
     def gemms(self, y: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor, stream=None):
         b = self.bufs

@@ -28,14 +28,14 @@ FP4_ERR_WORKSPACE = 8
 FP4_SCALE_E4M3, FP4_SCALE_UE5M3, FP4_SCALE_UE8M0 = 0, 1, 2
 FP4_BLOCK_1x16, FP4_BLOCK_16x16, FP4_BLOCK_1x32 = 0, 1, 2
 FP4_ROUND_RNE, FP4_ROUND_SR = 0, 1
-FP4_TSCALE_CURRENT, FP4_TSCALE_HELD = 0, 1
+FP4_TSCALE_CURRENT, FP4_TSCALE_HELD, FP4_TSCALE_GIVEN = 0, 1, 2
 FP4_ORIENT_ROWWISE, FP4_ORIENT_COLWISE = 0, 1
 FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05 = 0, 1
 
 EXPORTED = ["fp4_quantized_sizes", "fp4_workspace_bytes", "fp4_quantize", "fp4_dequantize", "fp4_gemm",
             "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
             "fp4_status_string", "fp4_abi_version", "fp4_quantize_noalloc", "fp4_quantize_dual",
-            "fp4_gemm_workspace_bytes", "fp4_gemm_ws"]
+            "fp4_gemm_workspace_bytes", "fp4_gemm_ws", "fp4_tensor_amax", "fp4_tensor_amax_dual"]
 
 
 class fp4_quant_params_t(ctypes.Structure):
@@ -86,6 +86,10 @@ def load() -> ctypes.CDLL:
             L.fp4_quantize_dual.restype = i32
             L.fp4_quantize_noalloc.argtypes = [QP, P, i64, i64, TP, TP, P, P, P]
             L.fp4_quantize_noalloc.restype = i32
+            L.fp4_tensor_amax.argtypes = [QP, P, i64, i64, P, P, sz, P]
+            L.fp4_tensor_amax.restype = i32
+            L.fp4_tensor_amax_dual.argtypes = [QP, QP, P, i64, i64, P, P, P, sz, P]
+            L.fp4_tensor_amax_dual.restype = i32
             L.fp4_dequantize.argtypes = [TP, P, i32, P]
             L.fp4_dequantize.restype = i32
             L.fp4_gemm.argtypes = [TP, TP, P, i32, i32, P]

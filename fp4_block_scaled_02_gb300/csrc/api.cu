@@ -75,7 +75,7 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     if (p->reserved != 0 || out->reserved != 0) return FP4_ERR_INVALID_ARG;
     if (p->scale_fmt < 0 || p->scale_fmt > 2 || p->block < 0 || p->block > 2) return FP4_ERR_INVALID_ARG;
     if (p->round < 0 || p->round > 1 || p->orient < 0 || p->orient > 1) return FP4_ERR_INVALID_ARG;
-    if (p->tscale < 0 || p->tscale > 1 || p->scale_layout < 0 || p->scale_layout > 1) return FP4_ERR_INVALID_ARG;
+    if (p->tscale < 0 || p->tscale > 2 || p->scale_layout < 0 || p->scale_layout > 1) return FP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0) return FP4_ERR_SHAPE;
     if (p->tensor_id == 0xFFFFFFFFu) return FP4_ERR_INVALID_ARG;
     const bool mx = p->scale_fmt == FP4_SCALE_UE8M0;
@@ -88,7 +88,9 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     if (p->emit_transpose && p->block != FP4_BLOCK_16x16) return FP4_ERR_INVALID_ARG;
     if (p->emit_transpose && out_t == nullptr) return FP4_ERR_INVALID_ARG;
     const bool held = !mx && p->tscale == FP4_TSCALE_HELD;
+    const bool given = !mx && p->tscale == FP4_TSCALE_GIVEN;
     if (held && (state == nullptr || p->refresh_every == 0)) return FP4_ERR_INVALID_ARG;
+    if (given && state == nullptr) return FP4_ERR_INVALID_ARG;
     if (!mx && !(p->target_T > 0.0f && p->target_T <= 3.0e38f)) return FP4_ERR_INVALID_ARG;
 
     const int bs = block_len(p->block);
@@ -125,8 +127,9 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     job.sr = p->round == FP4_ROUND_SR;
     job.colwise = colwise;
     job.rht = p->rht != 0;
-    job.held = held;
-    job.refresh = held ? (p->step % p->refresh_every == 0) : 1;
+    job.held = held || given;
+    job.refresh = given ? 0 : held ? (p->step % p->refresh_every == 0) : 1;
+    job.given = given;
     job.target_T = p->target_T;
     job.tensor_id = p->tensor_id;
     job.seed = p->seed;
@@ -258,6 +261,26 @@ RebiasLayout rebias_layout(int64_t M, int64_t N, int64_t K) {
 
 }  // namespace
 
+namespace {
+
+// Shape rules of a tensor amax: those of the quantize call with the same
+// parameters (its blocks must tile the tensor).
+fp4_status_t check_amax_params(const fp4_quant_params_t* p, int64_t rows, int64_t cols) {
+    if (p == nullptr) return FP4_ERR_INVALID_ARG;
+    if (p->scale_fmt < 0 || p->scale_fmt > 1) return FP4_ERR_INVALID_ARG;  // MXFP4 has no tensor amax
+    if (p->block < 0 || p->block > 1 || p->orient < 0 || p->orient > 1) return FP4_ERR_INVALID_ARG;
+    if (p->rht && (p->block != FP4_BLOCK_1x16 || p->orient != FP4_ORIENT_COLWISE)) return FP4_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return FP4_ERR_SHAPE;
+    const bool colwise = p->orient == FP4_ORIENT_COLWISE;
+    const int64_t R = colwise ? cols : rows, C = colwise ? rows : cols;
+    if (C % 16 != 0) return FP4_ERR_SHAPE;
+    if (p->block == FP4_BLOCK_16x16 && R % 16 != 0) return FP4_ERR_SHAPE;
+    if (colwise && cols % 8 != 0) return FP4_ERR_SHAPE;
+    return FP4_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp4_abi_version(void) { return 1; }
@@ -269,7 +292,7 @@ const char* fp4_status_string(fp4_status_t s) {
         case FP4_ERR_UNSUPPORTED: return "unsupported combination";
         case FP4_ERR_SHAPE: return "unsupported shape";
         case FP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
-        case FP4_ERR_STATE: return "held-amax state error (reserved)";
+        case FP4_ERR_STATE: return "given amax record not valid";
         case FP4_ERR_CUDA: return "CUDA runtime error";
         case FP4_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case FP4_ERR_WORKSPACE: return "workspace missing or too small";
@@ -293,7 +316,7 @@ fp4_status_t fp4_quantized_sizes(const fp4_quant_params_t* p, int64_t rows, int6
 size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols) {
     (void)rows;
     (void)cols;
-    if (p == nullptr || p->scale_fmt == FP4_SCALE_UE8M0) return 0;
+    if (p == nullptr || p->scale_fmt == FP4_SCALE_UE8M0 || p->tscale == FP4_TSCALE_GIVEN) return 0;
     return (size_t)kMaxAmaxPartials * sizeof(float);
 }
 
@@ -342,17 +365,54 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
         return FP4_ERR_UNSUPPORTED;
     if (rows % 128 != 0 || cols % 128 != 0) return FP4_ERR_SHAPE;
     const size_t half = (size_t)kMaxAmaxPartials * sizeof(float);
-    if (ws == nullptr || ws_bytes < 2 * half) return FP4_ERR_WORKSPACE;
+    const bool given = p_row->tscale == FP4_TSCALE_GIVEN;  // no amax pass: no workspace needed
+    if (!given && (ws == nullptr || ws_bytes < 2 * half)) return FP4_ERR_WORKSPACE;
     QuantJob jr, jc;
     fp4_status_t s = check_quantize(p_row, in_bf16, rows, cols, out_row, nullptr, state_row, counters_row, ws, half, jr);
     if (s != FP4_OK) return s;
     s = check_quantize(p_col, in_bf16, rows, cols, out_col, nullptr, state_col, counters_col,
-                       static_cast<char*>(ws) + half, half, jc);
+                       given ? nullptr : static_cast<char*>(ws) + half, half, jc);
     if (s != FP4_OK) return s;
     if (rows == 0 || cols == 0) return FP4_OK;
     jr.status = jc.status = device_status_ptr();
     if (jr.status == nullptr) return FP4_ERR_CUDA;
     return from_cuda(launch_quantize_dual(jr, jc, static_cast<cudaStream_t>(stream)));
+}
+
+
+fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+                             fp4_amax_state_t* out, void* ws, size_t ws_bytes, void* stream) {
+    fp4_status_t s = check_amax_params(p, rows, cols);
+    if (s != FP4_OK) return s;
+    if (out == nullptr || (rows > 0 && cols > 0 && in_bf16 == nullptr)) return FP4_ERR_INVALID_ARG;
+    if (ws == nullptr || ws_bytes < 2 * (size_t)kMaxAmaxPartials * sizeof(float)) return FP4_ERR_WORKSPACE;
+    if (!aligned16(ws) || !aligned16(in_bf16)) return FP4_ERR_ALIGNMENT;
+    int* status = device_status_ptr();
+    if (status == nullptr) return FP4_ERR_CUDA;
+    const bool rht = p->rht != 0;
+    return from_cuda(launch_tensor_amax(static_cast<const uint16_t*>(in_bf16), rows, cols, rht ? nullptr : out,
+                                        rht ? out : nullptr, rht, p->step, static_cast<float*>(ws), status,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
+                                  int64_t rows, int64_t cols, fp4_amax_state_t* out_row, fp4_amax_state_t* out_col,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    fp4_status_t s = check_amax_params(p_row, rows, cols);
+    if (s != FP4_OK) return s;
+    s = check_amax_params(p_col, rows, cols);
+    if (s != FP4_OK) return s;
+    if (p_row->orient != FP4_ORIENT_ROWWISE || p_col->orient != FP4_ORIENT_COLWISE) return FP4_ERR_INVALID_ARG;
+    if (p_row->step != p_col->step) return FP4_ERR_UNSUPPORTED;
+    if (out_row == nullptr || out_col == nullptr || (rows > 0 && cols > 0 && in_bf16 == nullptr))
+        return FP4_ERR_INVALID_ARG;
+    if (ws == nullptr || ws_bytes < 2 * (size_t)kMaxAmaxPartials * sizeof(float)) return FP4_ERR_WORKSPACE;
+    if (!aligned16(ws) || !aligned16(in_bf16)) return FP4_ERR_ALIGNMENT;
+    int* status = device_status_ptr();
+    if (status == nullptr) return FP4_ERR_CUDA;
+    return from_cuda(launch_tensor_amax(static_cast<const uint16_t*>(in_bf16), rows, cols, out_row, out_col,
+                                        p_col->rht != 0, p_row->step, static_cast<float*>(ws), status,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void* stream) {

@@ -48,8 +48,9 @@ struct QuantJob {
     int sr;             // stochastic rounding
     int colwise;
     int rht;
-    int held;           // held-amax tensor scale
+    int held;           // held-amax tensor scale (also set for a given amax)
     int refresh;        // held: this step refreshes the amax
+    int given;          // the amax is the state's, computed ahead (FP4_TSCALE_GIVEN)
     float target_T;
     uint32_t tensor_id;
     uint64_t seed;
@@ -82,6 +83,13 @@ cudaError_t launch_quantize(const QuantJob& job, cudaStream_t stream);
 cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStream_t stream);
 // Number of amax partials the amax pass of `job` writes (0: no amax pass).
 int amax_partials_needed(const QuantJob& job);
+// Tensor amax records ahead of quantization: the plain amax of the T x C BF16
+// tensor into st_plain and/or the post-RHT colwise amax (rht) or the plain one
+// (!rht) into st_col; null records are skipped. partials: 2 * kMaxAmaxPartials
+// floats. status: the device status word (bounded waits).
+cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, fp4_amax_state_t* st_plain,
+                               fp4_amax_state_t* st_col, bool rht, uint64_t step, float* partials, int* status,
+                               cudaStream_t stream);
 
 struct DequantJob {
     const uint8_t* codes;

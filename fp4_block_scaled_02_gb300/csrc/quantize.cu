@@ -44,6 +44,7 @@ struct QParams {
     const float* partials;
     int npartials;
     int held, refresh;
+    int given;    // the tensor amax is the state's (computed ahead by fp4_tensor_amax): no pass, no refresh
     int count_t;  // 16x16 with two outputs: the counters follow the transposed output
     float target_T;
     uint32_t tensor_id, step_lo, key0, key1;
@@ -71,7 +72,8 @@ __device__ float cta_max(float v) {
 // Tensor scale of this call (App. B.1; held amax per the UE5M3 paper), computed
 // redundantly by every CTA from the amax partials or the held state. CTA 0
 // publishes s_dec,G and, on refresh steps, the new held state. Returns false
-// (uniformly over the CTA) when a held state is needed but invalid.
+// (uniformly over the CTA) when a given amax is not valid (the status word then
+// holds FP4_ERR_STATE and nothing is written).
 __device__ bool cta_tensor_scale(const QParams& q, float& s_enc, float& s_dec) {
     __shared__ float s_amax;
     __shared__ int s_valid;
@@ -82,6 +84,10 @@ __device__ bool cta_tensor_scale(const QParams& q, float& s_enc, float& s_dec) {
         s_amax = s_valid ? q.state->amax_held : 0.0f;
     }
     __syncthreads();
+    if (q.given && s_valid == 0) {
+        if (threadIdx.x == 0) record_status(q.status, kStatusState);
+        return false;
+    }
     const bool use_held = s_valid != 0;
     if (!use_held) {
         float m = 0.0f;
@@ -967,7 +973,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         // rowwise: blocks (r, b) and (r + 32, b) of the tile's 64 x 8 blocks
         const int64_t code_row_tile = 8 * t0 * nb_row + (c0 >> 1);
         const int64_t sc_row_tile = 512 * ((t0 >> 7) * (nb_row >> 2) + (c0 >> 6)) + ((t0 & 64) >> 3);
-#pragma unroll
+        // kept rolled: with stochastic rounding the unrolled body's code size
+        // costs more in instruction fetch than the loop saves (measured)
+#pragma unroll 1
         for (int i = 0; i < 2; ++i) {
             const int r = r_row + 32 * i;
             const uint4 a = *reinterpret_cast<const uint4*>(&tile[r * kDualTC + 16 * b_row]);
@@ -1030,6 +1038,133 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     flush_counters(qr.counters, cr.esat, cr.eunder, cr.ssat, cr.sunder);
     flush_counters(qc.counters, cc.esat, cc.eunder, cc.ssat, cc.sunder);
+}
+
+// Tensor amax ahead of quantization (fp4_tensor_amax): the plain amax and/or
+// the post-RHT colwise amax of a T x C tensor (T % 64 == 0, C % 128 == 0), one
+// read, in 128-thread CTAs with one 16 KB TMA tile ring each (49 KB of shared
+// memory, few registers), one CTA per SM. Sized so a CTA fits on an SM beside
+// two conversion-pass CTAs of the dual quantizer: run on a second stream, the
+// amax of one tensor overlaps the (issue-bound) conversion of another.
+constexpr int kAmaxTileThreads = 128;
+template <bool PLAIN, bool RHT>
+__global__ void __launch_bounds__(kAmaxTileThreads)
+    amax_tile_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t T, int64_t C, float* __restrict__ part_plain,
+                     float* __restrict__ part_rht, int* status) {
+    pdl_begin();
+    extern __shared__ uint8_t amax_smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(amax_smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full_bar[kDualStages];
+    __shared__ float red[2][kAmaxTileThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid == 0) {
+        for (int k = 0; k < kDualStages; ++k) tc::mbar_init(tc::smem_u32(&full_bar[k]), 1);
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
+    const int64_t tiles_c = C / kDualTC, ntiles = (T / kDualTT) * tiles_c;
+    auto issue = [&](int64_t t, int s) {
+        const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
+        const uint32_t bar = tc::smem_u32(&full_bar[s]);
+        tc::mbar_arrive_expect_tx(bar, kDualTileBytes);
+        tc::tma_load_2d(tc::smem_u32(ring + s * kDualTileBytes), &tmap_x, (int32_t)c0, (int32_t)t0, bar);
+    };
+    if (tid == 0) {
+        tc::prefetch_tmap(&tmap_x);
+        for (int k = 0; k < kDualStages; ++k) {
+            const int64_t tk = blockIdx.x + (int64_t)k * gridDim.x;
+            if (tk < ntiles) issue(tk, k);
+        }
+    }
+    uint32_t mp = 0u;   // max |x| as BF16 bit pairs
+    float mr = 0.0f;    // max |RHT x| (times 4: the 1/4 is applied once at the end)
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = (int)(it % kDualStages);
+        const bool ok = tc::mbar_wait(tc::smem_u32(&full_bar[s]), (it / kDualStages) & 1u, status);
+        const uint8_t* tile = ring + s * kDualTileBytes;
+        if (PLAIN) {
+            // 64 x 128 BF16 = 1024 16-byte chunks, eight per thread
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 a = *reinterpret_cast<const uint4*>(tile + 16 * (tid + kAmaxTileThreads * i));
+                mp = __vmaxu2(mp, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                           __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+            }
+        }
+        if (RHT) {
+            // 4 token blocks x 64 channel pairs; a thread takes two of them
+#pragma unroll 1
+            for (int u = 0; u < 2; ++u) {
+                const int unit = tid + kAmaxTileThreads * u, cp = unit & 63, jb = unit >> 6;
+                f2 pv[16];
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + (16 * jb + tt) * (kDualTC * 2) + 4 * cp);
+                    pv[tt] = f2_pack(bf16_lo(w), bf16_hi(w));
+                }
+                wht16x2(pv);
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    float a, b;
+                    f2_unpack(pv[tt], a, b);
+                    mr = fmaxf(mr, fmaxf(fabsf(a), fabsf(b)));
+                }
+            }
+        }
+        if (!__syncthreads_and(ok)) break;
+        if (tid == 0) {
+            const int64_t tn = t + (int64_t)kDualStages * gridDim.x;
+            if (tn < ntiles) issue(tn, s);
+        }
+    }
+    float vp = __uint_as_float(max(mp & 0xFFFFu, mp >> 16) << 16), vr = __fmul_rn(mr, 0.25f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        vp = fmaxf(vp, __shfl_xor_sync(0xFFFFFFFFu, vp, o));
+        vr = fmaxf(vr, __shfl_xor_sync(0xFFFFFFFFu, vr, o));
+    }
+    if (lane == 0) {
+        red[0][tid >> 5] = vp;
+        red[1][tid >> 5] = vr;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float a = 0.0f, b = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kAmaxTileThreads / 32; ++w) {
+            a = fmaxf(a, red[0][w]);
+            b = fmaxf(b, red[1][w]);
+        }
+        if (PLAIN) part_plain[blockIdx.x] = a;
+        if (RHT) part_rht[blockIdx.x] = b;
+    }
+}
+
+// Reduce amax partials into tensor-amax records (one CTA); a null record is skipped.
+__global__ void __launch_bounds__(kThreads) amax_finalize_kernel(const float* __restrict__ part_a, fp4_amax_state_t* st_a,
+                                                                 const float* __restrict__ part_b, fp4_amax_state_t* st_b,
+                                                                 int n, uint64_t step) {
+    pdl_begin();
+    float a = 0.0f, b = 0.0f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        if (st_a) a = fmaxf(a, part_a[i]);
+        if (st_b) b = fmaxf(b, part_b[i]);
+    }
+    a = cta_max(a);
+    b = cta_max(b);
+    if (threadIdx.x == 0) {
+        if (st_a) {
+            st_a->amax_held = a;
+            st_a->valid = 1;
+            st_a->last_refresh_step = step;
+        }
+        if (st_b) {
+            st_b->amax_held = b;
+            st_b->valid = 1;
+            st_b->last_refresh_step = step;
+        }
+    }
 }
 
 int grid_for(int64_t threads_wanted, int per_sm) {
@@ -1138,6 +1273,7 @@ QParams make_params(const QuantJob& j) {
     q.scales_t = j.scales_t;
     q.s_dec_t = j.s_dec_t;
     q.state = j.state;
+    q.given = j.given;
     q.counters = j.counters;
     q.partials = j.partials;
     q.held = j.held;
@@ -1159,7 +1295,7 @@ QParams make_params(const QuantJob& j) {
 }  // namespace
 
 int amax_partials_needed(const QuantJob& j) {
-    if (j.scale_fmt == kFmtUE8M0) return 0;
+    if (j.scale_fmt == kFmtUE8M0 || j.given) return 0;
     if (j.rows == 0 || j.cols == 0) return 0;
     return amax_grid(j);  // held non-refresh steps too: the state may not be valid yet
 }
@@ -1217,10 +1353,63 @@ int dual_amax_grid(const QuantJob& jc) {
     return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
 }
 
+cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, fp4_amax_state_t* st_plain,
+                               fp4_amax_state_t* st_col, bool rht, uint64_t step, float* partials, int* status,
+                               cudaStream_t st) {
+    if (T == 0 || C == 0) {
+        // an empty tensor has amax 0
+        (void)launch_pdl(amax_finalize_kernel, 1, kThreads, 0, st, partials, st_plain, partials + kMaxAmaxPartials,
+                         st_col, 0, step);
+        return cudaGetLastError();
+    }
+    float* part_plain = partials;
+    float* part_col = partials + kMaxAmaxPartials;
+    const bool plain = st_plain != nullptr || (st_col != nullptr && !rht);
+    const bool post_rht = st_col != nullptr && rht;
+    int np;
+    CUtensorMap tmap_x;
+    if (T % kDualTT == 0 && C % kDualTC == 0 && make_tmap_bf16_2d(&tmap_x, in, T, C, kDualTT, kDualTC)) {
+        const int64_t ntiles = (T / kDualTT) * (C / kDualTC);
+        np = (int)(ntiles < num_sms() ? ntiles : num_sms());
+        const int smem = kDualStages * kDualTileBytes + 1024;
+#define FP4_AMAX_TILE(P, R)                                                                                     \
+    do {                                                                                                        \
+        auto kern = amax_tile_kernel<P, R>;                                                                     \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);          \
+        if (e != cudaSuccess) return e;                                                                         \
+        (void)launch_pdl(kern, np, kAmaxTileThreads, smem, st, tmap_x, T, C, part_plain, part_col, status);     \
+    } while (0)
+        if (plain && post_rht) FP4_AMAX_TILE(true, true);
+        else if (plain) FP4_AMAX_TILE(true, false);
+        else FP4_AMAX_TILE(false, true);
+#undef FP4_AMAX_TILE
+    } else {
+        // other shapes: the quantizer's own amax passes
+        QuantJob j{};
+        j.rows = T;
+        j.cols = C;
+        j.colwise = post_rht;
+        j.rht = post_rht;
+        np = amax_grid(j);
+        if (plain)
+            (void)launch_pdl(amax_plain_kernel, np, kThreads, 0, st, reinterpret_cast<const uint4*>(in), T * C / 8,
+                             part_plain, (const fp4_amax_state_t*)nullptr);
+        if (post_rht)
+            (void)launch_pdl(amax_rht_cols_kernel, np, kThreads, 0, st, in, T, C, part_col,
+                             (const fp4_amax_state_t*)nullptr);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // a colwise record without RHT takes the plain amax
+    (void)launch_pdl(amax_finalize_kernel, 1, kThreads, 0, st, part_plain, st_plain,
+                     post_rht ? part_col : part_plain, st_col, np, step);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStream_t st) {
     if (jr.rows == 0 || jr.cols == 0) return cudaSuccess;
     QParams qr = make_params(jr), qc = make_params(jc);
-    {
+    if (!jr.given) {
         // held non-refresh steps: the pass runs only while a held state is not valid yet
         const bool held_step = jr.held && !jr.refresh;
         const fp4_amax_state_t* skip_r = held_step ? jr.state : nullptr;

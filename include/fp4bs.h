@@ -44,7 +44,7 @@ typedef enum {
     FP4_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination */
     FP4_ERR_SHAPE = 3,         /* dimension not a multiple the path needs */
     FP4_ERR_ALIGNMENT = 4,     /* pointer not 16-byte aligned */
-    FP4_ERR_STATE = 5,         /* reserved (an invalid held state now triggers a refresh) */
+    FP4_ERR_STATE = 5,         /* a given amax record (FP4_TSCALE_GIVEN) was not valid (device status) */
     FP4_ERR_CUDA = 6,          /* a CUDA runtime call failed */
     FP4_ERR_DEVICE_TIMEOUT = 7,/* a bounded device-side wait gave up */
     FP4_ERR_WORKSPACE = 8      /* workspace missing or too small */
@@ -66,7 +66,7 @@ typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_round_t;
 /* Tensor scale: per-call amax (App. B.1) or held amax refreshed when
  * step % refresh_every == 0 or when the held state is not valid yet (UE5M3
  * page: refresh every 50 steps); other steps use the held amax. */
-typedef enum { FP4_TSCALE_CURRENT = 0, FP4_TSCALE_HELD = 1 } fp4_tscale_t;
+typedef enum { FP4_TSCALE_CURRENT = 0, FP4_TSCALE_HELD = 1, FP4_TSCALE_GIVEN = 2 } fp4_tscale_t;
 
 /* ROWWISE: the operand is the input itself (blocks run along its columns).
  * COLWISE: the operand is the input's transpose (blocks run along the input's
@@ -139,7 +139,11 @@ size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t co
  *              with the same codes and scales transposed (section 4.3); else NULL.
  *   state    : held-amax record (FP4_TSCALE_HELD), else NULL. Refresh steps, and
  *              steps that find it not valid yet, compute the amax and write it;
- *              other steps use it (their amax pass returns at once).
+ *              other steps use it (their amax pass returns at once). With
+ *              FP4_TSCALE_GIVEN: the record fp4_tensor_amax wrote, read and not
+ *              changed (no amax pass, ws may be NULL); a record that is not
+ *              valid when the kernel runs writes nothing and leaves
+ *              FP4_ERR_STATE in the device status word.
  *   counters : NULL or 4 device uint64: elem_sat, elem_underflow, scale_sat,
  *              scale_underflow; the call ADDS its counts (the caller zeroes).
  *   ws       : device workspace of fp4_workspace_bytes() bytes (any content).
@@ -180,6 +184,28 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
 fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
                                   const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                                   uint64_t* counters, void* stream);
+
+/* Tensor amax ahead of quantization (App. B.1: the amax that current scaling
+ * takes in its first memory pass), as a separate call so that it can run on
+ * another stream while other work proceeds. Computes the amax of the operand
+ * that p describes (max |x|, or max |RHT x| along tokens for a colwise operand
+ * with rht) and writes *out = {amax, valid = 1, last_refresh_step = p->step}
+ * when the stream reaches it. A later fp4_quantize with tscale
+ * FP4_TSCALE_GIVEN and state = out then quantizes exactly as FP4_TSCALE_CURRENT
+ * would (same s_enc,G), without its own amax pass. Only p's scale_fmt (E4M3 or
+ * UE5M3), block, orient, rht and step are read; shapes follow the quantize call
+ * with the same parameters. in: device BF16, 16-byte aligned. ws: device,
+ * 16-byte aligned, at least 2 * 2048 * 4 bytes, not shared with calls in flight.
+ * For T % 64 == 0 and C % 128 == 0 the pass runs in one 128-thread CTA per SM
+ * that fits beside the dual quantizer's conversion pass; other shapes use the
+ * quantizer's own amax kernels. fp4_tensor_amax_dual writes the rowwise
+ * operand's amax (out_row) and the colwise one's (out_col, post-RHT when
+ * p_col->rht) from one read. */
+fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+                             fp4_amax_state_t* out, void* ws, size_t ws_bytes, void* stream);
+fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
+                                  int64_t rows, int64_t cols, fp4_amax_state_t* out_row, fp4_amax_state_t* out_col,
+                                  void* ws, size_t ws_bytes, void* stream);
 
 /* Decode an operand back to real values, x = e2m1 * s_hat * s_dec,G computed as
  * RN(RN(e2m1 * s_hat) * s_dec,G) in FP32 (section A3; App. B.3), written as

@@ -337,3 +337,128 @@ def test_dual_quantize_equals_two_separate_calls_and_oracle(case):
         assert torch.equal(states[0].buf, states[2].buf) and torch.equal(states[1].buf, states[3].buf)
         assert_quant_equal(dr, oracle_quantize(cr, bits, state=ostates[0] if held else None), TC, cnt[0])
         assert_quant_equal(dc, oracle_quantize(cc, bits, state=ostates[1] if held else None), TC, cnt[1])
+
+
+# Tensor amax ahead of quantization (fp4_tensor_amax) and the given-amax mode:
+# the amax equals the oracle's tensor amax of the same operand, and quantizing
+# with it reproduces current scaling byte for byte. Tile shapes (T % 64,
+# C % 128) take the 128-thread tile pass, the others the quantizer's own kernels.
+AMAX_SHAPES = [(256, 512), (192, 384), (48, 80), (128, 208)]
+
+
+@pytest.mark.parametrize("shape", AMAX_SHAPES)
+def test_tensor_amax_matches_the_oracle(shape):
+    bits = random_bf16(26, shape, "log_normal_1e-4_2")
+    x = to_gpu_bf16(bits)
+    ws = torch.zeros(fb.AMAX_WS_BYTES // 4, dtype=torch.float32, device="cuda")
+    R, C = shape
+    cases = [(fb.QuantConfig(step=5), False, False)]
+    if R % 16 == 0 and C % 8 == 0:
+        cases += [(fb.QuantConfig(orient=fb.FP4_ORIENT_COLWISE, rht=True, seed=3, step=5), True, True),
+                  (fb.QuantConfig(orient=fb.FP4_ORIENT_COLWISE, step=5), True, False)]
+    if R % 16 == 0 and C % 16 == 0:
+        cases += [(fb.QuantConfig(block=fb.FP4_BLOCK_16x16, step=5), False, False)]
+    for cfg, colwise, rht in cases:
+        st = fb.AmaxState()
+        fb.fp4_tensor_amax(cfg, x, st, ws)
+        assert fb.fp4_device_status() == 0
+        ref = oracle.tensor_amax(bits, colwise=colwise, rht=rht, seed=cfg.seed)
+        assert np.float32(st.amax) == np.float32(ref), (cfg, st.amax, ref)
+        assert st.valid == 1 and st.last_refresh_step == 5
+    if R % 16 == 0 and C % 16 == 0:
+        sr_, sc_ = fb.AmaxState(), fb.AmaxState()
+        fb.fp4_tensor_amax_dual(fb.QuantConfig(step=2), fb.QuantConfig(orient=fb.FP4_ORIENT_COLWISE, rht=True,
+                                                                       seed=3, step=2), x, sr_, sc_, ws)
+        assert fb.fp4_device_status() == 0
+        assert np.float32(sr_.amax) == np.float32(oracle.tensor_amax(bits))
+        assert np.float32(sc_.amax) == np.float32(oracle.tensor_amax(bits, colwise=True, rht=True, seed=3))
+
+
+GIVEN_CASES = [
+    # (shape, fmt, round, target_T)
+    ((256, 512), fb.FP4_SCALE_E4M3, fb.FP4_ROUND_SR, 448.0),
+    ((384, 256), fb.FP4_SCALE_UE5M3, fb.FP4_ROUND_RNE, 2048.0),
+]
+
+
+@pytest.mark.parametrize("case", GIVEN_CASES)
+def test_given_amax_equals_current_scaling(case):
+    shape, fmt, rnd, T = case
+    bits = random_bf16(27, shape, "student_t4")
+    x = to_gpu_bf16(bits)
+    R, C = shape
+    ws = torch.zeros(fb.AMAX_WS_BYTES // 4, dtype=torch.float32, device="cuda")
+    kw = dict(scale_fmt=fmt, round=rnd, target_T=T, seed=4, step=9)
+    cr = fb.QuantConfig(tensor_id=3, **kw)
+    cc = fb.QuantConfig(tensor_id=4, orient=fb.FP4_ORIENT_COLWISE, rht=True, **kw)
+    cw = fb.QuantConfig(tensor_id=2, block=fb.FP4_BLOCK_16x16, emit_transpose=True, scale_fmt=fmt, target_T=T)
+    giv = dict(tscale=fb.FP4_TSCALE_GIVEN)
+    # dual: current vs given
+    a_r, a_c, g_r, g_c = (fb.QTensor.empty(R, C, fmt), fb.QTensor.empty(C, R, fmt),
+                          fb.QTensor.empty(R, C, fmt), fb.QTensor.empty(C, R, fmt))
+    cnt = torch.zeros((4, 4), dtype=torch.int64, device="cuda")
+    fb.fp4_quantize_dual(cr, cc, x, a_r, a_c, None, None, cnt[0], cnt[1], ws=torch.zeros(8192, device="cuda"))
+    st_r, st_c = fb.AmaxState(), fb.AmaxState()
+    fb.fp4_tensor_amax_dual(cr, cc, x, st_r, st_c, ws)
+    fb.fp4_quantize_dual(fb.QuantConfig(tensor_id=3, **kw, **giv),
+                         fb.QuantConfig(tensor_id=4, orient=fb.FP4_ORIENT_COLWISE, rht=True, **kw, **giv),
+                         x, g_r, g_c, st_r, st_c, cnt[2], cnt[3])
+    assert fb.fp4_device_status() == 0
+    for a, g in ((a_r, g_r), (a_c, g_c)):
+        assert torch.equal(a.codes, g.codes) and torch.equal(a.scales, g.scales)
+        assert a.s_dec[0:1].view(torch.int32).item() == g.s_dec[0:1].view(torch.int32).item()
+    assert torch.equal(cnt[0], cnt[2]) and torch.equal(cnt[1], cnt[3])
+    assert st_r.valid == 1 and st_c.valid == 1  # read, not changed
+    # 16x16 with both outputs: current vs given
+    w1, w1t, w2, w2t = (fb.QTensor.empty(R, C, fmt), fb.QTensor.empty(C, R, fmt),
+                        fb.QTensor.empty(R, C, fmt), fb.QTensor.empty(C, R, fmt))
+    fb.fp4_quantize(cw, x, w1, w1t, ws=new_ws())
+    st_w = fb.AmaxState()
+    fb.fp4_tensor_amax(cw, x, st_w, ws)
+    cwg = fb.QuantConfig(tensor_id=2, block=fb.FP4_BLOCK_16x16, emit_transpose=True, scale_fmt=fmt, target_T=T, **giv)
+    fb.fp4_quantize(cwg, x, w2, w2t, state=st_w)
+    assert fb.fp4_device_status() == 0
+    for a, g in ((w1, w2), (w1t, w2t)):
+        assert torch.equal(a.codes, g.codes) and torch.equal(a.scales, g.scales)
+    assert_quant_equal(g_r, oracle_quantize(cr, bits), TC, cnt[2])
+
+
+def test_given_amax_not_valid_leaves_a_state_error():
+    x = to_gpu_bf16(random_bf16(28, (256, 256), "normal"))
+    out = fb.QTensor.empty(256, 256)
+    out.codes.fill_(0xAA)
+    st = fb.AmaxState()  # zeroed: not valid
+    fb.fp4_quantize(fb.QuantConfig(tscale=fb.FP4_TSCALE_GIVEN), x, out, state=st)
+    assert fb.fp4_device_status() == fb._lib.FP4_ERR_STATE
+    assert int((out.codes != 0xAA).sum().item()) == 0  # nothing written
+    assert fb.fp4_device_status() == 0  # the status word was cleared by the read
+
+
+def test_linear_with_amax_on_a_side_stream_equals_the_plain_schedule():
+    """Fp4Linear computing W's and dY's amaxes on a second stream (given-amax
+    quantization) leaves the same quantized operands, counters and outputs."""
+    T, K, N = 512, 256, 512
+    xb = random_bf16(29, (T, K), "student_t4")
+    wb = random_bf16(30, (N, K), "weight")
+    dyb = random_bf16(31, (T, N), "log_normal_1e-4_2")
+    x, w, dy = to_gpu_bf16(xb), to_gpu_bf16(wb), to_gpu_bf16(dyb)
+    outs = []
+    for overlap in (False, True):
+        L = fb.Fp4Linear(T, K, N, rht=True, seed=2, overlap_amax=overlap)
+        assert (L.side is not None) == overlap
+        y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        dx = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+        dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+        for step in (0, 1):
+            L.counters.zero_()
+            L.step(x, w, dy, y, dx, dw, step=step)
+        torch.cuda.synchronize()
+        assert fb.fp4_device_status() == 0
+        outs.append((L, y, dx, dw))
+    (a, ya, dxa, dwa), (b, yb, dxb, dwb) = outs
+    for k in a.bufs:
+        assert torch.equal(a.bufs[k].codes, b.bufs[k].codes), k
+        assert torch.equal(a.bufs[k].scales, b.bufs[k].scales), k
+        assert torch.equal(a.bufs[k].s_dec[:1], b.bufs[k].s_dec[:1]), k  # element 0 is the tensor scale
+    assert torch.equal(a.counters, b.counters)
+    assert torch.equal(ya, yb) and torch.equal(dxa, dxb) and torch.equal(dwa, dwb)
