@@ -237,6 +237,7 @@ def run_gpu(args, workload):
     # per linear: 3 x (amax + quantize) + 3 GEMMs; with the amaxes of W and dY on a
     # side stream, those two amax launches become two (tile pass + finalize) each
     launches_per_step = sum(11 if L.side is not None else 9 for _, L, _, _ in layers)
+    q_launches = launches_per_step - 3 * len(layers)
 
     def step(ev=None):
         for lin, L, di, o in layers:
@@ -330,7 +331,8 @@ def run_gpu(args, workload):
                  "kernel": "gemm_nvfp4_kernel (6 launches per step)"}
     quant_roof = {"bound": "hbm", "achieved": quant_gbs, "peak": hbm_peak, "unit": "GB/s",
                   "frac": quant_gbs / hbm_peak, "traffic": traffic.get("quantize"),
-                  "peak_source": f"{src} hbm_gbs", "kernel": "amax + quantize kernels (12 launches per step)"}
+                  "peak_source": f"{src} hbm_gbs",
+                  "kernel": f"amax + quantize kernels ({q_launches} launches per step)"}
     dominant, other = (gemm_roof, quant_roof) if g_ms >= q_ms else (quant_roof, gemm_roof)
     cpu = cpu_baseline_entry(workload, args.ref_tokens, args.ref_feats) if not args.no_cpu_baseline else None
     lin_desc = [[l.k_in, l.n_out] for l in workload.linears]

@@ -11,16 +11,20 @@
 // tensor scale) with tcgen05.mma kind::mxf4 and alpha = 1.
 //
 // Design (one CTA per SM, persistent over output tiles of 128 x BN):
-//   warp 0      : TMA producer -- A/B code tiles (128-byte swizzled rows of 256
-//                 FP4 values) and the tiles' scale chunks (1-D bulk copies) into
+//   warp 0      : TMA producer -- the tiles' scale chunks (1-D bulk copies,
+//                 issued first, on a barrier of their own so the scale copies
+//                 into TMEM run while the operands are still in flight) and the
+//                 A/B code tiles (128-byte swizzled rows of 256 FP4 values) into
 //                 a STAGES-deep shared-memory ring guarded by mbarriers;
 //   warp 1      : allocates tensor memory; one lane issues, per stage, four
 //                 tcgen05.mma kind::mxf4nvf4 (M = 128, N = BN, K = 64 each) and
 //                 commits the stage back to the producer;
 //   warp 2      : one lane copies each stage's scale chunks into tensor memory
-//                 (tcgen05.cp.32x128b.warpx4) and commits them to a per-stage
-//                 barrier (measured on GB300: with the copies on the MMA thread
-//                 as well, that thread was the bottleneck);
+//                 (tcgen05.cp.32x128b.warpx4) as soon as they land and commits
+//                 them to a per-stage barrier (measured on GB300: with the copies
+//                 on the MMA thread as well, that thread was the bottleneck; with
+//                 the chunks on the operands' barrier the copy latency added to
+//                 every stage the MMA had to wait for, 2-3 % on the 1.2B shapes);
 //   warps 3..   : epilogue -- BN / 32 warps; warp w reads TMEM lane quadrant
 //                 w % 4 and 128 of the BN accumulator columns (tcgen05.ld),
 //                 scales by alpha and stores BF16 / FP32.
@@ -129,7 +133,7 @@ struct NvCfg {
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
     static_assert(OFF_EPI % 1024 == 0, "staging boxes must be 1024-byte aligned");
     static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BOX_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 2;
+    static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -156,6 +160,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t drain_bar = sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + 2 * Cfg::NUM_ACC);
     auto sf_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (2 * Cfg::STAGES + 2 * Cfg::NUM_ACC + 1 + s); };
     const uint32_t sf_drain_bar = sb + Cfg::OFF_BAR + 8u * (3 * Cfg::STAGES + 2 * Cfg::NUM_ACC + 1);
+    // scale chunks of a stage land on their own barrier, ahead of the operand tiles
+    auto sff_bar = [&](int s) { return sb + Cfg::OFF_BAR + 8u * (3 * Cfg::STAGES + 2 * Cfg::NUM_ACC + 2 + s); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
 
     const int64_t num_m = p.M / Cfg::BM, num_n = p.N / Cfg::BN, tiles = num_m * num_n;
@@ -173,6 +179,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         tc::mbar_init(drain_bar, 1);
         for (int s = 0; s < Cfg::STAGES; ++s) tc::mbar_init(sf_bar(s), 1);
+        for (int s = 0; s < Cfg::STAGES; ++s) tc::mbar_init(sff_bar(s), 1);
         tc::mbar_init(sf_drain_bar, 1);
         tc::mbar_init_fence();
         tc::prefetch_tmap(&tmap_a);
@@ -204,18 +211,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         ok = false;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(full_bar(s), Cfg::TX);
-                    tc::tma_load_2d(sb + Cfg::OFF_A + s * Cfg::A_BYTES, &tmap_a, kb * Cfg::ROW_BYTES,
-                                    (int32_t)(mb * Cfg::BM), full_bar(s));
-                    tc::tma_load_2d(sb + Cfg::OFF_B + s * Cfg::B_BYTES, &tmap_b, kb * Cfg::ROW_BYTES,
-                                    (int32_t)(nb * Cfg::BN), full_bar(s));
+                    tc::mbar_arrive_expect_tx(sff_bar(s), Cfg::SFA_BYTES + Cfg::SFB_BYTES);
                     tc::bulk_load(sb + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
-                                  p.a_scales + 512 * (mb * chunks_k + Cfg::SF_CHUNKS * kb), Cfg::SFA_BYTES, full_bar(s));
+                                  p.a_scales + 512 * (mb * chunks_k + Cfg::SF_CHUNKS * kb), Cfg::SFA_BYTES, sff_bar(s));
 #pragma unroll
                     for (int h = 0; h < Cfg::BN / 128; ++h)
                         tc::bulk_load(sb + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + 512 * Cfg::SF_CHUNKS * h,
                                       p.b_scales + 512 * ((nb * (Cfg::BN / 128) + h) * chunks_k + Cfg::SF_CHUNKS * kb),
-                                      512 * Cfg::SF_CHUNKS, full_bar(s));
+                                      512 * Cfg::SF_CHUNKS, sff_bar(s));
+                    tc::mbar_arrive_expect_tx(full_bar(s), Cfg::A_BYTES + Cfg::B_BYTES);
+                    tc::tma_load_2d(sb + Cfg::OFF_A + s * Cfg::A_BYTES, &tmap_a, kb * Cfg::ROW_BYTES,
+                                    (int32_t)(mb * Cfg::BM), full_bar(s));
+                    tc::tma_load_2d(sb + Cfg::OFF_B + s * Cfg::B_BYTES, &tmap_b, kb * Cfg::ROW_BYTES,
+                                    (int32_t)(nb * Cfg::BN), full_bar(s));
                 }
             }
         }
@@ -242,9 +250,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     const int s = (int)(it % Cfg::STAGES);
                     const uint32_t ph = (it / Cfg::STAGES) & 1u;
-                    // the scale warp's barrier completes after the stage's data
-                    // landed (it waited on the full barrier) and its scale
-                    // copies into tensor memory finished
+                    // the operand tiles landed (full barrier) and the stage's
+                    // scale copies into tensor memory finished (scale warp's barrier)
                     if (!tc::mbar_wait(full_bar(s), ph, p.status) || !tc::mbar_wait(sf_bar(s), ph, p.status)) {
                         ok = false;
                         break;
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t ph = (it / Cfg::STAGES) & 1u;
                     // a stage's scale columns are reused only after the producer
                     // refilled the stage, i.e. after the MMAs that read them retired
-                    if (!tc::mbar_wait(full_bar(s), ph, p.status)) {
+                    if (!tc::mbar_wait(sff_bar(s), ph, p.status)) {
                         ok = false;
                         break;
                     }

@@ -1043,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Tensor amax ahead of quantization (fp4_tensor_amax): the plain amax and/or
 // the post-RHT colwise amax of a T x C tensor (T % 64 == 0, C % 128 == 0), one
 // read, in 128-thread CTAs with one 16 KB TMA tile ring each (49 KB of shared
-// memory, few registers), one CTA per SM. Sized so a CTA fits on an SM beside
+// memory, few registers), two CTAs per SM. Sized so a CTA fits on an SM beside
 // two conversion-pass CTAs of the dual quantizer: run on a second stream, the
 // amax of one tensor overlaps the (issue-bound) conversion of another.
 constexpr int kAmaxTileThreads = 128;
@@ -1369,8 +1369,10 @@ cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, fp4_ama
     int np;
     CUtensorMap tmap_x;
     if (T % kDualTT == 0 && C % kDualTC == 0 && make_tmap_bf16_2d(&tmap_x, in, T, C, kDualTT, kDualTC)) {
-        const int64_t ntiles = (T / kDualTT) * (C / kDualTC);
-        np = (int)(ntiles < num_sms() ? ntiles : num_sms());
+        // two CTAs per SM when the pass runs alone; beside a conversion pass one fits
+        // and the other follows
+        const int64_t ntiles = (T / kDualTT) * (C / kDualTC), cap = 2 * (int64_t)num_sms();
+        np = (int)(ntiles < cap ? ntiles : cap);
         const int smem = kDualStages * kDualTileBytes + 1024;
 #define FP4_AMAX_TILE(P, R)                                                                                     \
     do {                                                                                                        \

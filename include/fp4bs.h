@@ -196,9 +196,9 @@ fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf
  * UE5M3), block, orient, rht and step are read; shapes follow the quantize call
  * with the same parameters. in: device BF16, 16-byte aligned. ws: device,
  * 16-byte aligned, at least 2 * 2048 * 4 bytes, not shared with calls in flight.
- * For T % 64 == 0 and C % 128 == 0 the pass runs in one 128-thread CTA per SM
- * that fits beside the dual quantizer's conversion pass; other shapes use the
- * quantizer's own amax kernels. fp4_tensor_amax_dual writes the rowwise
+ * For T % 64 == 0 and C % 128 == 0 the pass runs in 128-thread CTAs (two per
+ * SM; one fits beside the dual quantizer's conversion pass); other shapes use
+ * the quantizer's own amax kernels. fp4_tensor_amax_dual writes the rowwise
  * operand's amax (out_row) and the colwise one's (out_col, post-RHT when
  * p_col->rht) from one read. */
 fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
