@@ -234,9 +234,9 @@ def run_gpu(args, workload):
     gemm_flops = sum(3 * 2.0 * lin.tokens * lin.k_in * lin.n_out for lin, *_ in layers)
     quant_bytes = sum(BYTES_TWO_OPERANDS * (lin.tokens * (lin.k_in + lin.n_out) + lin.n_out * lin.k_in)
                       for lin, *_ in layers)
-    # per linear: 3 x (amax + quantize) + 3 GEMMs; with the amaxes of W and dY on a
-    # side stream, those two amax launches become two (tile pass + finalize) each
-    launches_per_step = sum(11 if L.side is not None else 9 for _, L, _, _ in layers)
+    # per linear: 3 x (amax + quantize) + 3 GEMMs; with the amaxes on a side
+    # stream, each amax launch becomes two (tile pass + finalize)
+    launches_per_step = sum(12 if L.side is not None else 9 for _, L, _, _ in layers)
     q_launches = launches_per_step - 3 * len(layers)
 
     def step(ev=None):

@@ -243,10 +243,11 @@ class Fp4Linear:
     `ue5m3_native` is set, else the emulated one.
 
     With current scaling and `overlap_amax` set (and T, K, N multiples of 128),
-    the tensor amaxes of W and dY are computed on a second stream
-    (fp4_tensor_amax) while X is quantized on the caller's stream, and W and dY
-    are then quantized with those amaxes (FP4_TSCALE_GIVEN): the same bytes as
-    current scaling, with their amax passes off the critical path."""
+    the tensor amaxes of W, X and dY are computed on a second stream
+    (fp4_tensor_amax) while the caller's stream quantizes W, X and dY in turn,
+    each with its amax (FP4_TSCALE_GIVEN) as soon as that is ready: the same
+    bytes as current scaling, with the amax passes off the critical path except
+    W's (the smallest)."""
     tokens: int
     k_in: int
     n_out: int
@@ -279,10 +280,11 @@ class Fp4Linear:
         self.side = None
         if self.overlap_amax and not self.held and T % 128 == 0 and K % 128 == 0 and N % 128 == 0:
             self.side = torch.cuda.Stream(device=dev)
-            self.ws_side = torch.empty(AMAX_WS_BYTES // 4, dtype=torch.float32, device=dev)
+            # one workspace per amax call: calls in flight must not share one
+            self.ws_side = [torch.empty(AMAX_WS_BYTES // 4, dtype=torch.float32, device=dev) for _ in range(3)]
             self.given = [AmaxState(dev) for _ in range(5)]
             self.ev_inputs = torch.cuda.Event()
-            self.ev_amax = torch.cuda.Event()
+            self.ev_amax = [torch.cuda.Event() for _ in range(3)]
         self.gemm_ws = None
         if f == FP4_SCALE_UE5M3 and self.ue5m3_native:
             b = self.bufs
@@ -330,25 +332,36 @@ class Fp4Linear:
                          state=self.states[4], counters=c[4], ws=self.ws, stream=stream)
 
     def _quantize_all_overlapped(self, x, w, dy, step, stream):
+        # side stream: the tensor amaxes of W (smallest, first), X and dY; main
+        # stream: W, X and dY quantized with them as each becomes ready, so only
+        # W's amax pass is not hidden behind a conversion pass
         b, c, g, rht = self.bufs, self.counters, self.given, self.rht
         main = torch.cuda.current_stream() if stream is None else stream
+        side = self.side
         self.ev_inputs.record(main)
-        self.side.wait_event(self.ev_inputs)
+        side.wait_event(self.ev_inputs)
+        for t in (x, w, dy):
+            t.record_stream(side)  # read on the side stream: keep the allocator from reusing it early
         w_cfg = dict(block=FP4_BLOCK_16x16)
+        x_c = dict(orient=FP4_ORIENT_COLWISE, rht=rht)
         dy_r = dict(round=FP4_ROUND_SR)
         dy_c = dict(orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR)
-        w.record_stream(self.side)  # read on the side stream: keep the allocator from reusing it early
-        dy.record_stream(self.side)
-        fp4_tensor_amax(self._cfg(2, step, **w_cfg), w, g[2], self.ws_side, stream=self.side)
-        fp4_tensor_amax_dual(self._cfg(3, step, **dy_r), self._cfg(4, step, **dy_c), dy, g[3], g[4], self.ws_side,
-                             stream=self.side)
-        self.ev_amax.record(self.side)
-        fp4_quantize_dual(self._cfg(0, step), self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x,
-                          b["x"], b["xt"], None, None, c[0], c[1], ws=self.ws, stream=main)
-        main.wait_event(self.ev_amax)
         giv = dict(tscale=FP4_TSCALE_GIVEN)
+        fp4_tensor_amax(self._cfg(2, step, **w_cfg), w, g[2], self.ws_side[0], stream=side)
+        self.ev_amax[0].record(side)
+        fp4_tensor_amax_dual(self._cfg(0, step), self._cfg(1, step, **x_c), x, g[0], g[1], self.ws_side[1],
+                             stream=side)
+        self.ev_amax[1].record(side)
+        fp4_tensor_amax_dual(self._cfg(3, step, **dy_r), self._cfg(4, step, **dy_c), dy, g[3], g[4], self.ws_side[2],
+                             stream=side)
+        self.ev_amax[2].record(side)
+        main.wait_event(self.ev_amax[0])
         fp4_quantize(self._cfg(2, step, emit_transpose=True, **w_cfg, **giv), w, b["w"], b["wt"], state=g[2],
                      counters=c[2], stream=main)
+        main.wait_event(self.ev_amax[1])
+        fp4_quantize_dual(self._cfg(0, step, **giv), self._cfg(1, step, **x_c, **giv), x, b["x"], b["xt"], g[0], g[1],
+                          c[0], c[1], stream=main)
+        main.wait_event(self.ev_amax[2])
         fp4_quantize_dual(self._cfg(3, step, **dy_r, **giv), self._cfg(4, step, **dy_c, **giv), dy, b["dy"], b["dyt"],
                           g[3], g[4], c[3], c[4], stream=main)
 
