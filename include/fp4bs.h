@@ -11,8 +11,10 @@
  *     (App. B.3, section 4.4), optional 16x16 random Hadamard transform on the
  *     Wgrad operands (section 4.2, App. C), 2D 16x16 weight scaling (4.3);
  *   - the three block-scaled FP4 GEMMs of a linear layer (section 4.1, Fig. 5:
- *     Fprop, Dgrad, Wgrad) on tcgen05 tensor cores (App. B.3), and a
- *     software-emulated path for UE5M3 scales, which have no hardware support.
+ *     Fprop, Dgrad, Wgrad) on tcgen05 tensor cores (App. B.3) for NVFP4 and
+ *     MXFP4 operands (section A3), and for UE5M3 scales, which no tensor core
+ *     reads, a software-emulated path and an exact rebias onto E4M3 scales
+ *     that runs on the native MMA (fp4_gemm_ws).
  *
  * Conventions for every entry point:
  *   - Ownership: the caller allocates and frees every buffer (inputs, codes,
@@ -23,8 +25,13 @@
  *     passed as void*; NULL = legacy default stream) and the call returns before
  *     it completes. Argument checks run synchronously on the host first: a call
  *     that fails them returns an error and enqueues nothing.
- *   - Device-side errors (a bounded wait that timed out) are recorded in a
- *     per-device status word read by fp4_device_status().
+ *   - Device-side errors (a bounded wait that timed out, a given amax record
+ *     that is not valid) are recorded in a per-device status word read by
+ *     fp4_device_status().
+ *   - Kernels are launched with programmatic dependent launch: each may start
+ *     while the previous kernel on the stream finishes, and waits for it
+ *     (griddepcontrol.wait) before touching global memory, so stream order
+ *     holds for all data.
  *   - Shapes: an operand is `rows x cols` with `cols` the dot-product dimension
  *     (K-major); BF16 inputs are row-major with leading dimension = cols.
  */
