@@ -379,3 +379,39 @@ class Fp4Linear:
     def step(self, x, w, dy, y, dx, dw, step: int = 0, stream=None):
         self.quantize_all(x, w, dy, step=step, stream=stream)
         self.gemms(y, dx, dw, stream=stream)
+
+    def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, step: int = 0, stream=None):
+        """`step` from pinned host tensors to pinned host tensors. The inputs are
+        copied to this layer's device buffers on a host-to-device stream, the
+        step runs on `stream` once they have landed, and the outputs are copied
+        back on a device-to-host stream once it is done. The call returns at once;
+        the next call's input copies wait only for this step to finish reading
+        the device inputs and its step only for the previous output copies, so
+        successive calls (of this and of other layers) overlap copies with
+        compute. `h2d_stream` can be made to wait on an event first; `ev_out`
+        marks the end of the output copies."""
+        dev = self.device
+        if not hasattr(self, "h2d_stream"):
+            self.h2d_stream = torch.cuda.Stream(device=dev)
+            self.d2h_stream = torch.cuda.Stream(device=dev)
+            self.ev_in, self.ev_done, self.ev_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            self.dev_in = {k: torch.empty(t.shape, dtype=t.dtype, device=dev)
+                           for k, t in (("x", x_h), ("w", w_h), ("dy", dy_h))}
+            self.dev_out = {k: torch.empty(t.shape, dtype=t.dtype, device=dev)
+                            for k, t in (("y", y_h), ("dx", dx_h), ("dw", dw_h))}
+        main = torch.cuda.current_stream() if stream is None else stream
+        di, do = self.dev_in, self.dev_out
+        self.h2d_stream.wait_event(self.ev_done)  # the previous step has read the device inputs
+        with torch.cuda.stream(self.h2d_stream):
+            for k, t in (("x", x_h), ("w", w_h), ("dy", dy_h)):
+                di[k].copy_(t, non_blocking=True)
+        self.ev_in.record(self.h2d_stream)
+        main.wait_event(self.ev_in)
+        main.wait_event(self.ev_out)  # the previous output copies have read the device outputs
+        self.step(di["x"], di["w"], di["dy"], do["y"], do["dx"], do["dw"], step=step, stream=main)
+        self.ev_done.record(main)
+        self.d2h_stream.wait_event(self.ev_done)
+        with torch.cuda.stream(self.d2h_stream):
+            for k, t in (("y", y_h), ("dx", dx_h), ("dw", dw_h)):
+                t.copy_(do[k], non_blocking=True)
+        self.ev_out.record(self.d2h_stream)

@@ -472,3 +472,29 @@ def test_8b_mxfp4_fprop_full_size_sampled():
     c_ref, s = oracle.gemm(refs[0]["codes"], refs[0]["scales"], 1.0, refs[1]["codes"], refs[1]["scales"], 1.0,
                            scale_fmt=oracle.FMT_UE8M0, bs=32, pairs=(ms, ns))
     _check(y.float().cpu().numpy()[ms, ns], c_ref, s, bf16=True)
+
+
+def test_step_from_host_equals_the_device_step():
+    """Fp4Linear.step_host (pinned host in, pinned host out, copies on their own
+    streams) gives the outputs of Fp4Linear.step on device copies of the inputs,
+    also when two layers' calls interleave over several steps."""
+    T, K, N = 512, 256, 512
+    rng_in = [(random_bf16(60 + 3 * i, (T, K), "student_t4"), random_bf16(61 + 3 * i, (N, K), "weight"),
+               random_bf16(62 + 3 * i, (T, N), "log_normal_1e-4_2")) for i in range(2)]
+    layers = [fb.Fp4Linear(T, K, N, rht=True, seed=1, layer=i) for i in range(2)]
+    host_in = [[torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for b in bits] for bits in rng_in]
+    host_out = [[torch.empty((T, N), dtype=torch.bfloat16).pin_memory(), torch.empty((T, K), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((N, K), dtype=torch.float32).pin_memory()] for _ in range(2)]
+    for _ in range(3):
+        for L, hi, ho in zip(layers, host_in, host_out):
+            L.step_host(*hi, *ho)
+    torch.cuda.synchronize()
+    assert fb.fp4_device_status() == 0
+    for i, (hi, ho) in enumerate(zip(host_in, host_out)):
+        L = fb.Fp4Linear(T, K, N, rht=True, seed=1, layer=i)
+        y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        dx = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+        dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+        L.step(*(t.cuda() for t in hi), y, dx, dw)
+        torch.cuda.synchronize()
+        assert torch.equal(y.cpu(), ho[0]) and torch.equal(dx.cpu(), ho[1]) and torch.equal(dw.cpu(), ho[2])
