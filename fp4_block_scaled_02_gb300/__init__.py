@@ -223,6 +223,11 @@ def fp4_linear_wgrad(dyt: QTensor, xt: QTensor, dw: torch.Tensor, accumulate: bo
                                             _stream(stream)), "fp4_linear_wgrad")
 
 
+def fp4_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (fp4_selftest_wait_timeout in fp4bs.h)."""
+    _lib.check(_lib.load().fp4_selftest_wait_timeout(limit_us, _stream(stream)), "fp4_selftest_wait_timeout")
+
+
 def fp4_device_status(stream=None) -> int:
     """Synchronise the stream; return and clear the device status word."""
     return _lib.load().fp4_device_status(_stream(stream))
@@ -379,6 +384,19 @@ class Fp4Linear:
     def step(self, x, w, dy, y, dx, dw, step: int = 0, stream=None):
         self.quantize_all(x, w, dy, step=step, stream=stream)
         self.gemms(y, dx, dw, stream=stream)
+
+    def state_dict(self) -> dict:
+        """The layer's only state across steps: the five held-amax records
+        (held scaling), as host copies. Randomness is keyed by (seed, tensor id,
+        step), which the caller passes in, so these records are all a resumed
+        run needs to continue byte for byte."""
+        return {"held_amax": [s.buf.cpu().clone() for s in self.states] if self.held else []}
+
+    def load_state_dict(self, d: dict) -> None:
+        recs = d["held_amax"]
+        assert len(recs) == (5 if self.held else 0), "state does not match this layer's scaling mode"
+        for s, r in zip(self.states, recs):
+            s.buf.copy_(r)
 
     def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, step: int = 0, stream=None):
         """`step` from pinned host tensors to pinned host tensors. The inputs are

@@ -35,7 +35,8 @@ FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05 = 0, 1
 EXPORTED = ["fp4_quantized_sizes", "fp4_workspace_bytes", "fp4_quantize", "fp4_dequantize", "fp4_gemm",
             "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
             "fp4_status_string", "fp4_abi_version", "fp4_quantize_noalloc", "fp4_quantize_dual",
-            "fp4_gemm_workspace_bytes", "fp4_gemm_ws", "fp4_tensor_amax", "fp4_tensor_amax_dual"]
+            "fp4_gemm_workspace_bytes", "fp4_gemm_ws", "fp4_tensor_amax", "fp4_tensor_amax_dual",
+            "fp4_selftest_wait_timeout"]
 
 
 class fp4_quant_params_t(ctypes.Structure):
@@ -104,6 +105,8 @@ def load() -> ctypes.CDLL:
             L.fp4_linear_dgrad.restype = i32
             L.fp4_linear_wgrad.argtypes = [TP, TP, P, i32, P]
             L.fp4_linear_wgrad.restype = i32
+            L.fp4_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
+            L.fp4_selftest_wait_timeout.restype = i32
             L.fp4_device_status.argtypes = [P]
             L.fp4_device_status.restype = i32
             L.fp4_status_string.argtypes = [i32]

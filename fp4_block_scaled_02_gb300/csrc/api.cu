@@ -498,6 +498,13 @@ fp4_status_t fp4_linear_wgrad(const fp4_tensor_t* dyt, const fp4_tensor_t* xt, f
     return fp4_gemm(dyt, xt, dw_fp32, 1, accumulate, stream);
 }
 
+fp4_status_t fp4_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+    if (limit_us == 0 || limit_us > 2000000u) return FP4_ERR_INVALID_ARG;
+    int* status = device_status_ptr();
+    if (status == nullptr) return FP4_ERR_CUDA;
+    return from_cuda(launch_wait_selftest((uint64_t)limit_us * 1000ull, status, static_cast<cudaStream_t>(stream)));
+}
+
 fp4_status_t fp4_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP4_ERR_CUDA;
     int* p = device_status_ptr();

@@ -661,6 +661,24 @@ __global__ void __launch_bounds__(128 * kRbParts)
 
 }  // namespace
 
+namespace {
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int* status) {
+    pdl_begin();
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(tc::smem_u32(&bar), 1);
+        tc::mbar_init_fence();
+        // phase 0 never completes: nothing arrives
+        (void)tc::mbar_wait(tc::smem_u32(&bar), 0u, status, limit_ns);
+    }
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t st) {
+    (void)launch_pdl(wait_selftest_kernel, 1, 32, 0, st, limit_ns, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_t* b_scales, int64_t N, int64_t K,
                                 uint8_t* a_out, uint8_t* b_out, int8_t* a_off, int8_t* b_off, uint8_t* flags,
                                 cudaStream_t st) {

@@ -137,6 +137,10 @@ cudaError_t launch_gemm_ue5m3(const GemmJob& job, cudaStream_t stream);
 cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_t* b_scales, int64_t N, int64_t K,
                                 uint8_t* a_out, uint8_t* b_out, int8_t* a_off, int8_t* b_off, uint8_t* flags,
                                 cudaStream_t stream);
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// completes; after limit_ns the wait records FP4_ERR_DEVICE_TIMEOUT in *status
+// and the kernel returns.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
 // Any of the n bytes at f nonzero (every thread of the calling warp gets the answer).
 __device__ __forceinline__ bool rb_any_flag(const uint8_t* f, int64_t n) {
     bool any = false;

@@ -53,12 +53,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // the status word and returns false, so no kernel spins forever.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) {
             record_status(status, kStatusTimeout);
             return false;
         }

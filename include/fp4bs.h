@@ -263,6 +263,13 @@ fp4_status_t fp4_linear_dgrad(const fp4_tensor_t* dy, const fp4_tensor_t* wt, vo
 fp4_status_t fp4_linear_wgrad(const fp4_tensor_t* dyt, const fp4_tensor_t* xt, float* dw_fp32,
                               int accumulate, void* stream);
 
+/* Diagnostic: exercises the path every kernel's bounded waits take on a stall.
+ * One thread of a one-block kernel waits on an mbarrier that nothing completes;
+ * after limit_us microseconds (1 .. 2,000,000) the wait gives up, records
+ * FP4_ERR_DEVICE_TIMEOUT in the device status word and the kernel returns,
+ * leaving the context usable. fp4_device_status() then reports the timeout. */
+fp4_status_t fp4_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
 /* Synchronise `stream`, then return and clear the current device's status word
  * (FP4_OK when no device-side error was recorded). */
 fp4_status_t fp4_device_status(void* stream);

@@ -53,6 +53,12 @@ def test_sizes_and_workspace_without_gpu(lib):
     assert lib.fp4_workspace_bytes(ctypes.byref(p), 256, 512) == 0
 
 
+def test_selftest_rejects_bad_limits_without_launching(lib):
+    from fp4_block_scaled_02_gb300 import _lib as L
+    assert lib.fp4_selftest_wait_timeout(0, None) == L.FP4_ERR_INVALID_ARG
+    assert lib.fp4_selftest_wait_timeout(2000001, None) == L.FP4_ERR_INVALID_ARG
+
+
 def test_argument_checks_return_before_any_launch(lib):
     from fp4_block_scaled_02_gb300 import _lib as L
     p = L.fp4_quant_params_t(0, 0, 0, 0, 0, 0, 448.0, 50, 0, 1, 0, 0, 0, 0)

@@ -498,3 +498,56 @@ def test_step_from_host_equals_the_device_step():
         L.step(*(t.cuda() for t in hi), y, dx, dw)
         torch.cuda.synchronize()
         assert torch.equal(y.cpu(), ho[0]) and torch.equal(dx.cpu(), ho[1]) and torch.equal(dw.cpu(), ho[2])
+
+
+def test_held_amax_checkpoint_resume_is_byte_identical():
+    """UE5M3 held-amax recipe: a run interrupted after step 30, its layer state
+    saved, restored into a new layer and continued to step 55 (past the refresh
+    at 50) leaves the same bytes and outputs as the uninterrupted run."""
+    from workloads import sweep_dy
+    T, K, N = 512, 256, 512
+    xb, wb = random_bf16(70, (T, K), "student_t4"), random_bf16(71, (N, K), "weight")
+    dyb = random_bf16(72, (T, N), "log_normal_1e-4_2")
+    x, w = to_gpu_bf16(xb), to_gpu_bf16(wb)
+    mk = lambda: fb.Fp4Linear(T, K, N, scale_fmt=UE, rht=False, held=True, target_T=2048.0, seed=5)
+    outs = lambda: (torch.empty((T, N), dtype=torch.bfloat16, device="cuda"),
+                    torch.empty((T, K), dtype=torch.bfloat16, device="cuda"),
+                    torch.empty((N, K), dtype=torch.float32, device="cuda"))
+    steps = list(range(0, 56, 5)) + [50, 55]
+    steps = sorted(set(steps))
+    a, oa = mk(), outs()
+    for s in steps:
+        a.step(x, w, to_gpu_bf16(sweep_dy(dyb, s, 100)), *oa, step=s)
+    b, ob = mk(), outs()
+    for s in [t for t in steps if t <= 30]:
+        b.step(x, w, to_gpu_bf16(sweep_dy(dyb, s, 100)), *ob, step=s)
+    saved = b.state_dict()
+    del b
+    c, oc = mk(), outs()
+    c.load_state_dict(saved)
+    for s in [t for t in steps if t > 30]:
+        c.step(x, w, to_gpu_bf16(sweep_dy(dyb, s, 100)), *oc, step=s)
+    torch.cuda.synchronize()
+    assert fb.fp4_device_status() == 0
+    for k in a.bufs:
+        assert torch.equal(a.bufs[k].codes, c.bufs[k].codes), k
+        assert torch.equal(a.bufs[k].scales, c.bufs[k].scales), k
+    for u, v in zip(oa, oc):
+        assert torch.equal(u, v)
+    for sa, sc in zip(a.states, c.states):
+        assert torch.equal(sa.buf, sc.buf)
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    """A kernel waiting on an mbarrier that nothing completes gives up after the
+    limit, records FP4_ERR_DEVICE_TIMEOUT, and later work runs normally."""
+    fb.fp4_selftest_wait_timeout(50000)  # 50 ms
+    assert fb.fp4_device_status() == fb._lib.FP4_ERR_DEVICE_TIMEOUT
+    assert fb.fp4_device_status() == 0   # read and cleared
+    ra, a = _operand(73, 128, 256, "normal")
+    rb, b = _operand(74, 128, 256, "normal")
+    d = torch.empty((128, 128), dtype=torch.float32, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert fb.fp4_device_status() == 0
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"])
+    _check(d.cpu().numpy(), c_ref, s, bf16=False)
