@@ -8,6 +8,10 @@
 #include <cuda_runtime.h>
 
 #include "fp4_device.cuh"
+#ifndef FP4BS_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 #include "internal.h"
 
 namespace fp4bs {
@@ -281,6 +285,28 @@ fp4_status_t check_amax_params(const fp4_quant_params_t* p, int64_t rows, int64_
 
 }  // namespace
 
+namespace {
+
+// An NVTX range around each launching entry point, so profilers show the C-ABI
+// calls on their timelines (no cost without a profiler attached; compile with
+// FP4BS_NO_NVTX to leave them out).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) {
+#ifndef FP4BS_NO_NVTX
+        nvtxRangePushA(name);
+#else
+        (void)name;
+#endif
+    }
+    ~NvtxRange() {
+#ifndef FP4BS_NO_NVTX
+        nvtxRangePop();
+#endif
+    }
+};
+
+}  // namespace
+
 extern "C" {
 
 int fp4_abi_version(void) { return 1; }
@@ -323,6 +349,7 @@ size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t co
 fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
                           const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                           uint64_t* counters, void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("fp4_quantize");
     QuantJob job;
     fp4_status_t s = check_quantize(p, in_bf16, rows, cols, out, out_t, state, counters, ws, ws_bytes, job);
     if (s != FP4_OK) return s;
@@ -335,6 +362,7 @@ fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int6
 fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
                                   const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                                   uint64_t* counters, void* stream) {
+    NvtxRange nvtx_range("fp4_quantize_noalloc");
     float* scratch = noalloc_scratch_ptr();
     if (scratch == nullptr) return FP4_ERR_CUDA;
     QuantJob job;
@@ -354,6 +382,7 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
                                int64_t rows, int64_t cols, const fp4_tensor_t* out_row, const fp4_tensor_t* out_col,
                                fp4_amax_state_t* state_row, fp4_amax_state_t* state_col, uint64_t* counters_row,
                                uint64_t* counters_col, void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("fp4_quantize_dual");
     if (p_row == nullptr || p_col == nullptr) return FP4_ERR_INVALID_ARG;
     if (p_row->orient != FP4_ORIENT_ROWWISE || p_col->orient != FP4_ORIENT_COLWISE) return FP4_ERR_INVALID_ARG;
     if (p_row->block != FP4_BLOCK_1x16 || p_col->block != FP4_BLOCK_1x16) return FP4_ERR_UNSUPPORTED;
@@ -382,6 +411,7 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
 
 fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
                              fp4_amax_state_t* out, void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("fp4_tensor_amax");
     fp4_status_t s = check_amax_params(p, rows, cols);
     if (s != FP4_OK) return s;
     if (out == nullptr || (rows > 0 && cols > 0 && in_bf16 == nullptr)) return FP4_ERR_INVALID_ARG;
@@ -398,6 +428,7 @@ fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, i
 fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
                                   int64_t rows, int64_t cols, fp4_amax_state_t* out_row, fp4_amax_state_t* out_col,
                                   void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("fp4_tensor_amax_dual");
     fp4_status_t s = check_amax_params(p_row, rows, cols);
     if (s != FP4_OK) return s;
     s = check_amax_params(p_col, rows, cols);
@@ -416,6 +447,7 @@ fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_qua
 }
 
 fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void* stream) {
+    NvtxRange nvtx_range("fp4_dequantize");
     if (t == nullptr || out == nullptr) return FP4_ERR_INVALID_ARG;
     if (t->rows == 0 || t->cols == 0) return FP4_OK;
     fp4_status_t s = check_operand(t);
@@ -434,6 +466,7 @@ fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void
 
 fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
                       void* stream) {
+    NvtxRange nvtx_range("fp4_gemm");
     GemmJob j;
     fp4_status_t s = prepare_gemm(a, b, d, out_fp32, accumulate, j);
     if (s != FP4_OK) return s;
@@ -451,6 +484,7 @@ size_t fp4_gemm_workspace_bytes(const fp4_tensor_t* a, const fp4_tensor_t* b) {
 
 fp4_status_t fp4_gemm_ws(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
                          void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("fp4_gemm_ws");
     GemmJob j;
     fp4_status_t s = prepare_gemm(a, b, d, out_fp32, accumulate, j);
     if (s != FP4_OK) return s;

@@ -551,3 +551,20 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
     assert fb.fp4_device_status() == 0
     c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"])
     _check(d.cpu().numpy(), c_ref, s, bf16=False)
+
+
+@pytest.mark.parametrize("fmt", [fb.FP4_SCALE_E4M3, MX, UE])
+def test_gemm_is_deterministic(fmt):
+    """Two launches of the same product give the same bits (no atomics, fixed
+    accumulation order), for NVFP4, MXFP4 and rebiased UE5M3 alike."""
+    M, N, K = 2048, 2176, 1280
+    kw = dict(block=fb.FP4_BLOCK_1x32) if fmt == MX else {}
+    _, a = _operand(75, M, K, "normal", fmt=fmt, **kw)
+    _, b = _operand(76, N, K, "student_t4", fmt=fmt, **kw)
+    ws = _ws_for(a, b) if fmt == UE else None
+    d1 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    d2 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    fb.fp4_gemm(a, b, d1, ws=ws)
+    fb.fp4_gemm(a, b, d2, ws=ws)
+    assert fb.fp4_device_status() == 0
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
