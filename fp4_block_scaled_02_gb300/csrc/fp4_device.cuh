@@ -325,10 +325,10 @@ __device__ __forceinline__ void sr_block_bits(uint64_t g0, uint32_t tensor_id, u
                                               const uint32_t (&rk)[20], uint4 r[4]) {
     unsigned long long p;
     asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(tensor_id), "r"(0xCD9E8D57u));
-    const uint32_t x1 = (uint32_t)(p >> 32) ^ (uint32_t)(g0 >> 32) ^ rk[0];  // round 1 output, word 0
-    const uint32_t y1k = (uint32_t)p ^ rk[2];                                // round 1 word 1, round 2 key folded
+    const uint32_t x1 = (uint32_t)(p >> 32) ^ (uint32_t)(g0 >> 32) ^ rk[0];  // word 0 after the first Philox round
+    const uint32_t y1k = (uint32_t)p ^ rk[2];                                // word 1 after it, with the next key folded in
     asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(x1), "r"(0xD2511F53u));
-    const uint32_t z2k = (uint32_t)(p >> 32) ^ rk[3], w2 = (uint32_t)p;    // round 2 parts from word 0
+    const uint32_t z2k = (uint32_t)(p >> 32) ^ rk[3], w2 = (uint32_t)p;    // second-round parts from word 0
     const uint32_t sk = step_lo ^ rk[1];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
