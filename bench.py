@@ -153,13 +153,17 @@ def cpu_baseline_entry(workload, tokens: int, feats: int, min_seconds: float = 1
 
 # --------------------------------------------------------------------------- distributed
 def dist_setup():
+    """One process per GPU (torchrun env vars). Replicas only: the ranks exchange
+    nothing but a barrier and the max of their timings. NCCL on GPUs, gloo on CPU."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        local = int(os.environ.get("LOCAL_RANK", "0"))
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
         return dist, dist.get_rank(), world
     return None, 0, 1
 
@@ -173,7 +177,8 @@ def max_over_ranks(dist, v: float) -> float:
     if dist is None:
         return v
     import torch
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
