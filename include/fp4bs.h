@@ -70,9 +70,11 @@ typedef enum { FP4_BLOCK_1x16 = 0, FP4_BLOCK_16x16 = 1, FP4_BLOCK_1x32 = 2 } fp4
 
 typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_round_t;
 
-/* Tensor scale: per-call amax (App. B.1) or held amax refreshed when
+/* Tensor scale: per-call amax (App. B.1: CURRENT), held amax refreshed when
  * step % refresh_every == 0 or when the held state is not valid yet (UE5M3
- * page: refresh every 50 steps); other steps use the held amax. */
+ * page: refresh every 50 steps; other steps use the held amax: HELD), or the
+ * amax a previous fp4_tensor_amax call left in the state record (GIVEN: the
+ * same bytes as CURRENT without the call's own amax pass). */
 typedef enum { FP4_TSCALE_CURRENT = 0, FP4_TSCALE_HELD = 1, FP4_TSCALE_GIVEN = 2 } fp4_tscale_t;
 
 /* ROWWISE: the operand is the input itself (blocks run along its columns).
