@@ -4,16 +4,19 @@ One step = the whole hot path over one batch of the 1.2B Transformer FFN
 workload (T = 8192 tokens; linears 2048 -> 6144 and 6144 -> 2048): for each
 linear, the five quantized operands (X rowwise and X^T colwise + RHT16 from one
 pass over X, W 16x16 in both orientations, dY rowwise SR and dY^T colwise +
-RHT16 + SR from one pass over dY; each pass preceded by its tensor-amax pass)
-and the three block-scaled NVFP4 GEMMs (Fprop, Dgrad, Wgrad).
+RHT16 + SR from one pass over dY; each preceded by its tensor amax, computed on
+a second stream while the previous operand is converted) and the three
+block-scaled NVFP4 GEMMs (Fprop, Dgrad, Wgrad).
 
 `value` is fwd+bwd GEMM TFLOP/s of the whole step (6 T N K per linear divided
 by the step time, quantization included) with inputs resident in HBM; `e2e`
-is the same metric through the public API with the inputs copied from pinned
-host memory and the outputs copied back inside the timed region.
+is the same metric through the public API (Fp4Linear.step_host) with the
+inputs copied from pinned host memory and the outputs copied back inside the
+timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1.2b|8b|12b|tiny]
     python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+    python bench.py --kernels              # single library calls, each against its roofline
 """
 from __future__ import annotations
 
@@ -376,6 +379,109 @@ def load_traffic() -> dict:
     return {}
 
 
+# --------------------------------------------------------------------------- per-kernel timings
+def run_kernels(args):
+    """`--kernels`: median CUDA-event time of single library calls (10 reps, L2
+    flushed before each by writing 256 MB), with each call's roofline fraction:
+    GEMMs against the FP4 dense peak (the emulated UE5M3 path against BF16),
+    quantizer calls against the HBM copy peak with their algorithmic bytes.
+    GEMM operands are random codes with block scales of moderate size; quantizer
+    inputs random normal BF16. Prints one JSON line."""
+    import torch
+
+    import fp4_block_scaled_02_gb300 as fb
+
+    fb._lib.load()
+    torch.manual_seed(0)
+    peaks, src = load_peaks()
+    fp4_peak, bf16_peak, hbm_peak = peaks["bf16_tflops"] * FP4_OVER_BF16, peaks["bf16_tflops"], peaks["hbm_gbs"]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def time_ms(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    def operand(rows, cols, fmt):
+        t = fb.QTensor.empty(rows, cols, fmt)
+        t.codes.copy_(torch.randint(0, 256, t.codes.shape, dtype=torch.uint8, device="cuda"))
+        lo = {fb.FP4_SCALE_E4M3: 0x30, fb.FP4_SCALE_UE5M3: 0x70, fb.FP4_SCALE_UE8M0: 0x7C}[fmt]
+        t.scales.copy_(torch.randint(lo, lo + 16, t.scales.shape, dtype=torch.uint8, device="cuda"))
+        t.s_dec.fill_(1.0)
+        return t
+
+    res = {}
+    gemms = [("nvfp4", fb.FP4_SCALE_E4M3, "8b_fprop", (8192, 21504, 4096)),
+             ("nvfp4", fb.FP4_SCALE_E4M3, "8b_dgrad", (8192, 4096, 21504)),
+             ("nvfp4", fb.FP4_SCALE_E4M3, "8b_wgrad", (21504, 4096, 8192)),
+             ("nvfp4", fb.FP4_SCALE_E4M3, "12b_fprop", (8192, 12288, 4608)),
+             ("nvfp4", fb.FP4_SCALE_E4M3, "12b_dgrad", (8192, 4608, 12288)),
+             ("nvfp4", fb.FP4_SCALE_E4M3, "1p2b_fprop", (8192, 6144, 2048)),
+             ("nvfp4", fb.FP4_SCALE_E4M3, "1p2b_dgrad", (8192, 2048, 6144)),
+             ("mxfp4", fb.FP4_SCALE_UE8M0, "8b_fprop", (8192, 21504, 4096)),
+             ("mxfp4", fb.FP4_SCALE_UE8M0, "1p2b_fprop", (8192, 6144, 2048)),
+             ("ue5m3_emulated", fb.FP4_SCALE_UE5M3, "sweep", (8192, 4096, 4096)),
+             ("ue5m3_rebiased", fb.FP4_SCALE_UE5M3, "sweep", (8192, 4096, 4096))]
+    for kind, fmt, name, (M, N, K) in gemms:
+        a, b = operand(M, K, fmt), operand(N, K, fmt)
+        d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(fb.fp4_gemm_workspace_bytes(a, b), dtype=torch.uint8, device="cuda") \
+            if kind == "ue5m3_rebiased" else None
+        ms = time_ms(lambda: fb.fp4_gemm(a, b, d, ws=ws))
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        peak = bf16_peak if kind == "ue5m3_emulated" else fp4_peak
+        res[f"gemm_{kind}_{name}_bf16"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peak, 3)}
+        del a, b, d, ws
+    T, C = 8192, 6144
+    x = torch.randn((T, C), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(8192, dtype=torch.float32, device="cuda")
+    E, SR = fb.FP4_SCALE_E4M3, fb.FP4_ROUND_SR
+    quants = {
+        "rows_rne": (lambda: fb.fp4_quantize(fb.QuantConfig(), x, o_r, ws=ws), 4.5625),
+        "rows_sr": (lambda: fb.fp4_quantize(fb.QuantConfig(round=SR), x, o_r, ws=ws), 4.5625),
+        "cols_rht_sr": (lambda: fb.fp4_quantize(fb.QuantConfig(round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True),
+                                                x, o_c, ws=ws), 4.5625),
+        "dual_rne_rht": (lambda: fb.fp4_quantize_dual(fb.QuantConfig(), fb.QuantConfig(
+            orient=fb.FP4_ORIENT_COLWISE, rht=True), x, o_r, o_c, ws=ws), 5.125),
+        "dual_sr_rht": (lambda: fb.fp4_quantize_dual(fb.QuantConfig(round=SR), fb.QuantConfig(
+            round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True), x, o_r, o_c, ws=ws), 5.125),
+        "mxfp4_rows": (lambda: fb.fp4_quantize(fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE8M0, block=fb.FP4_BLOCK_1x32),
+                                               x, o_mx), 2.53125),
+        "tensor_amax_dual_rht": (lambda: fb.fp4_tensor_amax_dual(fb.QuantConfig(), fb.QuantConfig(
+            orient=fb.FP4_ORIENT_COLWISE, rht=True), x, st_r, st_c, ws), 2.0),
+    }
+    o_r, o_c = fb.QTensor.empty(T, C), fb.QTensor.empty(C, T)
+    o_mx = fb.QTensor.empty(T, C, fb.FP4_SCALE_UE8M0)
+    st_r, st_c = fb.AmaxState(), fb.AmaxState()
+    for name, (fn, bpe) in quants.items():
+        ms = time_ms(fn)
+        gbs = bpe * T * C / (ms * 1e-3) / 1e9
+        res[f"quantize_{name}_{T}x{C}"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 3)}
+    w = torch.randn((12288, 4608), dtype=torch.bfloat16, device="cuda")
+    o1, o2 = fb.QTensor.empty(12288, 4608), fb.QTensor.empty(4608, 12288)
+    ms = time_ms(lambda: fb.fp4_quantize(fb.QuantConfig(block=fb.FP4_BLOCK_16x16, emit_transpose=True), w, o1, o2,
+                                         ws=ws))
+    gbs = 5.125 * w.numel() / (ms * 1e-3) / 1e9
+    res["quantize_2d_both_12288x4608"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 3)}
+    status = fb.fp4_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    print(json.dumps({"kernels": res, "peaks": {"fp4_tflops": fp4_peak, "bf16_tflops": bf16_peak,
+                                                "hbm_gbs": hbm_peak, "source": src},
+                      "method": "median of 10 CUDA-event timed calls, L2 flushed before each"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,12 +492,15 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--ref-feats", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels", action="store_true", help="time single library calls instead of the step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3
     from workloads import WORKLOADS
     workload = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.kernels:
+        run_kernels(args)
+    elif args.impl == "reference":
         run_reference(args, workload)
     else:
         run_gpu(args, workload)
