@@ -110,7 +110,6 @@ struct NvCfg {
     static_assert(BK % SF_CHUNK_K == 0, "whole scale chunks per stage");
     static constexpr int SFA_BYTES = (BM / 128) * 512 * SF_CHUNKS;
     static constexpr int SFB_BYTES = (BN / 128) * 512 * SF_CHUNKS;
-    static constexpr uint32_t TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int NUM_ACC = (BN <= 128) ? 2 : 1;
     static constexpr int SF_COLS_A = 4 * SF_CHUNKS;          // 4 columns per chunk
     static constexpr int SF_COLS_B = SF_CHUNKS * (BN / 32);  // (BN / 32) columns per chunk
