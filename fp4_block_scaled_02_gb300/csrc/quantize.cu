@@ -162,15 +162,15 @@ __device__ __forceinline__ void fill_enc_table(float* tab, float s_dec) {
 // and the code sign bits. Folding is exact: pre * v[i] is exact, and so is
 // pre * s_enc,L unless s_enc,L < 2^-124, where the two products are taken
 // apart. vmax is max |v[i]|, any_zero whether some v[i] is +-0; enc_tab holds
-// s_enc,L per scale code (fill_enc_table). `g0` = (index of element 0) / 4, the
-// first of the block's four SR groups.
+// s_enc,L per scale code (fill_enc_table). `c0` = (index of element 0) / 8, the
+// first of the block's two SR counters.
 // Event counts: scale saturation and underflow; element saturation, counted
 // per element only when the scaled block max exceeds 6 (rounding is monotone,
 // so otherwise no element can); element underflow = zero-magnitude codes minus
 // zero inputs.
 template <int FMT, bool SR, bool RHT>
 __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vmax, bool any_zero,
-                                                     const float* enc_tab, float s_enc, uint64_t g0, const QParams& q,
+                                                     const float* enc_tab, float s_enc, uint64_t c0, const QParams& q,
                                                      uint32_t smask_lo, uint32_t smask_hi, uint32_t& lo, uint32_t& hi,
                                                      Counts& cnt) {
     using F = ScaleFmt<FMT>;
@@ -207,8 +207,8 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vm
         for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[i]);
     }
     if (SR) {
-        uint4 r[4];
-        sr_block_bits(g0, q.tensor_id, q.step_lo, q.round_key, r);
+        uint4 r[2];
+        sr_block_bits(c0, q.tensor_id, q.step_lo, q.round_key, r);
         e2m1_sr_x16(x, r, lo, hi);
     } else {
         lo = e2m1_rne_x8(x);
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
                 float v[16];
                 unpack16(a, c, v);
                 uint32_t lo, hi;
-                sc = quantize_block16<FMT, SR, false>(v, vmax, any_zero, enc_tab, s_enc, (uint64_t)(4 * b), q, 0u, 0u,
+                sc = quantize_block16<FMT, SR, false>(v, vmax, any_zero, enc_tab, s_enc, (uint64_t)(2 * b), q, 0u, 0u,
                                                       lo, hi, cnt);
                 *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
             }
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_cols_kernel(QParams q) {
                     bool any_zero;
                     const float vmax = amax_f32x16(v, any_zero);
                     sc = quantize_block16<FMT, SR, RHT>(v, vmax, any_zero, enc_tab, s_enc,
-                                                        (uint64_t)((c * T + 16 * j) >> 2), q, smask_lo, smask_hi, lo,
+                                                        (uint64_t)((c * T + 16 * j) >> 3), q, smask_lo, smask_hi, lo,
                                                         hi, cnt);
                     *reinterpret_cast<uint2*>(q.codes + c * (T / 2) + 8 * j) = make_uint2(lo, hi);
                 }
@@ -650,8 +650,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (SR) {
                     // W element (n, k) has index n K + k
                     const int64_t e0 = (n0 + 16 * bn + l + 8 * h) * K + k0 + 16 * bk;
-                    uint4 r[4];
-                    sr_block_bits((uint64_t)(e0 >> 2), q.tensor_id, q.step_lo, q.round_key, r);
+                    uint4 r[2];
+                    sr_block_bits((uint64_t)(e0 >> 3), q.tensor_id, q.step_lo, q.round_key, r);
                     e2m1_sr_x16(x[h], r, cw[h][0], cw[h][1]);
                 } else {
                     cw[h][0] = e2m1_rne_x8(x[h]);
@@ -700,8 +700,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (SR) {
                         // W^T element (k, n) has index k N + n
                         const int64_t e0 = (k0 + 16 * bk + 2 * l + hh) * N + n0 + 16 * bn;
-                        uint4 r[4];
-                        sr_block_bits((uint64_t)(e0 >> 2), q.tensor_id, q.step_lo, q.round_key, r);
+                        uint4 r[2];
+                        sr_block_bits((uint64_t)(e0 >> 3), q.tensor_id, q.step_lo, q.round_key, r);
                         e2m1_sr_x16(x, r, tw[hh][0], tw[hh][1]);
                     } else {
                         tw[hh][0] = e2m1_rne_x8(x);
@@ -988,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int64_t code_off = code_row_tile + code_row_thr + 256 * i * nb_row;  // = 8 * block index
             uint32_t lo, hi;
             const uint32_t sc = quantize_block16<FMT, SR_ROW, false>(v, vmax, any_zero, tab_r, se_r,
-                                                                     (uint64_t)(code_off >> 1), qr, 0u, 0u, lo, hi, cr);
+                                                                     (uint64_t)(code_off >> 2), qr, 0u, 0u, lo, hi, cr);
             *reinterpret_cast<uint2*>(qr.codes + code_off) = make_uint2(lo, hi);
             uint32_t ww = sc << (8 * (lane & 3));
             ww |= __shfl_xor_sync(0xFFFFFFFFu, ww, 1);
@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int64_t code_off = code_col_tile + (int64_t)cc_local * (T >> 1);  // = 8 * block index
                 uint32_t lo, hi;
                 const uint32_t sc = quantize_block16<FMT, SR_COL, RHT>(v, vmax, any_zero, tab_c, se_c,
-                                                                       (uint64_t)(code_off >> 1), qc, smask_lo,
+                                                                       (uint64_t)(code_off >> 2), qc, smask_lo,
                                                                        smask_hi, lo, hi, cc);
                 *reinterpret_cast<uint2*>(qc.codes + code_off) = make_uint2(lo, hi);
                 qc.scales[sc_col_tile + 16 * (cc_local & 31) + 4 * (cc_local >> 5)] = (uint8_t)sc;

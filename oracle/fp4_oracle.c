@@ -164,13 +164,15 @@ uint8_t orc_e2m1_rne(float v) {
 
 /* Stochastic rounding ([NV] 4.4): round |v| to one of its two neighbouring E2M1
  * magnitudes lo <= |v| < hi, choosing hi with probability proportional to the
- * distance from lo. Reading of the random-bit contract: r is one uniform 32-bit
- * Philox word and the value rounds up iff (float)(r >> 8) < frac * 2^24, where
- * frac = (|v| - lo) / (hi - lo). frac is exact in FP32 (Sterbenz lemma:
- * hi <= 2 lo whenever lo > 0, and hi - lo is a power of two), frac * 2^24 and
- * the 24-bit integer are exact too, so P(up) = ceil(frac * 2^24) / 2^24, within
- * 2^-24 of frac. |v| >= 6 saturates to 6; the code's sign bit is v's. */
-uint8_t orc_e2m1_sr(float v, uint32_t r) {
+ * distance from lo. Reading of the random-bit contract: the one of the native
+ * FP4 stochastic-rounding conversion that [NV] A3 ("hardware support") says
+ * Blackwell provides -- each element draws a uniform 16-bit integer R and rounds
+ * up iff R + floor(frac * 2^16) >= 2^16, where frac = (|v| - lo) / (hi - lo).
+ * frac is exact in FP32 (Sterbenz lemma: hi <= 2 lo whenever lo > 0, and hi - lo
+ * is a power of two), and so are frac * 2^16 and its floor, so
+ * P(up) = floor(frac * 2^16) / 2^16, within 2^-16 of frac (never above it).
+ * |v| >= 6 saturates to 6; the code's sign bit is v's. */
+uint8_t orc_e2m1_sr(float v, uint32_t r16) {
     float a = fabsf(v);
     uint8_t sign = signbit(v) ? 8 : 0;
     if (a >= 6.0f) return (uint8_t)(sign | 7);
@@ -179,7 +181,8 @@ uint8_t orc_e2m1_sr(float v, uint32_t r) {
     float flo = (float)E2M1_MAG[lo];
     float fhi = (float)E2M1_MAG[lo + 1];
     float frac = (a - flo) / (fhi - flo);
-    int up = (float)(r >> 8) < frac * 16777216.0f;
+    uint32_t fh = (uint32_t)floorf(frac * 65536.0f);
+    int up = (r16 & 0xFFFFu) + fh >= 65536u;
     return (uint8_t)(sign | (lo + up));
 }
 
@@ -216,15 +219,22 @@ void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint3
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* Reading of the stochastic-rounding bits: element e (row-major linear index in
- * the quantized operand) takes word (e & 3) of
- * Philox(key = seed, counter = (lo32(e>>2), hi32(e>>2), tensor_id, lo32(step))). */
+/* Reading of the stochastic-rounding bits: one Philox(key = seed, counter =
+ * (lo32(e>>3), hi32(e>>3), tensor_id, lo32(step))) call serves the eight
+ * elements e>>3 of the quantized operand (e its row-major linear index). Each
+ * 32-bit word serves two of them: word 2 ((e>>2) & 1) + (e & 1), so a quad of
+ * elements 4q .. 4q+3 takes two words, one for its even and one for its odd
+ * elements. Within the word, the element with (e>>1) & 1 == 0 takes bytes 2
+ * (high) and 0 (low), the other bytes 3 (high) and 1 (low) -- the two 16-bit
+ * draws the native conversion reads from one random operand. Returns R. */
 uint32_t orc_sr_bits(uint64_t seed, uint32_t tensor_id, uint64_t step, uint64_t e) {
-    uint32_t ctr[4] = {(uint32_t)(e >> 2), (uint32_t)(e >> 34), tensor_id, (uint32_t)step};
+    uint32_t ctr[4] = {(uint32_t)(e >> 3), (uint32_t)(e >> 35), tensor_id, (uint32_t)step};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t w[4];
     orc_philox4x32_10(ctr, key, w);
-    return w[e & 3];
+    uint32_t word = w[2 * ((e >> 2) & 1) + (e & 1)];
+    if (((e >> 1) & 1) == 0) return (((word >> 16) & 0xFFu) << 8) | (word & 0xFFu);
+    return ((word >> 24) << 8) | ((word >> 8) & 0xFFu);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -82,29 +82,34 @@ def test_e2m1_rne_ties_go_to_even_code(orc):
 
 
 def test_e2m1_sr_thresholds_worked_by_hand(orc):
-    # 4.4 stochastic rounding, reading: up iff (r >> 8) < frac * 2^24 for the
-    # element's 32-bit draw r. Each case: value, lower code, and the first r that
-    # rounds DOWN (every r below it rounds up), worked out by hand from frac.
+    # 4.4 stochastic rounding, reading: up iff R + floor(frac * 2^16) >= 2^16 for
+    # the element's 16-bit draw R (the native FP4 SR conversion's contract). Each
+    # case: value, lower code, and the first R that rounds UP (every R below it
+    # rounds down), worked out by hand from frac; None = no draw rounds up.
     cases = [
-        (1.25, 2, 1 << 31),                 # lo 1, hi 1.5: frac 1/2 -> 2^23 -> r < 2^31
-        (0.75, 1, 1 << 31),                 # lo 0.5, hi 1: frac 1/2
-        (0.3046875, 0, 10223616 * 256),     # lo 0, hi 0.5: frac 0.609375 -> 10223616
-        (5.5, 6, 12582912 * 256),           # lo 4, hi 6: frac 3/4 -> 12582912
-        (1.0 + 2.0 ** -17 + 2.0 ** -21, 2, 272 * 256),  # frac 2^-16 + 2^-20 -> 272
-        (2.0 ** -20, 0, 32 * 256),          # frac 2^-19 -> 32
-        (2.0 ** -30, 0, 256),               # frac 2^-29 -> 1/32: only r >> 8 == 0 rounds up
+        (1.25, 2, 1 << 15),                   # lo 1, hi 1.5: frac 1/2 -> 32768 -> R >= 32768
+        (0.75, 1, 1 << 15),                   # lo 0.5, hi 1: frac 1/2
+        (0.3046875, 0, 65536 - 39936),        # lo 0, hi 0.5: frac 0.609375 -> 39936
+        (5.5, 6, 65536 - 49152),              # lo 4, hi 6: frac 3/4 -> 49152
+        (1.0 + 2.0 ** -17 + 2.0 ** -21, 2, 65535),  # frac 2^-16 + 2^-20 -> floor 1
+        (1.0 + 3 * 2.0 ** -17, 2, 65533),     # frac 3 * 2^-16 -> 3
+        (2.0 ** -17, 0, 65535),               # frac 2^-16 -> 1: only R = 0xFFFF rounds up
+        (2.0 ** -20, 0, None),                # frac 2^-19 -> floor 0: never up
     ]
-    for v, lo_code, first_down in cases:
+    for v, lo_code, first_up in cases:
         for sgn in (1.0, -1.0):
             sign = 8 if sgn < 0 else 0
-            assert orc.e2m1_sr(sgn * v, first_down - 1) == sign | (lo_code + 1), (v, first_down)
-            assert orc.e2m1_sr(sgn * v, first_down) == sign | lo_code, (v, first_down)
-            assert orc.e2m1_sr(sgn * v, 0) == sign | (lo_code + 1)
-            assert orc.e2m1_sr(sgn * v, 0xFFFFFFFF) == sign | lo_code
+            assert orc.e2m1_sr(sgn * v, 0) == sign | lo_code, v
+            if first_up is None:
+                assert orc.e2m1_sr(sgn * v, 0xFFFF) == sign | lo_code, v
+                continue
+            assert orc.e2m1_sr(sgn * v, first_up - 1) == sign | lo_code, (v, first_up)
+            assert orc.e2m1_sr(sgn * v, first_up) == sign | (lo_code + 1), (v, first_up)
+            assert orc.e2m1_sr(sgn * v, 0xFFFF) == sign | (lo_code + 1), v
     # on the grid nothing rounds up, whatever the draw
     for v, code in ((1.0, 2), (3.0, 5), (0.0, 0), (0.5, 1)):
-        assert orc.e2m1_sr(v, 0) == code
-    assert orc.e2m1_sr(-0.0, 0) == 8
+        assert orc.e2m1_sr(v, 0xFFFF) == code
+    assert orc.e2m1_sr(-0.0, 0xFFFF) == 8
     assert orc.e2m1_sr(6.0, 0) == 7 and orc.e2m1_sr(-7.0, 0) == 15 and orc.e2m1_sr(1e30, 0) == 7
 
 

@@ -60,12 +60,24 @@ def test_philox_matches_triton(orc):
 
 
 def test_sr_bits_index_contract(orc):
-    # element e uses word (e & 3) of the Philox block e >> 2
+    # one Philox block per 8 elements (counter e >> 3); word 2 ((e >> 2) & 1) +
+    # (e & 1); the element with (e >> 1) & 1 == 0 takes bytes 2:0 of the word,
+    # the other bytes 3:1 (high byte first)
     seed, tid, step = 0xDEADBEEF12345, 3, 77
-    for e in [0, 1, 2, 3, 4, 7, 8, 9, 1 << 33, (1 << 40) + 5]:
-        w = orc.philox4x32_10([(e >> 2) & 0xFFFFFFFF, (e >> 34) & 0xFFFFFFFF, tid, step & 0xFFFFFFFF],
+    for e in [0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 1 << 33, (1 << 40) + 5, (1 << 40) + 14]:
+        w = orc.philox4x32_10([(e >> 3) & 0xFFFFFFFF, (e >> 35) & 0xFFFFFFFF, tid, step & 0xFFFFFFFF],
                               [seed & 0xFFFFFFFF, seed >> 32])
-        assert orc.sr_bits(seed, tid, step, e) == int(w[e & 3])
+        b = int(w[2 * ((e >> 2) & 1) + (e & 1)]).to_bytes(4, "little")
+        want = b[2] * 256 + b[0] if (e >> 1) & 1 == 0 else b[3] * 256 + b[1]
+        assert orc.sr_bits(seed, tid, step, e) == want
+    # the eight elements of one block use all 256 bits once
+    got = sorted(orc.sr_bits(seed, tid, step, e) for e in range(8))
+    w = orc.philox4x32_10([0, 0, tid, step], [seed & 0xFFFFFFFF, seed >> 32])
+    halves = []
+    for x in w.tolist():
+        b = x.to_bytes(4, "little")
+        halves += [b[2] * 256 + b[0], b[3] * 256 + b[1]]
+    assert got == sorted(halves)
 
 
 def _kron_hadamard(n):
