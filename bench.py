@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -386,7 +387,8 @@ def run_kernels(args):
     GEMMs against the FP4 dense peak (the emulated UE5M3 path against BF16),
     quantizer calls against the HBM copy peak with their algorithmic bytes.
     GEMM operands are random codes with block scales of moderate size; quantizer
-    inputs random normal BF16. Prints one JSON line."""
+    inputs random normal BF16. `--only REGEX` keeps the calls whose key matches
+    (for a profiler capture of one kind of call). Prints one JSON line."""
     import torch
 
     import fp4_block_scaled_02_gb300 as fb
@@ -433,7 +435,14 @@ def run_kernels(args):
              ("mxfp4", fb.FP4_SCALE_UE8M0, "1p2b_fprop", (8192, 6144, 2048)),
              ("ue5m3_emulated", fb.FP4_SCALE_UE5M3, "sweep", (8192, 4096, 4096)),
              ("ue5m3_rebiased", fb.FP4_SCALE_UE5M3, "sweep", (8192, 4096, 4096))]
+    only = re.compile(args.only) if args.only else None
+
+    def wanted(key):
+        return only is None or only.search(key) is not None
+
     for kind, fmt, name, (M, N, K) in gemms:
+        if not wanted(f"gemm_{kind}_{name}_bf16"):
+            continue
         a, b = operand(M, K, fmt), operand(N, K, fmt)
         d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         ws = torch.zeros(fb.fp4_gemm_workspace_bytes(a, b), dtype=torch.uint8, device="cuda") \
@@ -465,15 +474,19 @@ def run_kernels(args):
     o_mx = fb.QTensor.empty(T, C, fb.FP4_SCALE_UE8M0)
     st_r, st_c = fb.AmaxState(), fb.AmaxState()
     for name, (fn, bpe) in quants.items():
+        if not wanted(f"quantize_{name}_{T}x{C}"):
+            continue
         ms = time_ms(fn)
         gbs = bpe * T * C / (ms * 1e-3) / 1e9
         res[f"quantize_{name}_{T}x{C}"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 3)}
-    w = torch.randn((12288, 4608), dtype=torch.bfloat16, device="cuda")
-    o1, o2 = fb.QTensor.empty(12288, 4608), fb.QTensor.empty(4608, 12288)
-    ms = time_ms(lambda: fb.fp4_quantize(fb.QuantConfig(block=fb.FP4_BLOCK_16x16, emit_transpose=True), w, o1, o2,
-                                         ws=ws))
-    gbs = 5.125 * w.numel() / (ms * 1e-3) / 1e9
-    res["quantize_2d_both_12288x4608"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 3)}
+    if wanted("quantize_2d_both_12288x4608"):
+        w = torch.randn((12288, 4608), dtype=torch.bfloat16, device="cuda")
+        o1, o2 = fb.QTensor.empty(12288, 4608), fb.QTensor.empty(4608, 12288)
+        ms = time_ms(lambda: fb.fp4_quantize(fb.QuantConfig(block=fb.FP4_BLOCK_16x16, emit_transpose=True), w, o1,
+                                             o2, ws=ws))
+        gbs = 5.125 * w.numel() / (ms * 1e-3) / 1e9
+        res["quantize_2d_both_12288x4608"] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                                              "frac": round(gbs / hbm_peak, 3)}
     status = fb.fp4_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
@@ -493,6 +506,7 @@ def main():
     ap.add_argument("--ref-feats", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="time single library calls instead of the step")
+    ap.add_argument("--only", default=None, help="with --kernels: time only the calls whose key matches this regex")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3
