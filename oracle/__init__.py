@@ -86,11 +86,11 @@ def lib() -> ctypes.CDLL:
             L.orc_global_encode_scale.argtypes = [f32, f32]
             L.orc_global_encode_scale.restype = f32
             L.orc_quantize.argtypes = [i32, i32, i32, i32, i32, u64, u32, u64, i32, f32, u32,
-                                       P, P, P, P, i64, i64, i64, i64, P, P, P, P, P]
+                                       P, P, P, P, i64, i64, i64, i64, P, P, P, P, P, i32, P]
             L.orc_quantize.restype = i32
-            L.orc_dequantize.argtypes = [i32, i32, i64, i64, P, P, f32, P]
+            L.orc_dequantize.argtypes = [i32, i32, i64, i64, P, P, f32, P, P]
             L.orc_dequantize.restype = None
-            L.orc_gemm.argtypes = [i32, i32, i64, i64, i64, P, P, f32, P, P, f32, P, P, i64, P, P]
+            L.orc_gemm.argtypes = [i32, i32, i64, i64, i64, P, P, f32, P, P, P, f32, P, P, i64, P, P]
             L.orc_gemm.restype = None
             L.orc_swizzle_scales.argtypes = [i64, i64, P, P]
             L.orc_swizzle_scales.restype = i32
@@ -201,11 +201,13 @@ def quantize(x_bits: np.ndarray, *, scale_fmt: int = FMT_E4M3, block: int = BLOC
              sr: bool = False, colwise: bool = False, rht: bool = False, seed: int = 0,
              tensor_id: int = 0, step: int = 0, held: bool = False, target_T: float = 448.0,
              refresh_every: int = 50, state: HeldState | None = None,
-             op_rows: tuple[int, int] | None = None) -> dict:
+             op_rows: tuple[int, int] | None = None, per_row: bool = False) -> dict:
     """Quantize a row-major BF16 bit array ``x_bits`` (rows x cols, uint16).
 
     Returns codes (R' x C'/2 uint8), plain scales (R' x C'/bs uint8), s_dec (float),
     amax (float) and counters (uint64[4]) for operand rows ``op_rows`` (default all).
+    With ``per_row`` each operand row has its own tensor scale ([NV] B.1's finer
+    granularity): ``s_dec_rows`` (float32 per returned row) holds them and s_dec is 0.
     """
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     rows, cols = x.shape
@@ -217,24 +219,39 @@ def quantize(x_bits: np.ndarray, *, scale_fmt: int = FMT_E4M3, block: int = BLOC
     sdec = np.zeros(1, dtype=np.float32)
     amax = np.zeros(1, dtype=np.float32)
     counters = np.zeros(4, dtype=np.uint64)
+    sdec_rows = np.zeros(r1 - r0, dtype=np.float32)
     st = state if state is not None else HeldState()
     rc = lib().orc_quantize(scale_fmt, block, int(sr), int(colwise), int(rht), seed, tensor_id, step,
                             int(held), target_T, refresh_every, _p(st.amax), _p(st.valid), _p(st.last),
                             _p(x), rows, cols, r0, r1, _p(codes), _p(scales), _p(sdec), _p(amax),
-                            _p(counters))
+                            _p(counters), int(per_row), _p(sdec_rows) if per_row else None)
     if rc != OK:
         raise OracleError(rc)
-    return {"codes": codes, "scales": scales, "s_dec": float(sdec[0]), "amax": float(amax[0]),
-            "counters": counters}
+    out = {"codes": codes, "scales": scales, "s_dec": float(sdec[0]), "amax": float(amax[0]),
+           "counters": counters}
+    if per_row:
+        out["s_dec_rows"] = sdec_rows
+    return out
 
 
-def dequantize(codes: np.ndarray, scales: np.ndarray, s_dec: float, scale_fmt: int = FMT_E4M3,
+def _sdec_arg(s_dec, n: int):
+    """A tensor decode scale (float) or one per row (array of n floats)."""
+    if np.ndim(s_dec) == 0:
+        return float(s_dec), None
+    rows = np.ascontiguousarray(s_dec, dtype=np.float32)
+    assert rows.shape == (n,)
+    return 0.0, rows
+
+
+def dequantize(codes: np.ndarray, scales: np.ndarray, s_dec, scale_fmt: int = FMT_E4M3,
                bs: int = 16) -> np.ndarray:
+    """s_dec: the tensor decode scale, or an array with one per row."""
     c = np.ascontiguousarray(codes, dtype=np.uint8)
     s = np.ascontiguousarray(scales, dtype=np.uint8)
     R, C = c.shape[0], c.shape[1] * 2
     out = np.zeros((R, C), dtype=np.float32)
-    lib().orc_dequantize(scale_fmt, bs, R, C, _p(c), _p(s), s_dec, _p(out))
+    sd, rows = _sdec_arg(s_dec, R)
+    lib().orc_dequantize(scale_fmt, bs, R, C, _p(c), _p(s), sd, _p(rows) if rows is not None else None, _p(out))
     return out
 
 
@@ -243,7 +260,8 @@ def gemm(a_codes, a_scales, a_sdec, b_codes, b_scales, b_sdec, *, scale_fmt: int
     """FP64 block-scaled GEMM C = A B^T of two K-major quantized operands.
 
     Returns (C_ref, S) where S = |alpha| sum |a b| is the error-bound scale. With
-    ``pairs=(ms, ns)`` only those outputs are computed (1-D arrays)."""
+    ``pairs=(ms, ns)`` only those outputs are computed (1-D arrays). ``a_sdec``
+    may be an array with one decode scale per row of A."""
     ac = np.ascontiguousarray(a_codes, dtype=np.uint8)
     asc = np.ascontiguousarray(a_scales, dtype=np.uint8)
     bc = np.ascontiguousarray(b_codes, dtype=np.uint8)
@@ -251,17 +269,19 @@ def gemm(a_codes, a_scales, a_sdec, b_codes, b_scales, b_sdec, *, scale_fmt: int
     M, K = ac.shape[0], ac.shape[1] * 2
     N = bc.shape[0]
     assert bc.shape[1] * 2 == K
+    sa, rows = _sdec_arg(a_sdec, M)
+    sa_rows = _p(rows) if rows is not None else None
     if pairs is None:
         c = np.zeros((M, N), dtype=np.float64)
         s = np.zeros((M, N), dtype=np.float64)
-        lib().orc_gemm(scale_fmt, bs, M, N, K, _p(ac), _p(asc), a_sdec, _p(bc), _p(bsc), b_sdec,
+        lib().orc_gemm(scale_fmt, bs, M, N, K, _p(ac), _p(asc), sa, sa_rows, _p(bc), _p(bsc), b_sdec,
                        None, None, 0, _p(c), _p(s))
     else:
         ms = np.ascontiguousarray(pairs[0], dtype=np.int64)
         ns = np.ascontiguousarray(pairs[1], dtype=np.int64)
         c = np.zeros(ms.shape[0], dtype=np.float64)
         s = np.zeros(ms.shape[0], dtype=np.float64)
-        lib().orc_gemm(scale_fmt, bs, M, N, K, _p(ac), _p(asc), a_sdec, _p(bc), _p(bsc), b_sdec,
+        lib().orc_gemm(scale_fmt, bs, M, N, K, _p(ac), _p(asc), sa, sa_rows, _p(bc), _p(bsc), b_sdec,
                        _p(ms), _p(ns), ms.shape[0], _p(c), _p(s))
     return c, s
 

@@ -349,7 +349,14 @@ float orc_global_encode_scale(float amax, float target_T) {
  * amax of this tensor; held scaling ([UE]: the amax is refreshed every
  * `refresh_every` steps and held in between) refreshes when
  * step % refresh_every == 0 or when the held state is not valid yet, and
- * otherwise uses the held amax. */
+ * otherwise uses the held amax.
+ *
+ * per_row ([NV] B.1: the global scale may span a smaller granularity, such as
+ * a row, to save the extra memory pass). Reading: each operand row r gets its
+ * own s_enc,G(r) = 6 * T / amax_r with amax_r = max |x| over that row -- B.1's
+ * formula with the tensor replaced by the row -- and s_dec,G(r) = 1 / s_enc,G(r)
+ * goes to s_dec_rows[r - op_r0]; *s_dec_out and *amax_out are set to 0. Current
+ * scaling of a plain (no RHT) rowwise 1 x 16 operand only; held must be 0. */
 int orc_quantize(int scale_fmt, int block, int sr, int colwise, int rht,
                  uint64_t seed, uint32_t tensor_id, uint64_t step,
                  int held, float target_T, uint32_t refresh_every,
@@ -357,7 +364,7 @@ int orc_quantize(int scale_fmt, int block, int sr, int colwise, int rht,
                  const uint16_t* in, int64_t rows, int64_t cols,
                  int64_t op_r0, int64_t op_r1,
                  uint8_t* codes, uint8_t* scales, float* s_dec_out, float* amax_out,
-                 uint64_t counters[4]) {
+                 uint64_t counters[4], int per_row, float* s_dec_rows) {
     int64_t R = colwise ? cols : rows, C = colwise ? rows : cols;
     int bs = (block == ORC_BLOCK_1x32) ? 32 : 16;
     int two_d = (block == ORC_BLOCK_16x16);
@@ -368,13 +375,16 @@ int orc_quantize(int scale_fmt, int block, int sr, int colwise, int rht,
     if (two_d && R % 16 != 0) return ORC_ERR_SHAPE;
     if (op_r0 < 0 || op_r1 > R || op_r0 > op_r1) return ORC_ERR_SHAPE;
     if (two_d && op_r0 % 16 != 0) return ORC_ERR_SHAPE;
+    if (per_row && (held || colwise || rht || block != ORC_BLOCK_1x16 || scale_fmt == ORC_FMT_UE8M0 ||
+                    s_dec_rows == NULL))
+        return ORC_ERR_ARG;
 
     operand_t op = {in, rows, cols, colwise};
     uint32_t signs = orc_rht_sign_word(seed);
 
     /* Tensor-level scale (B.1), current or held. */
     float s_enc_g = 1.0f, s_dec_g = 1.0f, amax_used = 0.0f;
-    if (scale_fmt != ORC_FMT_UE8M0) {
+    if (scale_fmt != ORC_FMT_UE8M0 && !per_row) {
         if (held) {
             if (refresh_every == 0) return ORC_ERR_ARG;
             if (step % refresh_every == 0 || !*st_valid) {
@@ -391,12 +401,23 @@ int orc_quantize(int scale_fmt, int block, int sr, int colwise, int rht,
         s_enc_g = orc_global_encode_scale(amax_used, target_T);
         s_dec_g = 1.0f / s_enc_g;
     }
-    *s_dec_out = s_dec_g;
+    *s_dec_out = per_row ? 0.0f : s_dec_g;
     *amax_out = amax_used;
 
     int64_t nb = C / bs;
     float fmt_max = (float)orc_scale_max(scale_fmt);
     for (int64_t r = op_r0; r < op_r1; r++) {
+        if (per_row) {
+            /* B.1 over one row: the row's amax, its encode and decode scales */
+            float amax_r = 0.0f;
+            for (int64_t c = 0; c < C; c++) {
+                float a = fabsf(operand_at(&op, r, c));
+                if (a > amax_r) amax_r = a;
+            }
+            s_enc_g = orc_global_encode_scale(amax_r, target_T);
+            s_dec_g = 1.0f / s_enc_g;
+            s_dec_rows[r - op_r0] = s_dec_g;
+        }
         for (int64_t b = 0; b < nb; b++) {
             int64_t c0 = b * bs;
             float v[32];
@@ -483,7 +504,8 @@ int orc_quantize(int scale_fmt, int block, int sr, int colwise, int rht,
 /* x~ = RN(RN(e2m1 * s_hat) * s_dec,G) in FP32; the first product is exact.    */
 /* ------------------------------------------------------------------------- */
 void orc_dequantize(int scale_fmt, int bs, int64_t R, int64_t C,
-                    const uint8_t* codes, const uint8_t* scales, float s_dec_g, float* out) {
+                    const uint8_t* codes, const uint8_t* scales, float s_dec_g, const float* s_dec_rows,
+                    float* out) {
     int64_t nb = C / bs;
     for (int64_t r = 0; r < R; r++)
         for (int64_t c = 0; c < C; c++) {
@@ -492,7 +514,7 @@ void orc_dequantize(int scale_fmt, int bs, int64_t R, int64_t C,
             float e = (float)orc_e2m1_value(code);
             float s = (float)orc_scale_decode(scale_fmt, scales[r * nb + c / bs]);
             float t = e * s;
-            out[r * C + c] = t * s_dec_g;
+            out[r * C + c] = t * (s_dec_rows != NULL ? s_dec_rows[r] : s_dec_g);
         }
 }
 
@@ -503,6 +525,8 @@ void orc_dequantize(int scale_fmt, int bs, int64_t R, int64_t C,
 /* scales are applied to the final output).                                   */
 /*                                                                            */
 /*   C[m,n] = s_dec,G,A * s_dec,G,B * sum_k (e2m1(a_mk) s_A) (e2m1(b_nk) s_B)  */
+/*   (s_dec,G,A[m] per row of A when a_sdec_rows != NULL: [NV] B.1's finer     */
+/*   granularity; a row's decode scale is constant along the dot dimension)    */
 /*   S[m,n] = |s_dec,G,A * s_dec,G,B| * sum_k |(e2m1(a_mk) s_A)(e2m1(b_nk) s_B)| */
 /*                                                                            */
 /* in binary64: every factor is exact in binary32 and every product exact in  */
@@ -533,19 +557,19 @@ static void gemm_one(int scale_fmt, int bs, int64_t K,
 }
 
 void orc_gemm(int scale_fmt, int bs, int64_t M, int64_t N, int64_t K,
-              const uint8_t* a_codes, const uint8_t* a_scales, float a_sdec,
+              const uint8_t* a_codes, const uint8_t* a_scales, float a_sdec, const float* a_sdec_rows,
               const uint8_t* b_codes, const uint8_t* b_scales, float b_sdec,
               const int64_t* ms, const int64_t* ns, int64_t npairs,
               double* c_ref, double* s_abs) {
     if (ms == NULL) {
         for (int64_t m = 0; m < M; m++)
             for (int64_t n = 0; n < N; n++)
-                gemm_one(scale_fmt, bs, K, a_codes, a_scales, a_sdec, b_codes, b_scales, b_sdec,
-                         m, n, &c_ref[m * N + n], &s_abs[m * N + n]);
+                gemm_one(scale_fmt, bs, K, a_codes, a_scales, a_sdec_rows != NULL ? a_sdec_rows[m] : a_sdec,
+                         b_codes, b_scales, b_sdec, m, n, &c_ref[m * N + n], &s_abs[m * N + n]);
     } else {
         for (int64_t i = 0; i < npairs; i++)
-            gemm_one(scale_fmt, bs, K, a_codes, a_scales, a_sdec, b_codes, b_scales, b_sdec,
-                     ms[i], ns[i], &c_ref[i], &s_abs[i]);
+            gemm_one(scale_fmt, bs, K, a_codes, a_scales, a_sdec_rows != NULL ? a_sdec_rows[ms[i]] : a_sdec,
+                     b_codes, b_scales, b_sdec, ms[i], ns[i], &c_ref[i], &s_abs[i]);
     }
 }
 

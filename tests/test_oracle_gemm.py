@@ -132,3 +132,25 @@ def test_scale_layout_positions(orc):
         plain = np.zeros((R, NB), dtype=np.uint8)
         plain[r, j] = 1
         assert np.flatnonzero(orc.swizzle_scales(plain)).tolist() == [off]
+
+
+def test_gemm_per_row_a_scale_exact_rational(orc):
+    # A's decode scale per row (B.1's finer granularity): C[m, n] = sa[m] sb sum_k a b
+    rng = np.random.default_rng(23)
+    M, N, K = 6, 5, 64
+    ac, asc = _rand_operand(rng, M, K)
+    bc, bsc = _rand_operand(rng, N, K)
+    sa = np.array([0.0123, 1.0, 2.0 ** -20, 7.25, 0.5, 3.0e4], dtype=np.float32)
+    sb = np.float32(0.375)
+    c, s = orc.gemm(ac, asc, sa, bc, bsc, float(sb))
+    A, B = _dequant64(ac, asc), _dequant64(bc, bsc)
+    for m in range(M):
+        alpha = Fraction(float(sa[m])) * Fraction(float(sb))
+        for n in range(N):
+            exact = alpha * sum(Fraction(A[m, k]) * Fraction(B[n, k]) for k in range(K))
+            sabs = abs(alpha) * sum(abs(Fraction(A[m, k]) * Fraction(B[n, k])) for k in range(K))
+            assert abs(Fraction(c[m, n]) - exact) <= Fraction(2) ** -45 * sabs
+            assert abs(Fraction(s[m, n]) - sabs) <= Fraction(2) ** -45 * sabs
+    ms, ns = np.array([5, 0, 3]), np.array([1, 4, 0])
+    cs, ss = orc.gemm(ac, asc, sa, bc, bsc, float(sb), pairs=(ms, ns))
+    assert np.array_equal(cs, c[ms, ns]) and np.array_equal(ss, s[ms, ns])

@@ -262,3 +262,58 @@ def test_argument_validation(orc):
         orc.quantize(x, scale_fmt=orc.FMT_UE8M0)                 # MX needs 1x32
     with pytest.raises(orc.OracleError):
         orc.quantize(x, rht=True, block=orc.BLOCK_16x16)
+
+
+def test_per_row_tensor_scale_is_each_rows_own_current_scale(orc):
+    # B.1's finer granularity, reading: each operand row is scaled as if it were
+    # the whole tensor. Row by row, the per-row mode must give the bytes that
+    # current tensor scaling gives the one-row tensor x[r:r+1] (RNE), and the
+    # row's s_dec must be that call's s_dec.
+    rng_rows = [random_bf16(31, (1, 96), d) for d in ("normal", "student_t4", "log_normal_1e-4_2")]
+    x = np.concatenate(rng_rows + [np.zeros((1, 96), np.uint16)], axis=0)  # last row all +0
+    q = orc.quantize(x, per_row=True)
+    assert q["s_dec"] == 0.0 and q["s_dec_rows"].shape == (4,)
+    total = np.zeros(4, dtype=np.uint64)
+    for r in range(x.shape[0]):
+        one = orc.quantize(x[r:r + 1])
+        assert np.array_equal(q["codes"][r], one["codes"][0]), r
+        assert np.array_equal(q["scales"][r], one["scales"][0]), r
+        assert np.float32(q["s_dec_rows"][r]) == np.float32(one["s_dec"]), r
+        total += one["counters"]
+    assert np.array_equal(q["counters"], total)
+    # a zero row: s_enc,G = 1 (B.1 has no amax to divide by), every code +0
+    assert q["s_dec_rows"][3] == 1.0 and not q["codes"][3].any()
+    # the row holding amax_r gets block scale T = 448 (B.1: amax_r maps to 6 * 448)
+    for r in range(3):
+        vals = np.abs(bf16_bits_to_f32(x[r]))
+        blk = int(np.argmax(vals)) // 16
+        assert e4m3_decode(q["scales"][r:r + 1, blk:blk + 1])[0, 0] == 448.0
+
+
+def test_per_row_equals_tensor_scale_when_rows_share_their_amax(orc):
+    # every row holds the same amax (one planted 8.0 per row), so each row's
+    # scale equals the tensor's: the per-row mode must reproduce current tensor
+    # scaling bit for bit, SR draws included (they index the whole operand)
+    x = random_bf16(32, (48, 64), "normal")
+    v = np.abs(bf16_bits_to_f32(x))
+    assert v.max() < 8.0
+    x[:, 5] = f32_to_bf16_bits(np.full(48, 8.0, np.float32))
+    for sr in (False, True):
+        a = orc.quantize(x, per_row=True, sr=sr, seed=9, tensor_id=2, step=4)
+        b = orc.quantize(x, sr=sr, seed=9, tensor_id=2, step=4)
+        assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["scales"], b["scales"])
+        assert np.all(a["s_dec_rows"] == np.float32(b["s_dec"]))
+        assert np.array_equal(a["counters"], b["counters"])
+    # operand-row windows see the same rows
+    w = orc.quantize(x, per_row=True, op_rows=(16, 32))
+    full = orc.quantize(x, per_row=True)
+    assert np.array_equal(w["codes"], full["codes"][16:32])
+    assert np.array_equal(w["s_dec_rows"], full["s_dec_rows"][16:32])
+
+
+def test_per_row_rejects_what_it_does_not_define(orc):
+    x = random_bf16(33, (32, 64), "normal")
+    for kw in (dict(colwise=True), dict(colwise=True, rht=True), dict(held=True),
+               dict(block=orc.BLOCK_16x16), dict(scale_fmt=orc.FMT_UE8M0, block=orc.BLOCK_1x32)):
+        with pytest.raises(orc.OracleError):
+            orc.quantize(x, per_row=True, **kw)
