@@ -415,8 +415,8 @@ def run_kernels(args):
         ts.sort()
         return ts[len(ts) // 2]
 
-    def operand(rows, cols, fmt):
-        t = fb.QTensor.empty(rows, cols, fmt)
+    def operand(rows, cols, fmt, per_row=False):
+        t = fb.QTensor.empty(rows, cols, fmt, per_row=per_row)
         t.codes.copy_(torch.randint(0, 256, t.codes.shape, dtype=torch.uint8, device="cuda"))
         lo = {fb.FP4_SCALE_E4M3: 0x30, fb.FP4_SCALE_UE5M3: 0x70, fb.FP4_SCALE_UE8M0: 0x7C}[fmt]
         t.scales.copy_(torch.randint(lo, lo + 16, t.scales.shape, dtype=torch.uint8, device="cuda"))
@@ -431,6 +431,7 @@ def run_kernels(args):
              ("nvfp4", fb.FP4_SCALE_E4M3, "12b_dgrad", (8192, 4608, 12288)),
              ("nvfp4", fb.FP4_SCALE_E4M3, "1p2b_fprop", (8192, 6144, 2048)),
              ("nvfp4", fb.FP4_SCALE_E4M3, "1p2b_dgrad", (8192, 2048, 6144)),
+             ("nvfp4_rowscale", fb.FP4_SCALE_E4M3, "1p2b_fprop", (8192, 6144, 2048)),
              ("mxfp4", fb.FP4_SCALE_UE8M0, "8b_fprop", (8192, 21504, 4096)),
              ("mxfp4", fb.FP4_SCALE_UE8M0, "1p2b_fprop", (8192, 6144, 2048)),
              ("ue5m3_emulated", fb.FP4_SCALE_UE5M3, "sweep", (8192, 4096, 4096)),
@@ -443,7 +444,7 @@ def run_kernels(args):
     for kind, fmt, name, (M, N, K) in gemms:
         if not wanted(f"gemm_{kind}_{name}_bf16"):
             continue
-        a, b = operand(M, K, fmt), operand(N, K, fmt)
+        a, b = operand(M, K, fmt, per_row=kind == "nvfp4_rowscale"), operand(N, K, fmt)
         d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         ws = torch.zeros(fb.fp4_gemm_workspace_bytes(a, b), dtype=torch.uint8, device="cuda") \
             if kind == "ue5m3_rebiased" else None
@@ -467,11 +468,16 @@ def run_kernels(args):
             round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True), x, o_r, o_c, ws=ws), 5.125),
         "mxfp4_rows": (lambda: fb.fp4_quantize(fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE8M0, block=fb.FP4_BLOCK_1x32),
                                                x, o_mx), 2.53125),
+        # per-row tensor scales: one pass, so the input is read once (2 + 0.5625 B/elem)
+        "rows_rowscale_rne": (lambda: fb.fp4_quantize(fb.QuantConfig(tscale=fb.FP4_TSCALE_ROW), x, o_rr), 2.5625),
+        "rows_rowscale_sr": (lambda: fb.fp4_quantize(fb.QuantConfig(tscale=fb.FP4_TSCALE_ROW, round=SR), x, o_rr),
+                             2.5625),
         "tensor_amax_dual_rht": (lambda: fb.fp4_tensor_amax_dual(fb.QuantConfig(), fb.QuantConfig(
             orient=fb.FP4_ORIENT_COLWISE, rht=True), x, st_r, st_c, ws), 2.0),
     }
     o_r, o_c = fb.QTensor.empty(T, C), fb.QTensor.empty(C, T)
     o_mx = fb.QTensor.empty(T, C, fb.FP4_SCALE_UE8M0)
+    o_rr = fb.QTensor.empty(T, C, per_row=True)
     st_r, st_c = fb.AmaxState(), fb.AmaxState()
     for name, (fn, bpe) in quants.items():
         if not wanted(f"quantize_{name}_{T}x{C}"):

@@ -21,6 +21,7 @@ from . import _lib
 from ._lib import (FP4_BLOCK_1x16, FP4_BLOCK_1x32, FP4_BLOCK_16x16, FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05,
                    FP4_ORIENT_COLWISE, FP4_ORIENT_ROWWISE, FP4_ROUND_RNE, FP4_ROUND_SR, FP4_SCALE_E4M3,
                    FP4_SCALE_UE5M3, FP4_SCALE_UE8M0, FP4_TSCALE_CURRENT, FP4_TSCALE_GIVEN, FP4_TSCALE_HELD,
+                   FP4_TSCALE_ROW,
                    Fp4Error)
 
 __all__ = ["QTensor", "QuantConfig", "AmaxState", "fp4_quantize", "fp4_quantize_dual", "fp4_dequantize", "fp4_gemm",
@@ -41,7 +42,8 @@ def _stream(stream) -> ctypes.c_void_p:
 @dataclass
 class QTensor:
     """A quantized operand: rows x cols E2M1 codes (cols = dot dimension),
-    block scales, and the FP32 decode tensor scale."""
+    block scales, and the FP32 decode tensor scale (one per row with per_row,
+    the output of tscale FP4_TSCALE_ROW)."""
     codes: torch.Tensor
     scales: torch.Tensor
     s_dec: torch.Tensor
@@ -50,19 +52,23 @@ class QTensor:
     scale_fmt: int = FP4_SCALE_E4M3
     block_k: int = 16
     layout: int = FP4_LAYOUT_TCGEN05
+    per_row: bool = False
 
     @staticmethod
     def empty(rows: int, cols: int, scale_fmt: int = FP4_SCALE_E4M3, layout: int = FP4_LAYOUT_TCGEN05,
-              device="cuda") -> "QTensor":
+              device="cuda", per_row: bool = False) -> "QTensor":
         bk = 32 if scale_fmt == FP4_SCALE_UE8M0 else 16
         codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
         scales = torch.empty((rows * (cols // bk),), dtype=torch.uint8, device=device)
-        s_dec = torch.empty((4,), dtype=torch.float32, device=device)  # 16 bytes keeps later buffers aligned
-        return QTensor(codes, scales, s_dec, rows, cols, scale_fmt, bk, layout)
+        # 16-byte multiples keep later buffers aligned
+        n_sdec = (rows + 3) // 4 * 4 if per_row else 4
+        s_dec = torch.empty((max(n_sdec, 4),), dtype=torch.float32, device=device)
+        return QTensor(codes, scales, s_dec, rows, cols, scale_fmt, bk, layout, per_row)
 
     def desc(self) -> _lib.fp4_tensor_t:
         return _lib.fp4_tensor_t(self.codes.data_ptr(), self.scales.data_ptr(), self.s_dec.data_ptr(),
-                                 self.rows, self.cols, self.scale_fmt, self.block_k, self.layout, 0)
+                                 self.rows, self.cols, self.scale_fmt, self.block_k, self.layout,
+                                 int(self.per_row))
 
 
 @dataclass

@@ -28,7 +28,7 @@ FP4_ERR_WORKSPACE = 8
 FP4_SCALE_E4M3, FP4_SCALE_UE5M3, FP4_SCALE_UE8M0 = 0, 1, 2
 FP4_BLOCK_1x16, FP4_BLOCK_16x16, FP4_BLOCK_1x32 = 0, 1, 2
 FP4_ROUND_RNE, FP4_ROUND_SR = 0, 1
-FP4_TSCALE_CURRENT, FP4_TSCALE_HELD, FP4_TSCALE_GIVEN = 0, 1, 2
+FP4_TSCALE_CURRENT, FP4_TSCALE_HELD, FP4_TSCALE_GIVEN, FP4_TSCALE_ROW = 0, 1, 2, 3
 FP4_ORIENT_ROWWISE, FP4_ORIENT_COLWISE = 0, 1
 FP4_LAYOUT_PLAIN, FP4_LAYOUT_TCGEN05 = 0, 1
 
@@ -51,7 +51,8 @@ class fp4_quant_params_t(ctypes.Structure):
 class fp4_tensor_t(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("s_dec_global", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("scale_fmt", ctypes.c_int32),
-                ("block_k", ctypes.c_int32), ("scale_layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("block_k", ctypes.c_int32), ("scale_layout", ctypes.c_int32),
+                ("sdec_per_row", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

@@ -76,10 +76,10 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
                             const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                             uint64_t* counters, void* ws, size_t ws_bytes, QuantJob& job) {
     if (p == nullptr || out == nullptr) return FP4_ERR_INVALID_ARG;
-    if (p->reserved != 0 || out->reserved != 0) return FP4_ERR_INVALID_ARG;
+    if (p->reserved != 0) return FP4_ERR_INVALID_ARG;
     if (p->scale_fmt < 0 || p->scale_fmt > 2 || p->block < 0 || p->block > 2) return FP4_ERR_INVALID_ARG;
     if (p->round < 0 || p->round > 1 || p->orient < 0 || p->orient > 1) return FP4_ERR_INVALID_ARG;
-    if (p->tscale < 0 || p->tscale > 2 || p->scale_layout < 0 || p->scale_layout > 1) return FP4_ERR_INVALID_ARG;
+    if (p->tscale < 0 || p->tscale > 3 || p->scale_layout < 0 || p->scale_layout > 1) return FP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0) return FP4_ERR_SHAPE;
     if (p->tensor_id == 0xFFFFFFFFu) return FP4_ERR_INVALID_ARG;
     const bool mx = p->scale_fmt == FP4_SCALE_UE8M0;
@@ -93,6 +93,12 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     if (p->emit_transpose && out_t == nullptr) return FP4_ERR_INVALID_ARG;
     const bool held = !mx && p->tscale == FP4_TSCALE_HELD;
     const bool given = !mx && p->tscale == FP4_TSCALE_GIVEN;
+    // per-row current scaling: E4M3, plain rowwise 1x16 only, into a per-row s_dec
+    const bool per_row = !mx && p->tscale == FP4_TSCALE_ROW;
+    if (out->sdec_per_row != (per_row ? 1 : 0)) return FP4_ERR_INVALID_ARG;
+    if (per_row && (p->scale_fmt != FP4_SCALE_E4M3 || p->block != FP4_BLOCK_1x16 ||
+                    p->orient != FP4_ORIENT_ROWWISE || p->rht || p->emit_transpose))
+        return FP4_ERR_UNSUPPORTED;
     if (held && (state == nullptr || p->refresh_every == 0)) return FP4_ERR_INVALID_ARG;
     if (given && state == nullptr) return FP4_ERR_INVALID_ARG;
     if (!mx && !(p->target_T > 0.0f && p->target_T <= 3.0e38f)) return FP4_ERR_INVALID_ARG;
@@ -108,7 +114,7 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     if (colwise && p->block == FP4_BLOCK_1x16 && (cols % 8 != 0)) return FP4_ERR_SHAPE;
     if (p->scale_layout == FP4_LAYOUT_TCGEN05 && (R % 128 != 0 || (C / bs) % 4 != 0)) return FP4_ERR_SHAPE;
     if (p->emit_transpose) {
-        if (out_t->reserved != 0) return FP4_ERR_INVALID_ARG;
+        if (out_t->sdec_per_row != 0) return FP4_ERR_INVALID_ARG;
         if (out_t->rows != C || out_t->cols != R) return FP4_ERR_SHAPE;
         if (out_t->scale_fmt != p->scale_fmt || out_t->block_k != 16) return FP4_ERR_INVALID_ARG;
         if (out_t->scale_layout == FP4_LAYOUT_TCGEN05 && (C % 128 != 0 || (R / 16) % 4 != 0)) return FP4_ERR_SHAPE;
@@ -134,6 +140,7 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     job.held = held || given;
     job.refresh = given ? 0 : held ? (p->step % p->refresh_every == 0) : 1;
     job.given = given;
+    job.per_row = per_row;
     job.target_T = p->target_T;
     job.tensor_id = p->tensor_id;
     job.seed = p->seed;
@@ -163,7 +170,8 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
 fp4_status_t check_operand(const fp4_tensor_t* t) {
     if (t == nullptr || t->codes == nullptr || t->scales == nullptr || t->s_dec_global == nullptr)
         return FP4_ERR_INVALID_ARG;
-    if (t->reserved != 0) return FP4_ERR_INVALID_ARG;
+    if (t->sdec_per_row != 0 && (t->sdec_per_row != 1 || t->scale_fmt != FP4_SCALE_E4M3))
+        return FP4_ERR_INVALID_ARG;
     if (!aligned16(t->codes) || !aligned16(t->scales)) return FP4_ERR_ALIGNMENT;
     return FP4_OK;
 }
@@ -224,6 +232,7 @@ fp4_status_t prepare_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d,
     const int bs = a->scale_fmt == FP4_SCALE_UE8M0 ? 32 : 16;
     if (a->scale_fmt != b->scale_fmt || a->block_k != bs || b->block_k != bs) return FP4_ERR_UNSUPPORTED;
     if (a->scale_layout != FP4_LAYOUT_TCGEN05 || b->scale_layout != FP4_LAYOUT_TCGEN05) return FP4_ERR_UNSUPPORTED;
+    if (b->sdec_per_row) return FP4_ERR_UNSUPPORTED;  // per-row decode scales on A only
     if (a->cols != b->cols) return FP4_ERR_SHAPE;
     if (a->rows % 128 != 0 || b->rows % 128 != 0 || a->cols % 256 != 0 || a->cols <= 0 || a->rows <= 0 ||
         b->rows <= 0)
@@ -232,6 +241,7 @@ fp4_status_t prepare_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d,
     j.a_codes = a->codes;
     j.a_scales = a->scales;
     j.a_sdec = a->s_dec_global;
+    j.a_sdec_rows = a->sdec_per_row != 0;
     j.b_codes = b->codes;
     j.b_scales = b->scales;
     j.b_sdec = b->s_dec_global;
@@ -309,7 +319,7 @@ struct NvtxRange {
 
 extern "C" {
 
-int fp4_abi_version(void) { return 1; }
+int fp4_abi_version(void) { return 2; }
 
 const char* fp4_status_string(fp4_status_t s) {
     switch (s) {
@@ -342,7 +352,9 @@ fp4_status_t fp4_quantized_sizes(const fp4_quant_params_t* p, int64_t rows, int6
 size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols) {
     (void)rows;
     (void)cols;
-    if (p == nullptr || p->scale_fmt == FP4_SCALE_UE8M0 || p->tscale == FP4_TSCALE_GIVEN) return 0;
+    if (p == nullptr || p->scale_fmt == FP4_SCALE_UE8M0 || p->tscale == FP4_TSCALE_GIVEN ||
+        p->tscale == FP4_TSCALE_ROW)
+        return 0;
     return (size_t)kMaxAmaxPartials * sizeof(float);
 }
 
@@ -388,6 +400,7 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
     if (p_row->block != FP4_BLOCK_1x16 || p_col->block != FP4_BLOCK_1x16) return FP4_ERR_UNSUPPORTED;
     if (p_row->scale_fmt != p_col->scale_fmt || p_row->scale_fmt == FP4_SCALE_UE8M0) return FP4_ERR_UNSUPPORTED;
     if (p_row->round != p_col->round || p_row->tscale != p_col->tscale) return FP4_ERR_UNSUPPORTED;
+    if (p_row->tscale == FP4_TSCALE_ROW) return FP4_ERR_UNSUPPORTED;  // a colwise row is a whole column
     if (p_row->tscale == FP4_TSCALE_HELD && p_row->refresh_every != p_col->refresh_every) return FP4_ERR_UNSUPPORTED;
     if (p_row->step != p_col->step) return FP4_ERR_UNSUPPORTED;
     if (p_row->scale_layout != FP4_LAYOUT_TCGEN05 || p_col->scale_layout != FP4_LAYOUT_TCGEN05)
@@ -458,7 +471,7 @@ fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void
     if (t->block_k != bs || t->rows < 0 || t->cols % bs != 0) return FP4_ERR_SHAPE;
     if (t->scale_layout == FP4_LAYOUT_TCGEN05 && (t->rows % 128 != 0 || (t->cols / bs) % 4 != 0))
         return FP4_ERR_SHAPE;
-    DequantJob j{t->codes, t->scales, t->s_dec_global, t->rows, t->cols, t->scale_fmt, bs,
+    DequantJob j{t->codes, t->scales, t->s_dec_global, t->sdec_per_row != 0, t->rows, t->cols, t->scale_fmt, bs,
                  t->scale_layout, out, out_fp32 != 0};
     return from_cuda(launch_dequantize(j, static_cast<cudaStream_t>(stream)));
 }

@@ -72,6 +72,7 @@ struct GemmParams {
     const int8_t* b_off;
     const uint8_t* rb_flags;  // rebiased UE5M3: return at once when any of the rb_nflags bytes is set
     int64_t rb_nflags;
+    int a_sdec_rows;          // a_sdec holds one decode scale per row of A (App. B.1, per-row scaling)
 };
 
 // 256-bit global store (sm_100+), 32-byte aligned destination.
@@ -327,7 +328,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int half = (warp - Cfg::FIRST_EPI_WARP) >> 2;  // which 128 of the BN columns
         uint8_t* ebox = smem + Cfg::OFF_EPI + (warp - Cfg::FIRST_EPI_WARP) * Cfg::EPI_BOX_BYTES;
         const uint32_t ebox_s = sb + Cfg::OFF_EPI + (uint32_t)((warp - Cfg::FIRST_EPI_WARP) * Cfg::EPI_BOX_BYTES);
-        const float alpha = Cfg::MX ? 1.0f : __fmul_rn(*p.a_sdec, *p.b_sdec);
+        // alpha = s_dec,G,A * s_dec,G,B; with per-row A scales it is formed per row (m) below
+        const bool alpha_rows = !Cfg::MX && p.a_sdec_rows;
+        const float alpha_tensor = Cfg::MX ? 1.0f : alpha_rows ? 0.0f : __fmul_rn(*p.a_sdec, *p.b_sdec);
+        const float b_sdec = alpha_rows ? *p.b_sdec : 0.0f;
         const int nchunks = (num_k + Cfg::CHUNK_STAGES - 1) / Cfg::CHUNK_STAGES;
         uint32_t chunk = 0;
         bool ok = true;
@@ -363,6 +367,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (!ok) break;
             const int64_t m = mb * Cfg::BM + q * 32 + lane;
             const int64_t n0 = nb * Cfg::BN + half * Cfg::EPI_COLS;
+            const float alpha = alpha_rows ? __fmul_rn(p.a_sdec[m], b_sdec) : alpha_tensor;
             if (Cfg::RB) {
                 // undo the rebias: times 2^(a_off[m] + b_off[n]), a power of two,
                 // so each sum equals the one over the UE5M3-scaled products
@@ -543,7 +548,7 @@ cudaError_t run_nvfp4(const GemmJob& j, cudaStream_t st) {
     if (!make_tmap_u8_swizzled(&tb, j.b_codes, j.N, j.K / 2, Cfg::BN, Cfg::ROW_BYTES)) return cudaErrorInvalidValue;
     if (!make_tmap_out(&td, j.d, j.M, j.N, OUT32, Cfg::EPI_ROW_BYTES)) return cudaErrorInvalidValue;
     GemmParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status,
-                 j.a_off, j.b_off, j.rb_flags, j.rb_nflags};
+                 j.a_off, j.b_off, j.rb_flags, j.rb_nflags, j.a_sdec_rows};
     auto kern = gemm_nvfp4_kernel<Cfg, OUT32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;

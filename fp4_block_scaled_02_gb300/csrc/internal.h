@@ -51,6 +51,7 @@ struct QuantJob {
     int held;           // held-amax tensor scale (also set for a given amax)
     int refresh;        // held: this step refreshes the amax
     int given;          // the amax is the state's, computed ahead (FP4_TSCALE_GIVEN)
+    int per_row;        // one tensor scale per operand row (FP4_TSCALE_ROW), s_dec[rows]
     float target_T;
     uint32_t tensor_id;
     uint64_t seed;
@@ -95,6 +96,7 @@ struct DequantJob {
     const uint8_t* codes;
     const uint8_t* scales;
     const float* s_dec;
+    int s_dec_rows;     // s_dec holds one float per row
     int64_t rows, cols;
     int scale_fmt, block_k, layout;
     void* out;
@@ -107,6 +109,7 @@ struct GemmJob {
     const uint8_t* a_codes;
     const uint8_t* a_scales;
     const float* a_sdec;
+    int a_sdec_rows;    // a_sdec holds one float per row of A
     const uint8_t* b_codes;
     const uint8_t* b_scales;
     const float* b_sdec;

@@ -163,16 +163,17 @@ __device__ __forceinline__ void fill_enc_table(float* tab, float s_dec) {
 // pre * s_enc,L unless s_enc,L < 2^-124, where the two products are taken
 // apart. vmax is max |v[i]|, any_zero whether some v[i] is +-0; enc_tab holds
 // s_enc,L per scale code (fill_enc_table). `c0` = (index of element 0) / 8, the
-// first of the block's two SR counters.
+// first of the block's two SR counters. DIRECT: no table; s_enc,L is formed
+// from `s_dec` for this block alone (the expression fill_enc_table uses).
 // Event counts: scale saturation and underflow; element saturation, counted
 // per element only when the scaled block max exceeds 6 (rounding is monotone,
 // so otherwise no element can); element underflow = zero-magnitude codes minus
 // zero inputs.
-template <int FMT, bool SR, bool RHT>
+template <int FMT, bool SR, bool RHT, bool DIRECT = false>
 __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vmax, bool any_zero,
                                                      const float* enc_tab, float s_enc, uint64_t c0, const QParams& q,
                                                      uint32_t smask_lo, uint32_t smask_hi, uint32_t& lo, uint32_t& hi,
-                                                     Counts& cnt) {
+                                                     Counts& cnt, float s_dec = 0.0f) {
     using F = ScaleFmt<FMT>;
     const float amax_b = RHT ? __fmul_rn(vmax, 0.25f) : vmax;
     const float s = __fmul_rn(div6_rn(amax_b), s_enc);
@@ -190,7 +191,7 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vm
         hi = sign_nibbles8(v + 8) ^ smask_hi;
         return 0u;
     }
-    const float enc_l = enc_tab[sc];
+    const float enc_l = DIRECT ? __frcp_rn(__fmul_rn(F::decode(sc), s_dec)) : enc_tab[sc];
     float x[16];
     float xmax;
     if (!RHT || enc_l >= 0x1p-124f) {
@@ -360,6 +361,92 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
                 }
             } else if (active) {
                 q.scales[b] = (uint8_t)sc;
+            }
+        }
+    }
+    flush_counters(q.counters, cnt.esat, cnt.eunder, cnt.ssat, cnt.sunder);
+}
+
+// ----------------------------------------------------------------------------
+// K2r: rowwise 1x16 quantizer with one tensor scale per operand row (App. B.1:
+// the global scale at the granularity of a row, so that current scaling needs
+// no separate amax pass). A warp owns whole rows: it takes the row's amax
+// (max |bf16| as 16-bit integers, eight 16-byte loads in flight per lane),
+// forms s_enc,G(r) and s_dec,G(r) exactly as the tensor-wide scale is formed,
+// then converts the row's blocks as the rowwise kernel does, re-reading the row
+// from cache (one pass over memory). With no table per row, each block forms
+// its s_enc,L directly.
+template <int FMT, bool SR, bool TCL>
+__global__ void __launch_bounds__(kThreads) quantize_rows_rowscale_kernel(QParams q) {
+    pdl_begin();
+    const int64_t nb_row = q.cols / 16, n_vec = q.cols / 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    Counts cnt;
+    for (int64_t r = warp; r < q.rows; r += nwarps) {
+        const uint4* row = reinterpret_cast<const uint4*>(q.in + r * q.cols);
+        uint32_t m = 0u;
+        int64_t i = lane;
+        for (; i + 32 * (kAmaxVec - 1) < n_vec; i += 32 * kAmaxVec) {
+            uint4 v[kAmaxVec];
+#pragma unroll
+            for (int k = 0; k < kAmaxVec; ++k) v[k] = __ldg(row + i + 32 * k);
+#pragma unroll
+            for (int k = 0; k < kAmaxVec; ++k)
+                m = __vmaxu2(m, __vmaxu2(__vmaxu2(v[k].x & 0x7FFF7FFFu, v[k].y & 0x7FFF7FFFu),
+                                         __vmaxu2(v[k].z & 0x7FFF7FFFu, v[k].w & 0x7FFF7FFFu)));
+        }
+        for (; i < n_vec; i += 32) {
+            const uint4 a = __ldg(row + i);
+            m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                     __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+        }
+        m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float amax = __uint_as_float(m << 16);
+        const float s_enc = global_encode_scale(amax, q.target_T);
+        const float s_dec = __fdiv_rn(1.0f, s_enc);
+        if (lane == 0) q.s_dec[r] = s_dec;
+        for (int64_t base = 0; base < nb_row; base += 64) {
+            uint4 in[2][2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t j = base + 32 * u + lane;
+                if (j < nb_row) {
+                    in[u][0] = ldg16(q.in + r * q.cols + 16 * j);
+                    in[u][1] = ldg16(q.in + r * q.cols + 16 * j + 8);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t j = base + 32 * u + lane;
+                const int64_t b = r * nb_row + j;  // flat block index
+                const bool active = j < nb_row;
+                uint32_t sc = 0u;
+                if (active) {
+                    const uint4 a = in[u][0], c = in[u][1];
+                    const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+                    bool any_zero;
+                    const float vmax = amax_bf16x16(w, any_zero);
+                    float v[16];
+                    unpack16(a, c, v);
+                    uint32_t lo, hi;
+                    sc = quantize_block16<FMT, SR, false, true>(v, vmax, any_zero, nullptr, s_enc, (uint64_t)(2 * b), q,
+                                                                0u, 0u, lo, hi, cnt, s_dec);
+                    *reinterpret_cast<uint2*>(q.codes + 8 * b) = make_uint2(lo, hi);
+                }
+                if (TCL) {
+                    // lanes 4k..4k+3 hold the four adjacent scale bytes of this row
+                    uint32_t w = sc << (8 * (lane & 3));
+                    w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+                    w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+                    if (active && (lane & 3) == 0)
+                        *reinterpret_cast<uint32_t*>(q.scales + tc_scale_offset(r, j, nb_row)) = w;
+                } else if (active) {
+                    q.scales[b] = (uint8_t)sc;
+                }
             }
         }
     }
@@ -802,14 +889,15 @@ __global__ void __launch_bounds__(kThreads) quantize_mx_rows_kernel(QParams q) {
 template <int FMT, int BS, bool TCL, bool OUT32>
 __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
                                                               const uint8_t* __restrict__ scales,
-                                                              const float* __restrict__ s_dec_p, int64_t rows,
-                                                              int64_t cols, void* __restrict__ out) {
+                                                              const float* __restrict__ s_dec_p, int s_dec_rows,
+                                                              int64_t rows, int64_t cols, void* __restrict__ out) {
     pdl_begin();
-    const float s_dec = *s_dec_p;
+    const float s_dec0 = s_dec_rows ? 0.0f : *s_dec_p;
     const int64_t nb_row = cols / BS, nblk = rows * nb_row;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride) {
         const int64_t r = b / nb_row, j = b % nb_row;
+        const float s_dec = s_dec_rows ? s_dec_p[r] : s_dec0;
         const uint32_t sc = scales[TCL ? tc_scale_offset(r, j, nb_row) : b];
         float s_hat;
         if constexpr (FMT == kFmtUE8M0) s_hat = exp2_exact((int)sc - 127);
@@ -1295,7 +1383,7 @@ QParams make_params(const QuantJob& j) {
 }  // namespace
 
 int amax_partials_needed(const QuantJob& j) {
-    if (j.scale_fmt == kFmtUE8M0 || j.given) return 0;
+    if (j.scale_fmt == kFmtUE8M0 || j.given || j.per_row) return 0;
     if (j.rows == 0 || j.cols == 0) return 0;
     return amax_grid(j);  // held non-refresh steps too: the state may not be valid yet
 }
@@ -1308,6 +1396,16 @@ cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
         const int grid = grid_for(j.rows * (j.cols / 32), 8);
         if (j.layout == FP4_LAYOUT_TCGEN05) (void)launch_pdl(quantize_mx_rows_kernel<true>, grid, kThreads, 0, st, q);
         else (void)launch_pdl(quantize_mx_rows_kernel<false>, grid, kThreads, 0, st, q);
+        return cudaGetLastError();
+    }
+    if (j.per_row) {
+        // one warp per operand row (E4M3, rowwise 1x16: checked by the caller)
+        const int grid = grid_for(j.rows * 32, 8);
+        const bool tcl = j.layout == FP4_LAYOUT_TCGEN05;
+#define FP4_ROWSCALE(SR, TCL) launch_pdl(quantize_rows_rowscale_kernel<kFmtE4M3, SR, TCL>, grid, kThreads, 0, st, q)
+        if (j.sr) { if (tcl) FP4_ROWSCALE(true, true); else FP4_ROWSCALE(true, false); }
+        else { if (tcl) FP4_ROWSCALE(false, true); else FP4_ROWSCALE(false, false); }
+#undef FP4_ROWSCALE
         return cudaGetLastError();
     }
     // pass 1 (current scaling, or a held-amax refresh step): amax partials
@@ -1333,11 +1431,11 @@ cudaError_t launch_dequantize(const DequantJob& j, cudaStream_t st) {
 #define FP4_DQ(FMT, BS)                                                                                           \
     do {                                                                                                          \
         if (tcl) {                                                                                                \
-            if (j.out_fp32) (void)launch_pdl(dequantize_kernel<FMT, BS, true, true>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
-            else (void)launch_pdl(dequantize_kernel<FMT, BS, true, false>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            if (j.out_fp32) (void)launch_pdl(dequantize_kernel<FMT, BS, true, true>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.s_dec_rows, j.rows, j.cols, j.out); \
+            else (void)launch_pdl(dequantize_kernel<FMT, BS, true, false>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.s_dec_rows, j.rows, j.cols, j.out); \
         } else {                                                                                                  \
-            if (j.out_fp32) (void)launch_pdl(dequantize_kernel<FMT, BS, false, true>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
-            else (void)launch_pdl(dequantize_kernel<FMT, BS, false, false>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.rows, j.cols, j.out); \
+            if (j.out_fp32) (void)launch_pdl(dequantize_kernel<FMT, BS, false, true>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.s_dec_rows, j.rows, j.cols, j.out); \
+            else (void)launch_pdl(dequantize_kernel<FMT, BS, false, false>, grid, kThreads, 0, st, j.codes, j.scales, j.s_dec, j.s_dec_rows, j.rows, j.cols, j.out); \
         }                                                                                                         \
     } while (0)
     if (j.scale_fmt == kFmtE4M3) FP4_DQ(kFmtE4M3, 16);

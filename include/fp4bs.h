@@ -74,8 +74,19 @@ typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_round_t;
  * step % refresh_every == 0 or when the held state is not valid yet (UE5M3
  * page: refresh every 50 steps; other steps use the held amax: HELD), or the
  * amax a previous fp4_tensor_amax call left in the state record (GIVEN: the
- * same bytes as CURRENT without the call's own amax pass). */
-typedef enum { FP4_TSCALE_CURRENT = 0, FP4_TSCALE_HELD = 1, FP4_TSCALE_GIVEN = 2 } fp4_tscale_t;
+ * same bytes as CURRENT without the call's own amax pass). ROW: current
+ * scaling per operand row, the finer granularity App. B.1 suggests to save the
+ * extra memory pass: row r of the operand gets s_enc,G(r) = 6 T / amax_r from
+ * its own amax, computed in the same single pass that converts it, and
+ * s_dec,G(r) goes to s_dec_global[r]. ROW needs E4M3 scales, 1x16 blocks,
+ * ROWWISE without RHT, an output with sdec_per_row set (s_dec_global holding
+ * rows floats) and no workspace; fp4_quantize_dual does not take it. */
+typedef enum {
+    FP4_TSCALE_CURRENT = 0,
+    FP4_TSCALE_HELD = 1,
+    FP4_TSCALE_GIVEN = 2,
+    FP4_TSCALE_ROW = 3
+} fp4_tscale_t;
 
 /* ROWWISE: the operand is the input itself (blocks run along its columns).
  * COLWISE: the operand is the input's transpose (blocks run along the input's
@@ -110,17 +121,18 @@ typedef struct {
 
 /* A quantized operand: rows x cols E2M1 codes, K-major, element 2i of a row in
  * the low nibble of byte i; block scales; and the FP32 decode tensor scale
- * s_dec,G (App. B.1; 1.0 for UE8M0). */
+ * s_dec,G (App. B.1; 1.0 for UE8M0), one for the tensor or one per row. */
 typedef struct {
     uint8_t* codes;          /* rows * cols / 2 bytes */
     uint8_t* scales;         /* rows * cols / block_k bytes */
-    float* s_dec_global;     /* one float */
+    float* s_dec_global;     /* one float, or rows floats with sdec_per_row */
     int64_t rows;
     int64_t cols;            /* dot-product dimension */
     int32_t scale_fmt;       /* fp4_scale_fmt_t */
     int32_t block_k;         /* 16 or 32: scale block length along cols */
     int32_t scale_layout;    /* fp4_scale_layout_t */
-    int32_t reserved;        /* must be 0 */
+    int32_t sdec_per_row;    /* 0: one s_dec,G; 1: s_dec_global[r] per row
+                                (FP4_TSCALE_ROW outputs; E4M3 only) */
 } fp4_tensor_t;
 
 /* Held-amax record of one tensor (device memory, 16 bytes, zero-initialised by
@@ -218,13 +230,16 @@ fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_qua
 
 /* Decode an operand back to real values, x = e2m1 * s_hat * s_dec,G computed as
  * RN(RN(e2m1 * s_hat) * s_dec,G) in FP32 (section A3; App. B.3), written as
- * rows x cols BF16 (out_fp32 == 0) or FP32. */
+ * rows x cols BF16 (out_fp32 == 0) or FP32; with sdec_per_row, row r takes
+ * s_dec_global[r]. */
 fp4_status_t fp4_dequantize(const fp4_tensor_t* t, void* out, int out_fp32, void* stream);
 
 /* Block-scaled GEMM D[M x N] = s_dec,G,A * s_dec,G,B * sum_k (a_mk s_A)(b_nk s_B)
  * with FP32 accumulation ("Pretraining LLMs with NVFP4", App. B.3; A3 hardware
  * support). A is M x K, B is N x K, both quantized, K-major, TCGEN05 scale
- * layout, same scale format. E4M3 (block 16) runs natively (tcgen05
+ * layout, same scale format. A may carry one s_dec,G per row (sdec_per_row,
+ * E4M3 only: output row m is scaled by s_dec,G,A[m] * s_dec,G,B); B may not
+ * (FP4_ERR_UNSUPPORTED). E4M3 (block 16) runs natively (tcgen05
  * kind::mxf4nvf4); UE8M0 (MXFP4, block 32, section A3) runs natively too
  * (tcgen05 kind::mxf4) with alpha = 1: MXFP4 has no tensor scale, so its
  * s_dec_global is not read; UE5M3 (block 16) runs the software-emulated path

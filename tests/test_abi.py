@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.fp4_abi_version() == 1
+    assert lib.fp4_abi_version() == 2
     for s in range(9):
         assert lib.fp4_status_string(s)
     assert lib.fp4_status_string(0) == b"ok"
