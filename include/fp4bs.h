@@ -149,7 +149,8 @@ fp4_status_t fp4_quantized_sizes(const fp4_quant_params_t* p, int64_t rows, int6
                                  size_t* codes_bytes, size_t* scales_bytes);
 
 /* Device workspace bytes fp4_quantize needs (the per-CTA amax partials of the
- * amax pass); 0 when no amax pass runs (UE8M0). Host only. */
+ * amax pass); 0 when no amax pass runs (UE8M0, FP4_TSCALE_GIVEN, FP4_TSCALE_ROW).
+ * Host only. */
 size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols);
 
 /* Quantize a row-major BF16 input `in_bf16` (rows x cols) into `out`

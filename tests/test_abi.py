@@ -80,3 +80,38 @@ def test_argument_checks_return_before_any_launch(lib):
     a.rows = 128
     a.scale_fmt = L.FP4_SCALE_UE8M0
     assert lib.fp4_gemm(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(16), 1, 0, None) == L.FP4_ERR_UNSUPPORTED
+
+
+def test_per_row_scale_argument_rules_without_gpu(lib):
+    # FP4_TSCALE_ROW (App. B.1's per-row global scale): rowwise E4M3 1x16 into an
+    # output flagged sdec_per_row, no workspace; everything else refused before
+    # any launch
+    from fp4_block_scaled_02_gb300 import _lib as L
+    p = L.fp4_quant_params_t(0, 0, 0, 0, 0, L.FP4_TSCALE_ROW, 448.0, 50, 0, 1, 0, 0, 0, 0)
+    assert lib.fp4_workspace_bytes(ctypes.byref(p), 256, 512) == 0
+    flat = L.fp4_tensor_t(16, 16, 16, 128, 64, 0, 16, 1, 0)
+    rows = L.fp4_tensor_t(16, 16, 16, 128, 64, 0, 16, 1, 1)
+
+    def q(params, out, r=128, c=64):
+        return lib.fp4_quantize(ctypes.byref(params), ctypes.c_void_p(16), r, c, ctypes.byref(out), None, None,
+                                None, None, 0, None)
+    assert q(p, flat) == L.FP4_ERR_INVALID_ARG            # ROW needs a per-row s_dec output
+    cur = L.fp4_quant_params_t(0, 0, 0, 0, 0, L.FP4_TSCALE_CURRENT, 448.0, 50, 0, 1, 0, 0, 0, 0)
+    assert q(cur, rows) == L.FP4_ERR_INVALID_ARG          # and only ROW writes one
+    p.orient = L.FP4_ORIENT_COLWISE
+    colrows = L.fp4_tensor_t(16, 16, 16, 64, 128, 0, 16, 1, 1)
+    assert q(p, colrows) == L.FP4_ERR_UNSUPPORTED         # a colwise row spans the whole tensor
+    p.orient = L.FP4_ORIENT_ROWWISE
+    p.scale_fmt = rows.scale_fmt = L.FP4_SCALE_UE5M3
+    assert q(p, rows) == L.FP4_ERR_UNSUPPORTED            # E4M3 only
+    p.tscale = 4
+    assert q(p, rows) == L.FP4_ERR_INVALID_ARG            # no such mode
+    # GEMM: per-row decode scales on A only, E4M3 only
+    a = L.fp4_tensor_t(16, 16, 16, 128, 256, 0, 16, 1, 1)
+    b = L.fp4_tensor_t(16, 16, 16, 128, 256, 0, 16, 1, 1)
+    assert lib.fp4_gemm(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(16), 1, 0, None) == L.FP4_ERR_UNSUPPORTED
+    b.sdec_per_row = 2
+    assert lib.fp4_gemm(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(16), 1, 0, None) == L.FP4_ERR_INVALID_ARG
+    b.sdec_per_row = 0
+    a.scale_fmt = b.scale_fmt = L.FP4_SCALE_UE5M3
+    assert lib.fp4_gemm(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(16), 1, 0, None) == L.FP4_ERR_INVALID_ARG
