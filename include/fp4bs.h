@@ -6,7 +6,8 @@
  * "Pretraining Large Language Models with NVFP4" (arXiv 2509.25149) and the
  * UE5M3 block-scale paper summarised at arXiv 2609.02846 describe it:
  *   - a quantizer: tensor amax -> FP32 tensor scale (App. B.1; or a held amax
- *     refreshed every N steps), per-block scale (App. B.2) in E4M3, UE5M3 or
+ *     refreshed every N steps, or one scale per operand row, the finer
+ *     granularity B.1 suggests), per-block scale (App. B.2) in E4M3, UE5M3 or
  *     UE8M0, E2M1 conversion with round-to-nearest-even or stochastic rounding
  *     (App. B.3, section 4.4), optional 16x16 random Hadamard transform on the
  *     Wgrad operands (section 4.2, App. C), 2D 16x16 weight scaling (4.3);
