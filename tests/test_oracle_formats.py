@@ -113,6 +113,26 @@ def test_e2m1_sr_thresholds_worked_by_hand(orc):
     assert orc.e2m1_sr(6.0, 0) == 7 and orc.e2m1_sr(-7.0, 0) == 15 and orc.e2m1_sr(1e30, 0) == 7
 
 
+def test_e2m1_sr_probability_by_enumerating_every_draw(orc):
+    # 4.4: rounding up with probability proportional to the distance from the lower
+    # neighbour. Over all 2^16 draws exactly floor(frac * 2^16) must round up, for
+    # fractions that 16 bits hold exactly and for ones they truncate (1/3, 1/7, ...).
+    from fractions import Fraction
+    cases = [(1.25, 1.0, 1.5), (0.3046875, 0.0, 0.5), (5.5, 4.0, 6.0),
+             (1.0 + 1.0 / 6.0, 1.0, 1.5), (2.0 + 1.0 / 7.0, 2.0, 3.0), (0.5 + 1.0 / 3.0 / 2.0, 0.5, 1.0),
+             (4.0 + 2.0 ** -15, 4.0, 6.0), (2.0 ** -18, 0.0, 0.5)]
+    for v, lo, hi in cases:
+        v32 = float(np.float32(v))
+        frac = (Fraction(v32) - Fraction(lo)) / (Fraction(hi) - Fraction(lo))
+        want = int(frac * 65536)  # floor
+        lo_code = E2M1_SET.index(lo)  # the page's value set, in code order
+        codes = np.array([orc.e2m1_sr(v32, r) for r in range(65536)])
+        assert set(np.unique(codes)) <= {lo_code, lo_code + 1}
+        assert int(np.sum(codes == lo_code + 1)) == want, (v, want)
+        # the draws that round up are the top ones: R >= 2^16 - floor(frac * 2^16)
+        assert np.all(codes[65536 - want:] == lo_code + 1) and np.all(codes[:65536 - want] == lo_code)
+
+
 def _brute_nearest(s: float, table: list[float]) -> int:
     """Index of the nearest table value, ties to the even index, saturating."""
     if s >= table[-1]:
