@@ -144,6 +144,34 @@ def test_gemm_zero_operand_gives_zero():
     assert torch.count_nonzero(d).item() == 0
 
 
+@pytest.mark.parametrize("K", [2048, 8192, 21504])
+def test_gemm_all_positive_products_within_bound(K):
+    """All-positive products are the worst case for an accumulator that loses
+    low bits as it adds: the losses never cancel. With every code positive and
+    block scales near 1, each output's partial sums grow monotonically over K,
+    and the FP32 result must still lie within 2^-20 * sum |a b| of the exact sum
+    (App. B.3: FP32 accumulation of the block-scaled products). K runs up to
+    21504, the longest dot product of the workloads (the 8B down-projection's
+    Fprop and its up-projection's Dgrad)."""
+    M, N = 256, 256
+    rng = np.random.default_rng(K)
+
+    def positive_operand(rows):
+        c = rng.integers(1, 8, size=(rows, K), dtype=np.uint8)  # E2M1 magnitudes 0.5 .. 6
+        codes = (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+        scales = rng.integers(0x34, 0x3C, size=(rows, K // 16), dtype=np.uint8)  # E4M3 0.625 .. 1.75
+        return {"codes": codes, "scales": scales, "s_dec": 1.0}
+
+    ra, rb = positive_operand(M), positive_operand(N)
+    a, b = upload_operand(ra, M, K), upload_operand(rb, N, K)
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    fb.fp4_gemm(a, b, d)
+    assert fb.fp4_device_status() == 0
+    c_ref, s = oracle.gemm(ra["codes"], ra["scales"], 1.0, rb["codes"], rb["scales"], 1.0)
+    assert np.all(c_ref > 0)
+    _check(d.cpu().numpy(), c_ref, s, bf16=False)
+
+
 def test_gemm_shape_validation():
     _, a = _operand(39, 128, 256, "normal")
     _, b = _operand(40, 128, 256, "normal")
@@ -182,9 +210,11 @@ def _linear_end_to_end(w, which=0, fmt=fb.FP4_SCALE_E4M3, rht=True, sample=None)
     for k, (cfg, bits) in cfgs.items():
         refs[k] = oracle_quantize(cfg, bits)
         assert_quant_equal(b[k], refs[k], fb.FP4_LAYOUT_TCGEN05)
+    # one counter row per tensor id: X, X^T, W (both orientations, each element
+    # once), dY, dY^T
     counters = L.counters.cpu().numpy()
-    assert counters[0].tolist() == refs["x"]["counters"].tolist()
-    assert counters[4].tolist() == refs["dyt"]["counters"].tolist()
+    for row, key in enumerate(("x", "xt", "w", "dy", "dyt")):
+        assert counters[row].tolist() == refs[key]["counters"].tolist(), key
     for out, (ka, kb), bf16 in [(y, ("x", "w"), True), (dx, ("dy", "wt"), True), (dw, ("dyt", "xt"), False)]:
         ra, rb = refs[ka], refs[kb]
         if sample is None:
@@ -337,7 +367,7 @@ def test_ue5m3_periodic_scaling_sweep_steps(T_target, native):
     y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
     dx = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
     dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
-    states = {k: oracle.HeldState() for k in ("x", "w", "dy", "xt", "dyt")}
+    states = {k: oracle.HeldState() for k in ("x", "w", "wt", "dy", "xt", "dyt")}
     rng = np.random.default_rng(3)
     for step in (0, 49, 50, 99):
         dyb = sweep_dy(inp["dy"], step, w.steps)
@@ -347,6 +377,8 @@ def test_ue5m3_periodic_scaling_sweep_steps(T_target, native):
         cfgs = {
             "x": (L._cfg(0, step), inp["x"], 0),
             "w": (L._cfg(2, step, block=fb.FP4_BLOCK_16x16), inp["w"], 2),
+            # W^T shares W's quantize call, held amax and counter row
+            "wt": (L._cfg(2, step, block=fb.FP4_BLOCK_16x16, orient=fb.FP4_ORIENT_COLWISE), inp["w"], None),
             "dy": (L._cfg(3, step, round=fb.FP4_ROUND_SR), dyb, 3),
             "xt": (L._cfg(1, step, orient=fb.FP4_ORIENT_COLWISE), inp["x"], 1),
             "dyt": (L._cfg(4, step, orient=fb.FP4_ORIENT_COLWISE, round=fb.FP4_ROUND_SR), dyb, 4),
@@ -355,11 +387,13 @@ def test_ue5m3_periodic_scaling_sweep_steps(T_target, native):
         for k, (cfg, bits, ci) in cfgs.items():
             refs[k] = oracle_quantize(cfg, bits, state=states[k])
             assert_quant_equal(L.bufs[k], refs[k], fb.FP4_LAYOUT_TCGEN05)
+            if ci is None:
+                continue
             assert L.counters[ci].cpu().numpy().tolist() == refs[k]["counters"].tolist(), (step, k)
             gst = L.states[ci]
             assert np.float32(gst.amax) == states[k].amax[0] and gst.last_refresh_step == int(states[k].last[0])
         ms, ns = rng.integers(0, T, 1500), rng.integers(0, N, 1500)
-        for out, (ka, kb), bf16 in [(y, ("x", "w"), True), (dw, ("dyt", "xt"), False)]:
+        for out, (ka, kb), bf16 in [(y, ("x", "w"), True), (dx, ("dy", "wt"), True), (dw, ("dyt", "xt"), False)]:
             ra, rb = refs[ka], refs[kb]
             mm = ms % out.shape[0]
             nn = ns % out.shape[1]
@@ -368,11 +402,13 @@ def test_ue5m3_periodic_scaling_sweep_steps(T_target, native):
             _check(out.float().cpu().numpy()[mm, nn], c_ref, s, bf16)
 
 
-def _banded_linear(w, which, band=128, samples=2000):
+def _banded_linear(w, which, band=128, samples=1000):
     """Full-size linear of a large workload: the GPU runs the whole recipe; the
-    oracle quantizes one band of `band` operand rows of every operand (the
-    tensor amax still covers the whole tensor), those bytes must match the GPU's
-    exactly, and GEMM outputs sampled inside the bands must meet the bound."""
+    oracle quantizes three bands of `band` operand rows of every operand -- the
+    first, the last and one at random (the tensor amax still covers the whole
+    tensor) -- whose bytes must match the GPU's exactly, and GEMM outputs sampled
+    where the bands cross must meet the bound: in the first output tile, in the
+    last one (past the first persistent wave of tiles) and in a random one."""
     inp = linear_inputs(w, which)
     lin = w.linears[which]
     T, K, N = lin.tokens, lin.k_in, lin.n_out
@@ -394,28 +430,31 @@ def _banded_linear(w, which, band=128, samples=2000):
     }
     refs, r0s = {}, {}
     for k, (cfg, bits, R) in cfgs.items():
-        r0 = int(rng.integers(0, R // band)) * band
-        r0s[k] = r0
-        ref = oracle.quantize(bits, scale_fmt=oracle.FMT_E4M3,
-                              block=oracle.BLOCK_16x16 if cfg.block == fb.FP4_BLOCK_16x16 else oracle.BLOCK_1x16,
-                              sr=cfg.round == fb.FP4_ROUND_SR, colwise=cfg.orient == fb.FP4_ORIENT_COLWISE,
-                              rht=cfg.rht, seed=cfg.seed, tensor_id=cfg.tensor_id, step=0,
-                              op_rows=(r0, r0 + band))
-        refs[k] = ref
+        r0s[k] = [0, R - band, int(rng.integers(1, R // band - 1)) * band]
+        refs[k] = []
         q = L.bufs[k]
-        assert np.array_equal(q.codes[r0:r0 + band].cpu().numpy(), ref["codes"]), k
-        # scales of the band: the band is one 128-row tile of the tensor-core layout
         nb = q.cols // 16
-        got = q.scales.view(-1, nb * 128)[r0 // 128].cpu().numpy()
-        assert np.array_equal(got, oracle.swizzle_scales(ref["scales"])), k
-        assert np.float32(q.s_dec[0].item()) == np.float32(ref["s_dec"]), k
+        for r0 in r0s[k]:
+            ref = oracle.quantize(bits, scale_fmt=oracle.FMT_E4M3,
+                                  block=oracle.BLOCK_16x16 if cfg.block == fb.FP4_BLOCK_16x16 else oracle.BLOCK_1x16,
+                                  sr=cfg.round == fb.FP4_ROUND_SR, colwise=cfg.orient == fb.FP4_ORIENT_COLWISE,
+                                  rht=cfg.rht, seed=cfg.seed, tensor_id=cfg.tensor_id, step=0,
+                                  op_rows=(r0, r0 + band))
+            refs[k].append(ref)
+            assert np.array_equal(q.codes[r0:r0 + band].cpu().numpy(), ref["codes"]), (k, r0)
+            # scales of the band: the band is one 128-row tile of the tensor-core layout
+            got = q.scales.view(-1, nb * 128)[r0 // 128].cpu().numpy()
+            assert np.array_equal(got, oracle.swizzle_scales(ref["scales"])), (k, r0)
+            assert np.float32(q.s_dec[0].item()) == np.float32(ref["s_dec"]), k
     for out, (ka, kb), bf16 in [(y, ("x", "w"), True), (dx, ("dy", "wt"), True), (dw, ("dyt", "xt"), False)]:
-        ra, rb = refs[ka], refs[kb]
-        ms = rng.integers(0, band, samples)
-        ns = rng.integers(0, band, samples)
-        c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
-                               pairs=(ms, ns))
-        _check(out.float().cpu().numpy()[r0s[ka] + ms, r0s[kb] + ns], c_ref, s, bf16)
+        host = out.float().cpu().numpy()
+        for i in range(3):  # first tile, last tile, a random tile
+            ra, rb = refs[ka][i], refs[kb][i]
+            ms = rng.integers(0, band, samples)
+            ns = rng.integers(0, band, samples)
+            c_ref, s = oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"], rb["s_dec"],
+                                   pairs=(ms, ns))
+            _check(host[r0s[ka][i] + ms, r0s[kb][i] + ns], c_ref, s, bf16)
 
 
 @pytest.mark.parametrize("which", [0, 1])
