@@ -36,7 +36,8 @@ EXPORTED = ["fp4_quantized_sizes", "fp4_workspace_bytes", "fp4_quantize", "fp4_d
             "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
             "fp4_status_string", "fp4_abi_version", "fp4_quantize_noalloc", "fp4_quantize_dual",
             "fp4_gemm_workspace_bytes", "fp4_gemm_ws", "fp4_tensor_amax", "fp4_tensor_amax_dual",
-            "fp4_selftest_wait_timeout"]
+            "fp4_selftest_wait_timeout", "fp4_selftest_div6", "fp4_device_status_record", "fp4_last_device_status",
+            "fp4_quantized_bytes"]
 
 
 class fp4_quant_params_t(ctypes.Structure):
@@ -80,17 +81,19 @@ def load() -> ctypes.CDLL:
             TP = ctypes.POINTER(fp4_tensor_t)
             L.fp4_quantized_sizes.argtypes = [QP, i64, i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]
             L.fp4_quantized_sizes.restype = i32
+            L.fp4_quantized_bytes.argtypes = [QP, i64, i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+            L.fp4_quantized_bytes.restype = i32
             L.fp4_workspace_bytes.argtypes = [QP, i64, i64]
             L.fp4_workspace_bytes.restype = sz
-            L.fp4_quantize.argtypes = [QP, P, i64, i64, TP, TP, P, P, P, sz, P]
+            L.fp4_quantize.argtypes = [QP, P, i64, i64, i64, TP, TP, P, P, P, sz, P]
             L.fp4_quantize.restype = i32
-            L.fp4_quantize_dual.argtypes = [QP, QP, P, i64, i64, TP, TP, P, P, P, P, P, sz, P]
+            L.fp4_quantize_dual.argtypes = [QP, QP, P, i64, i64, i64, TP, TP, P, P, P, P, P, sz, P]
             L.fp4_quantize_dual.restype = i32
-            L.fp4_quantize_noalloc.argtypes = [QP, P, i64, i64, TP, TP, P, P, P]
+            L.fp4_quantize_noalloc.argtypes = [QP, P, i64, i64, i64, TP, TP, P, P, P]
             L.fp4_quantize_noalloc.restype = i32
-            L.fp4_tensor_amax.argtypes = [QP, P, i64, i64, P, P, sz, P]
+            L.fp4_tensor_amax.argtypes = [QP, P, i64, i64, i64, P, P, sz, P]
             L.fp4_tensor_amax.restype = i32
-            L.fp4_tensor_amax_dual.argtypes = [QP, QP, P, i64, i64, P, P, P, sz, P]
+            L.fp4_tensor_amax_dual.argtypes = [QP, QP, P, i64, i64, i64, P, P, P, sz, P]
             L.fp4_tensor_amax_dual.restype = i32
             L.fp4_dequantize.argtypes = [TP, P, i32, P]
             L.fp4_dequantize.restype = i32
@@ -108,8 +111,14 @@ def load() -> ctypes.CDLL:
             L.fp4_linear_wgrad.restype = i32
             L.fp4_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
             L.fp4_selftest_wait_timeout.restype = i32
+            L.fp4_selftest_div6.argtypes = [P, P, i64, P]
+            L.fp4_selftest_div6.restype = i32
             L.fp4_device_status.argtypes = [P]
             L.fp4_device_status.restype = i32
+            L.fp4_last_device_status.argtypes = [P]
+            L.fp4_last_device_status.restype = i32
+            L.fp4_device_status_record.argtypes = [P, P]
+            L.fp4_device_status_record.restype = i32
             L.fp4_status_string.argtypes = [i32]
             L.fp4_status_string.restype = ctypes.c_char_p
             L.fp4_abi_version.argtypes = []

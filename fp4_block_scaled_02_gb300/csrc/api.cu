@@ -65,22 +65,44 @@ int* device_status_ptr() {
 
 }  // namespace fp4bs
 
+namespace fp4bs {
+namespace {
+
+// Stream-ordered status read: when the stream reaches it, move the status word
+// (and its reset to 0) into *dst.
+__global__ void status_record_kernel(int* status, int32_t* dst) {
+    pdl_begin();
+    *dst = atomicExch(status, 0);
+}
+
+}  // namespace
+}  // namespace fp4bs
+
 using namespace fp4bs;
 
 namespace {
 
 int block_len(int block) { return block == FP4_BLOCK_1x32 ? 32 : 16; }
 
-// Checks shared by the quantizer entry points. Fills `job` on success.
-fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t rows, int64_t cols,
-                            const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
-                            uint64_t* counters, void* ws, size_t ws_bytes, QuantJob& job) {
+// Row stride of a BF16 input: at least its width and a multiple of 8 elements,
+// so that every row starts 16-byte aligned like the base pointer.
+bool ld_ok(int64_t rows, int64_t cols, int64_t ld) {
+    if (rows == 0 || cols == 0) return true;
+    return ld >= cols && ld % 8 == 0;
+}
+
+// Argument checks shared by the quantizer entry points (everything but the
+// workspace). Fills `job` on success.
+fp4_status_t check_quantize_args(const fp4_quant_params_t* p, const void* in, int64_t rows, int64_t cols, int64_t ld,
+                                 const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
+                                 uint64_t* counters, QuantJob& job) {
     if (p == nullptr || out == nullptr) return FP4_ERR_INVALID_ARG;
     if (p->reserved != 0) return FP4_ERR_INVALID_ARG;
     if (p->scale_fmt < 0 || p->scale_fmt > 2 || p->block < 0 || p->block > 2) return FP4_ERR_INVALID_ARG;
     if (p->round < 0 || p->round > 1 || p->orient < 0 || p->orient > 1) return FP4_ERR_INVALID_ARG;
     if (p->tscale < 0 || p->tscale > 3 || p->scale_layout < 0 || p->scale_layout > 1) return FP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0) return FP4_ERR_SHAPE;
+    if (!ld_ok(rows, cols, ld)) return FP4_ERR_SHAPE;
     if (p->tensor_id == 0xFFFFFFFFu) return FP4_ERR_INVALID_ARG;
     const bool mx = p->scale_fmt == FP4_SCALE_UE8M0;
     if (mx != (p->block == FP4_BLOCK_1x32)) return FP4_ERR_INVALID_ARG;
@@ -148,6 +170,7 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     job.in = static_cast<const uint16_t*>(in);
     job.rows = rows;
     job.cols = cols;
+    job.ld = ld;
     job.codes = out->codes;
     job.scales = out->scales;
     job.s_dec = out->s_dec_global;
@@ -160,11 +183,26 @@ fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t
     }
     job.state = state;
     job.counters = counters;
-    job.partials = static_cast<float*>(ws);
-    const int np = amax_partials_needed(job);
-    if (np > 0 && (ws == nullptr || ws_bytes < (size_t)np * sizeof(float))) return FP4_ERR_WORKSPACE;
-    if (np > 0 && !aligned16(ws)) return FP4_ERR_ALIGNMENT;
     return FP4_OK;
+}
+
+// The amax pass's partials go to ws: enough room for every partial it writes,
+// 16-byte aligned (nothing is checked or used when the call runs no amax pass).
+fp4_status_t attach_workspace(QuantJob& job, void* ws, size_t ws_bytes) {
+    const int np = amax_partials_needed(job);
+    if (np == 0) return FP4_OK;
+    if (ws == nullptr || ws_bytes < (size_t)np * sizeof(float)) return FP4_ERR_WORKSPACE;
+    if (!aligned16(ws)) return FP4_ERR_ALIGNMENT;
+    job.partials = static_cast<float*>(ws);
+    return FP4_OK;
+}
+
+fp4_status_t check_quantize(const fp4_quant_params_t* p, const void* in, int64_t rows, int64_t cols, int64_t ld,
+                            const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
+                            uint64_t* counters, void* ws, size_t ws_bytes, QuantJob& job) {
+    fp4_status_t s = check_quantize_args(p, in, rows, cols, ld, out, out_t, state, counters, job);
+    if (s != FP4_OK) return s;
+    return attach_workspace(job, ws, ws_bytes);
 }
 
 fp4_status_t check_operand(const fp4_tensor_t* t) {
@@ -192,8 +230,10 @@ fp4_status_t check_operand(const fp4_tensor_t* t) {
 //
 // The array's host-side name is only a stand-in for the device symbol, so its
 // device address is looked up once per device (cudaGetSymbolAddress, with the
-// device current) by the first call made on that device; make that first call
-// before any stream capture begins. Every call shares the one array and it
+// device current) by the first call on that device that runs an amax pass
+// (current scaling, or a held-amax call); make that first call before any
+// stream capture begins. Calls that run no amax pass (UE8M0, a given amax, per-
+// row scales) never touch the array. Every call shares the one array and it
 // keeps the last call's contents; nothing in it needs to start at zero,
 // because the amax pass writes every partial the conversion pass reads. Calls
 // whose work overlaps on the GPU (different streams, no ordering between
@@ -319,7 +359,7 @@ struct NvtxRange {
 
 extern "C" {
 
-int fp4_abi_version(void) { return 2; }
+int fp4_abi_version(void) { return 3; }
 
 const char* fp4_status_string(fp4_status_t s) {
     switch (s) {
@@ -358,12 +398,12 @@ size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t co
     return (size_t)kMaxAmaxPartials * sizeof(float);
 }
 
-fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols, int64_t ld,
                           const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                           uint64_t* counters, void* ws, size_t ws_bytes, void* stream) {
     NvtxRange nvtx_range("fp4_quantize");
     QuantJob job;
-    fp4_status_t s = check_quantize(p, in_bf16, rows, cols, out, out_t, state, counters, ws, ws_bytes, job);
+    fp4_status_t s = check_quantize(p, in_bf16, rows, cols, ld, out, out_t, state, counters, ws, ws_bytes, job);
     if (s != FP4_OK) return s;
     if (rows == 0 || cols == 0) return FP4_OK;
     job.status = device_status_ptr();
@@ -372,18 +412,23 @@ fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int6
 }
 
 fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
-                                  const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
-                                  uint64_t* counters, void* stream) {
+                                  int64_t ld, const fp4_tensor_t* out, const fp4_tensor_t* out_t,
+                                  fp4_amax_state_t* state, uint64_t* counters, void* stream) {
     NvtxRange nvtx_range("fp4_quantize_noalloc");
-    float* scratch = noalloc_scratch_ptr();
-    if (scratch == nullptr) return FP4_ERR_CUDA;
     QuantJob job;
-    // the scratch is offered as a workspace of its fixed size: a call that
-    // would need more amax partials than it holds is rejected with
-    // FP4_ERR_WORKSPACE before anything is launched
-    fp4_status_t s = check_quantize(p, in_bf16, rows, cols, out, out_t, state, counters, scratch,
-                                    sizeof(float) * kNoAllocScratchFloats, job);
+    fp4_status_t s = check_quantize_args(p, in_bf16, rows, cols, ld, out, out_t, state, counters, job);
     if (s != FP4_OK) return s;
+    // the scratch is offered as a workspace of its fixed size, looked up only
+    // when the call runs an amax pass: a call that would need more partials
+    // than it holds is rejected with FP4_ERR_WORKSPACE before anything is launched
+    const int np = amax_partials_needed(job);
+    if (np > kNoAllocScratchFloats) return FP4_ERR_WORKSPACE;
+    if (np > 0) {
+        float* scratch = noalloc_scratch_ptr();
+        if (scratch == nullptr) return FP4_ERR_CUDA;
+        s = attach_workspace(job, scratch, sizeof(float) * kNoAllocScratchFloats);
+        if (s != FP4_OK) return s;
+    }
     if (rows == 0 || cols == 0) return FP4_OK;
     job.status = device_status_ptr();
     if (job.status == nullptr) return FP4_ERR_CUDA;
@@ -391,7 +436,8 @@ fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf
 }
 
 fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
-                               int64_t rows, int64_t cols, const fp4_tensor_t* out_row, const fp4_tensor_t* out_col,
+                               int64_t rows, int64_t cols, int64_t ld, const fp4_tensor_t* out_row,
+                               const fp4_tensor_t* out_col,
                                fp4_amax_state_t* state_row, fp4_amax_state_t* state_col, uint64_t* counters_row,
                                uint64_t* counters_col, void* ws, size_t ws_bytes, void* stream) {
     NvtxRange nvtx_range("fp4_quantize_dual");
@@ -410,9 +456,10 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
     const bool given = p_row->tscale == FP4_TSCALE_GIVEN;  // no amax pass: no workspace needed
     if (!given && (ws == nullptr || ws_bytes < 2 * half)) return FP4_ERR_WORKSPACE;
     QuantJob jr, jc;
-    fp4_status_t s = check_quantize(p_row, in_bf16, rows, cols, out_row, nullptr, state_row, counters_row, ws, half, jr);
+    fp4_status_t s =
+        check_quantize(p_row, in_bf16, rows, cols, ld, out_row, nullptr, state_row, counters_row, ws, half, jr);
     if (s != FP4_OK) return s;
-    s = check_quantize(p_col, in_bf16, rows, cols, out_col, nullptr, state_col, counters_col,
+    s = check_quantize(p_col, in_bf16, rows, cols, ld, out_col, nullptr, state_col, counters_col,
                        given ? nullptr : static_cast<char*>(ws) + half, half, jc);
     if (s != FP4_OK) return s;
     if (rows == 0 || cols == 0) return FP4_OK;
@@ -422,28 +469,30 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
 }
 
 
-fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols, int64_t ld,
                              fp4_amax_state_t* out, void* ws, size_t ws_bytes, void* stream) {
     NvtxRange nvtx_range("fp4_tensor_amax");
     fp4_status_t s = check_amax_params(p, rows, cols);
     if (s != FP4_OK) return s;
+    if (!ld_ok(rows, cols, ld)) return FP4_ERR_SHAPE;
     if (out == nullptr || (rows > 0 && cols > 0 && in_bf16 == nullptr)) return FP4_ERR_INVALID_ARG;
     if (ws == nullptr || ws_bytes < 2 * (size_t)kMaxAmaxPartials * sizeof(float)) return FP4_ERR_WORKSPACE;
     if (!aligned16(ws) || !aligned16(in_bf16)) return FP4_ERR_ALIGNMENT;
     int* status = device_status_ptr();
     if (status == nullptr) return FP4_ERR_CUDA;
     const bool rht = p->rht != 0;
-    return from_cuda(launch_tensor_amax(static_cast<const uint16_t*>(in_bf16), rows, cols, rht ? nullptr : out,
+    return from_cuda(launch_tensor_amax(static_cast<const uint16_t*>(in_bf16), rows, cols, ld, rht ? nullptr : out,
                                         rht ? out : nullptr, rht, p->step, static_cast<float*>(ws), status,
                                         static_cast<cudaStream_t>(stream)));
 }
 
 fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
-                                  int64_t rows, int64_t cols, fp4_amax_state_t* out_row, fp4_amax_state_t* out_col,
-                                  void* ws, size_t ws_bytes, void* stream) {
+                                  int64_t rows, int64_t cols, int64_t ld, fp4_amax_state_t* out_row,
+                                  fp4_amax_state_t* out_col, void* ws, size_t ws_bytes, void* stream) {
     NvtxRange nvtx_range("fp4_tensor_amax_dual");
     fp4_status_t s = check_amax_params(p_row, rows, cols);
     if (s != FP4_OK) return s;
+    if (!ld_ok(rows, cols, ld)) return FP4_ERR_SHAPE;
     s = check_amax_params(p_col, rows, cols);
     if (s != FP4_OK) return s;
     if (p_row->orient != FP4_ORIENT_ROWWISE || p_col->orient != FP4_ORIENT_COLWISE) return FP4_ERR_INVALID_ARG;
@@ -454,7 +503,7 @@ fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_qua
     if (!aligned16(ws) || !aligned16(in_bf16)) return FP4_ERR_ALIGNMENT;
     int* status = device_status_ptr();
     if (status == nullptr) return FP4_ERR_CUDA;
-    return from_cuda(launch_tensor_amax(static_cast<const uint16_t*>(in_bf16), rows, cols, out_row, out_col,
+    return from_cuda(launch_tensor_amax(static_cast<const uint16_t*>(in_bf16), rows, cols, ld, out_row, out_col,
                                         p_col->rht != 0, p_row->step, static_cast<float*>(ws), status,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -550,6 +599,28 @@ fp4_status_t fp4_selftest_wait_timeout(uint32_t limit_us, void* stream) {
     int* status = device_status_ptr();
     if (status == nullptr) return FP4_ERR_CUDA;
     return from_cuda(launch_wait_selftest((uint64_t)limit_us * 1000ull, status, static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status_t fp4_selftest_div6(const float* in, float* out, int64_t n, void* stream) {
+    if (n < 0) return FP4_ERR_SHAPE;
+    if (n > 0 && (in == nullptr || out == nullptr)) return FP4_ERR_INVALID_ARG;
+    if (n > 0 && (!aligned16(in) || !aligned16(out))) return FP4_ERR_ALIGNMENT;
+    return from_cuda(launch_div6_selftest(in, out, n, static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status_t fp4_device_status_record(int32_t* dst, void* stream) {
+    if (dst == nullptr || (reinterpret_cast<uintptr_t>(dst) & 3u) != 0) return FP4_ERR_INVALID_ARG;
+    int* p = device_status_ptr();
+    if (p == nullptr) return FP4_ERR_CUDA;
+    (void)launch_pdl(status_record_kernel, 1, 1, 0, static_cast<cudaStream_t>(stream), p, dst);
+    return from_cuda(cudaGetLastError());
+}
+
+fp4_status_t fp4_last_device_status(void* stream) { return fp4_device_status(stream); }
+
+fp4_status_t fp4_quantized_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols, size_t* codes_bytes,
+                                 size_t* scales_bytes) {
+    return fp4_quantized_sizes(p, rows, cols, codes_bytes, scales_bytes);
 }
 
 fp4_status_t fp4_device_status(void* stream) {

@@ -188,14 +188,18 @@ __device__ __forceinline__ float exp2_exact(int k) {
     return __uint_as_float(1u << (k + 149));
 }
 
-// RN(a / 6) in binary32 with one multiply and two fused multiply-adds:
-// q0 = RN(a * y) with y = RN(1/6), r = RN(a - 6 q0) (exact), q1 = RN(q0 + r * y).
-// Checked exhaustively against the correctly rounded quotient over whole
-// binades (normal binades all behave alike, being exact scalings of one
-// another); below 2^-120 the quotient approaches the subnormal range, where
-// the IEEE division is used instead.
+// RN(a / 6) in binary32 by division with a precomputed reciprocal and one
+// correction step (Markstein's residual correction, IBM J. Res. Dev. 34(1),
+// 1990; Muller et al., "Handbook of Floating-Point Arithmetic", on division by
+// a constant): q0 = RN(a * y) with y = RN(1/6), the residual r = a - 6 q0 is
+// exact in one fused multiply-add, and q1 = RN(q0 + r * y). A GPU test checks
+// it bit for bit against the correctly rounded quotient over whole binades
+// (normal binades all behave alike, being exact scalings of one another, as
+// long as no step leaves the normal range). Below 2^-120 the residual nears
+// the subnormal range, and an infinite or NaN a would make r = inf - inf: both
+// take the IEEE division instead.
 __device__ __forceinline__ float div6_rn(float a) {
-    if (!(a >= 0x1p-120f)) return __fdiv_rn(a, 6.0f);
+    if (!(a >= 0x1p-120f && a <= 0x1.fffffep127f)) return __fdiv_rn(a, 6.0f);
     const float y = 0x1.555556p-3f;
     const float q0 = __fmul_rn(a, y);
     const float r = __fmaf_rn(-6.0f, q0, a);

@@ -504,14 +504,15 @@ bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_
     return make_tmap_u8_swizzled(map, base, rows, row_bytes, box_rows, 128);
 }
 
-// 2-D BF16 matrix (rows x cols, row-major), box_rows x box_cols tiles, optionally
-// with the 128-byte swizzle (box_cols * 2 == 128 then).
+// 2-D BF16 matrix (rows x cols, row-major, rows ld elements apart; ld = 0:
+// cols), box_rows x box_cols tiles, optionally with the 128-byte swizzle
+// (box_cols * 2 == 128 then).
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols,
-                       bool swizzle128) {
+                       bool swizzle128, int64_t ld) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld > 0 ? ld : cols) * 2};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
     if (swizzle128 && box_cols * 2 != 128) return false;

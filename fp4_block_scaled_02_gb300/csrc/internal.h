@@ -58,6 +58,7 @@ struct QuantJob {
     uint64_t step;
     const uint16_t* in;
     int64_t rows, cols;
+    int64_t ld;         // input row stride in elements (>= cols, a multiple of 8)
     // primary output (the operand) and, for 16x16, the optional transposed one
     uint8_t* codes;
     uint8_t* scales;
@@ -88,7 +89,7 @@ int amax_partials_needed(const QuantJob& job);
 // tensor into st_plain and/or the post-RHT colwise amax (rht) or the plain one
 // (!rht) into st_col; null records are skipped. partials: 2 * kMaxAmaxPartials
 // floats. status: the device status word (bounded waits).
-cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, fp4_amax_state_t* st_plain,
+cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, int64_t ld, fp4_amax_state_t* st_plain,
                                fp4_amax_state_t* st_col, bool rht, uint64_t step, float* partials, int* status,
                                cudaStream_t stream);
 
@@ -144,6 +145,8 @@ cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_
 // completes; after limit_ns the wait records FP4_ERR_DEVICE_TIMEOUT in *status
 // and the kernel returns.
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
+// out[i] = the quantizer's RN(in[i] / 6) for i < n (diagnostic).
+cudaError_t launch_div6_selftest(const float* in, float* out, int64_t n, cudaStream_t stream);
 // Any of the n bytes at f nonzero (every thread of the calling warp gets the answer).
 __device__ __forceinline__ bool rb_any_flag(const uint8_t* f, int64_t n) {
     bool any = false;
@@ -155,8 +158,9 @@ __device__ __forceinline__ bool rb_any_flag(const uint8_t* f, int64_t n) {
 // swizzling (defined in gemm_nvfp4.cu).
 bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows);
 // 2-D BF16 matrix tensor map with box_rows x box_cols tiles, unswizzled or with
-// the 128-byte swizzle (defined in gemm_nvfp4.cu).
+// the 128-byte swizzle; rows lie ld elements apart (ld = 0: cols) (defined in
+// gemm_nvfp4.cu).
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, int box_cols,
-                       bool swizzle128 = false);
+                       bool swizzle128 = false, int64_t ld = 0);
 
 }  // namespace fp4bs

@@ -33,6 +33,7 @@ constexpr int kThreads = 256;
 struct QParams {
     const uint16_t* in;
     int64_t rows, cols;
+    int64_t ld;  // input row stride in elements (>= cols, a multiple of 8)
     uint8_t* codes;
     uint8_t* scales;
     float* s_dec;
@@ -54,6 +55,15 @@ struct QParams {
 };
 
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+// Input offset of unit u of a row-major rows x cols input cut into units of
+// `unit` elements (per_row = cols / unit of them per row) when its rows lie ld
+// elements apart: unit * u for a dense input (ld == cols, the common case, no
+// division), else row * ld + column.
+__device__ __forceinline__ int64_t strided_off(int64_t u, int unit, int64_t per_row, int64_t cols, int64_t ld) {
+    if (ld == cols) return (int64_t)unit * u;
+    return (u / per_row) * ld + (int64_t)unit * (u % per_row);
+}
 
 // Block-wide max of a non-negative float (all threads of the CTA call it).
 __device__ float cta_max(float v) {
@@ -239,6 +249,7 @@ __device__ __forceinline__ bool amax_pass_skipped(const fp4_amax_state_t* a, con
 }
 
 __global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __restrict__ in, int64_t n_vec,
+                                                                 int64_t row_vec, int64_t ld_vec,
                                                                  float* __restrict__ partials,
                                                                  const fp4_amax_state_t* skip_if_valid) {
     pdl_begin();
@@ -249,14 +260,14 @@ __global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __
     for (; i + (kAmaxVec - 1) * stride < n_vec; i += kAmaxVec * stride) {
         uint4 v[kAmaxVec];
 #pragma unroll
-        for (int k = 0; k < kAmaxVec; ++k) v[k] = __ldg(in + i + k * stride);
+        for (int k = 0; k < kAmaxVec; ++k) v[k] = __ldg(in + strided_off(i + k * stride, 1, row_vec, row_vec, ld_vec));
 #pragma unroll
         for (int k = 0; k < kAmaxVec; ++k)
             m = __vmaxu2(m, __vmaxu2(__vmaxu2(v[k].x & 0x7FFF7FFFu, v[k].y & 0x7FFF7FFFu),
                                      __vmaxu2(v[k].z & 0x7FFF7FFFu, v[k].w & 0x7FFF7FFFu)));
     }
     for (; i < n_vec; i += stride) {
-        const uint4 a = __ldg(in + i);
+        const uint4 a = __ldg(in + strided_off(i, 1, row_vec, row_vec, ld_vec));
         m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
                                  __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
     }
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 4) amax_plain_kernel(const uint4* __
 // the max magnitude. The RHT's signs do not change magnitudes and its 1/4 is an
 // exact scaling, so the max is taken over the raw butterfly and scaled once.
 __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ in, int64_t T,
-                                                                 int64_t C, float* __restrict__ partials,
+                                                                 int64_t C, int64_t ld, float* __restrict__ partials,
                                                                  const fp4_amax_state_t* skip_if_valid) {
     pdl_begin();
     if (amax_pass_skipped(skip_if_valid, nullptr)) return;
@@ -281,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
         const int64_t g = u % ug, j = u / ug;
         uint2 x[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) x[t] = __ldg(reinterpret_cast<const uint2*>(in + (16 * j + t) * C + 4 * g));
+        for (int t = 0; t < 16; ++t) x[t] = __ldg(reinterpret_cast<const uint2*>(in + (16 * j + t) * ld + 4 * g));
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr) {
             f2 pv[16];
@@ -329,8 +340,9 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(QParams q) {
         for (int u = 0; u < 2; ++u) {
             const int64_t b = base + 32 * u + lane;
             if (b < nblk) {
-                in[u][0] = ldg16(q.in + 16 * b);
-                in[u][1] = ldg16(q.in + 16 * b + 8);
+                const int64_t o = strided_off(b, 16, nb_row, q.cols, q.ld);
+                in[u][0] = ldg16(q.in + o);
+                in[u][1] = ldg16(q.in + o + 8);
             }
         }
 #pragma unroll
@@ -385,7 +397,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_rowscale_kernel(QParam
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     Counts cnt;
     for (int64_t r = warp; r < q.rows; r += nwarps) {
-        const uint4* row = reinterpret_cast<const uint4*>(q.in + r * q.cols);
+        const uint4* row = reinterpret_cast<const uint4*>(q.in + r * q.ld);
         uint32_t m = 0u;
         int64_t i = lane;
         for (; i + 32 * (kAmaxVec - 1) < n_vec; i += 32 * kAmaxVec) {
@@ -415,8 +427,8 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_rowscale_kernel(QParam
             for (int u = 0; u < 2; ++u) {
                 const int64_t j = base + 32 * u + lane;
                 if (j < nb_row) {
-                    in[u][0] = ldg16(q.in + r * q.cols + 16 * j);
-                    in[u][1] = ldg16(q.in + r * q.cols + 16 * j + 8);
+                    in[u][0] = ldg16(q.in + r * q.ld + 16 * j);
+                    in[u][1] = ldg16(q.in + r * q.ld + 16 * j + 8);
                 }
             }
 #pragma unroll
@@ -487,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_cols_kernel(QParams q) {
         uint2 x[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-            x[t] = active ? __ldg(reinterpret_cast<const uint2*>(q.in + (16 * j + t) * C + 4 * g)) : make_uint2(0, 0);
+            x[t] = active ? __ldg(reinterpret_cast<const uint2*>(q.in + (16 * j + t) * q.ld + 4 * g)) : make_uint2(0, 0);
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr) {
             // channels 4g + 2pr (low lane) and 4g + 2pr + 1 (high lane)
@@ -559,7 +571,7 @@ __global__ void __launch_bounds__(kThreads) quantize_2d_kernel(QParams q) {
         const int64_t n = 16 * tn + i, k0 = 16 * tk;
         float v[16];
         if (active) {
-            const uint4 a = ldg16(q.in + n * K + k0), c = ldg16(q.in + n * K + k0 + 8);
+            const uint4 a = ldg16(q.in + n * q.ld + k0), c = ldg16(q.in + n * q.ld + k0 + 8);
             unpack16(a, c, v);
         } else {
 #pragma unroll
@@ -835,8 +847,9 @@ __global__ void __launch_bounds__(kThreads) quantize_mx_rows_kernel(QParams q) {
         uint32_t sc = 0u;
         if (active) {
             float v[32];
-            unpack16(ldg16(q.in + 32 * b), ldg16(q.in + 32 * b + 8), v);
-            unpack16(ldg16(q.in + 32 * b + 16), ldg16(q.in + 32 * b + 24), v + 16);
+            const int64_t o = strided_off(b, 32, nb_row, q.cols, q.ld);
+            unpack16(ldg16(q.in + o), ldg16(q.in + o + 8), v);
+            unpack16(ldg16(q.in + o + 16), ldg16(q.in + o + 24), v + 16);
             float amax_b = 0.0f;
 #pragma unroll
             for (int e = 0; e < 32; ++e) amax_b = fmaxf(amax_b, fabsf(v[e]));
@@ -945,7 +958,7 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __r
 // tokens x 4 channels.
 template <bool RHT>
 __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __restrict__ in, int64_t T, int64_t C,
-                                                             float* __restrict__ partials_row,
+                                                             int64_t ld, float* __restrict__ partials_row,
                                                              float* __restrict__ partials_col,
                                                              const fp4_amax_state_t* skip_row,
                                                              const fp4_amax_state_t* skip_col) {
@@ -959,7 +972,7 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const uint16_t* __r
         const int64_t g = u % ug, j = u / ug;
         uint2 x[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) x[t] = __ldg(reinterpret_cast<const uint2*>(in + (16 * j + t) * C + 4 * g));
+        for (int t = 0; t < 16; ++t) x[t] = __ldg(reinterpret_cast<const uint2*>(in + (16 * j + t) * ld + 4 * g));
 #pragma unroll
         for (int t = 0; t < 16; ++t) mr = __vmaxu2(mr, __vmaxu2(x[t].x & 0x7FFF7FFFu, x[t].y & 0x7FFF7FFFu));
         if (RHT) {
@@ -1288,7 +1301,7 @@ cudaError_t launch_fmt(const QuantJob& j, const QParams& q, cudaStream_t st) {
         }
         const bool a = lw == FP4_LAYOUT_TCGEN05, b = lwt == FP4_LAYOUT_TCGEN05;
         CUtensorMap tmap_w;
-        if (j.rows % 64 == 0 && j.cols % 128 == 0 && make_tmap_bf16_2d(&tmap_w, j.in, j.rows, j.cols, 64, 64, true)) {
+        if (j.rows % 64 == 0 && j.cols % 128 == 0 && make_tmap_bf16_2d(&tmap_w, j.in, j.rows, j.cols, 64, 64, true, j.ld)) {
             const int64_t ntiles = (j.rows / 64) * (j.cols / 128);
             const int64_t cap = (int64_t)num_sms() * 2;
             const int g2 = (int)(ntiles < cap ? ntiles : cap);
@@ -1354,6 +1367,7 @@ QParams make_params(const QuantJob& j) {
     q.in = j.in;
     q.rows = j.rows;
     q.cols = j.cols;
+    q.ld = j.ld;
     q.codes = j.codes;
     q.scales = j.scales;
     q.s_dec = j.s_dec;
@@ -1413,15 +1427,31 @@ cudaError_t launch_quantize(const QuantJob& j, cudaStream_t st) {
     q.npartials = np;
     if (np > 0) {
         const fp4_amax_state_t* skip = (j.held && !j.refresh) ? j.state : nullptr;
-        if (j.rht) (void)launch_pdl(amax_rht_cols_kernel, np, kThreads, 0, st, j.in, j.rows, j.cols, j.partials, skip);
-        else (void)launch_pdl(amax_plain_kernel, np, kThreads, 0, st, reinterpret_cast<const uint4*>(j.in), j.rows * j.cols / 8,
-                                                         j.partials, skip);
+        if (j.rht)
+            (void)launch_pdl(amax_rht_cols_kernel, np, kThreads, 0, st, j.in, j.rows, j.cols, j.ld, j.partials, skip);
+        else
+            (void)launch_pdl(amax_plain_kernel, np, kThreads, 0, st, reinterpret_cast<const uint4*>(j.in),
+                             j.rows * j.cols / 8, j.cols / 8, j.ld / 8, j.partials, skip);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     // pass 2: scale and convert
     if (j.scale_fmt == kFmtE4M3) return launch_fmt<kFmtE4M3>(j, q, st);
     return launch_fmt<kFmtUE5M3>(j, q, st);
+}
+
+namespace {
+__global__ void div6_selftest_kernel(const float* __restrict__ in, float* __restrict__ out, int64_t n) {
+    pdl_begin();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) out[i] = div6_rn(in[i]);
+}
+}  // namespace
+
+cudaError_t launch_div6_selftest(const float* in, float* out, int64_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    (void)launch_pdl(div6_selftest_kernel, grid_for(n, 4), kThreads, 0, st, in, out, n);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dequantize(const DequantJob& j, cudaStream_t st) {
@@ -1451,7 +1481,7 @@ int dual_amax_grid(const QuantJob& jc) {
     return g < kMaxAmaxPartials ? g : kMaxAmaxPartials;
 }
 
-cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, fp4_amax_state_t* st_plain,
+cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, int64_t ld, fp4_amax_state_t* st_plain,
                                fp4_amax_state_t* st_col, bool rht, uint64_t step, float* partials, int* status,
                                cudaStream_t st) {
     if (T == 0 || C == 0) {
@@ -1466,7 +1496,7 @@ cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, fp4_ama
     const bool post_rht = st_col != nullptr && rht;
     int np;
     CUtensorMap tmap_x;
-    if (T % kDualTT == 0 && C % kDualTC == 0 && make_tmap_bf16_2d(&tmap_x, in, T, C, kDualTT, kDualTC)) {
+    if (T % kDualTT == 0 && C % kDualTC == 0 && make_tmap_bf16_2d(&tmap_x, in, T, C, kDualTT, kDualTC, false, ld)) {
         // two CTAs per SM when the pass runs alone; beside a conversion pass one fits
         // and the other follows
         const int64_t ntiles = (T / kDualTT) * (C / kDualTC), cap = 2 * (int64_t)num_sms();
@@ -1488,14 +1518,15 @@ cudaError_t launch_tensor_amax(const uint16_t* in, int64_t T, int64_t C, fp4_ama
         QuantJob j{};
         j.rows = T;
         j.cols = C;
+        j.ld = ld;
         j.colwise = post_rht;
         j.rht = post_rht;
         np = amax_grid(j);
         if (plain)
             (void)launch_pdl(amax_plain_kernel, np, kThreads, 0, st, reinterpret_cast<const uint4*>(in), T * C / 8,
-                             part_plain, (const fp4_amax_state_t*)nullptr);
+                             C / 8, ld / 8, part_plain, (const fp4_amax_state_t*)nullptr);
         if (post_rht)
-            (void)launch_pdl(amax_rht_cols_kernel, np, kThreads, 0, st, in, T, C, part_col,
+            (void)launch_pdl(amax_rht_cols_kernel, np, kThreads, 0, st, in, T, C, ld, part_col,
                              (const fp4_amax_state_t*)nullptr);
     }
     cudaError_t e = cudaGetLastError();
@@ -1517,10 +1548,10 @@ cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStr
         const int np = dual_amax_grid(jc);
         qr.npartials = qc.npartials = np;
         if (jc.rht)
-            (void)launch_pdl(amax_dual_kernel<true>, np, kThreads, 0, st, jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
+            (void)launch_pdl(amax_dual_kernel<true>, np, kThreads, 0, st, jr.in, jr.rows, jr.cols, jr.ld, jr.partials, jc.partials, skip_r,
                                                              skip_c);
         else
-            (void)launch_pdl(amax_dual_kernel<false>, np, kThreads, 0, st, jr.in, jr.rows, jr.cols, jr.partials, jc.partials, skip_r,
+            (void)launch_pdl(amax_dual_kernel<false>, np, kThreads, 0, st, jr.in, jr.rows, jr.cols, jr.ld, jr.partials, jc.partials, skip_r,
                                                               skip_c);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1529,7 +1560,7 @@ cudaError_t launch_quantize_dual(const QuantJob& jr, const QuantJob& jc, cudaStr
     const int64_t cap = (int64_t)num_sms() * 2;
     const int grid = (int)(ntiles < cap ? ntiles : cap);
     CUtensorMap tmap_x;
-    if (!make_tmap_bf16_2d(&tmap_x, jr.in, jr.rows, jr.cols, kDualTT, kDualTC)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&tmap_x, jr.in, jr.rows, jr.cols, kDualTT, kDualTC, false, jr.ld)) return cudaErrorInvalidValue;
 #define FP4_DUAL(FMT, SR, RHT)                                                                                   \
     do {                                                                                                         \
         auto kern = quantize_dual_kernel<FMT, SR, SR, RHT>;                                                      \

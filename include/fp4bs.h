@@ -34,7 +34,10 @@
  *     (griddepcontrol.wait) before touching global memory, so stream order
  *     holds for all data.
  *   - Shapes: an operand is `rows x cols` with `cols` the dot-product dimension
- *     (K-major); BF16 inputs are row-major with leading dimension = cols.
+ *     (K-major). BF16 inputs are row-major with their rows `ld` elements apart
+ *     (ld >= cols and a multiple of 8, so every row starts 16-byte aligned; ld
+ *     is not checked for empty inputs): a column slice of a wider buffer is
+ *     quantized in place.
  */
 #ifndef FP4BS_H
 #define FP4BS_H
@@ -145,8 +148,11 @@ typedef struct {
 } fp4_amax_state_t;
 
 /* Sizes of the codes and scales buffers fp4_quantize writes for an input of
- * rows x cols (for COLWISE the operand is cols x rows). Host only. */
+ * rows x cols (for COLWISE the operand is cols x rows). Host only.
+ * fp4_quantized_bytes is the same call under its other name. */
 fp4_status_t fp4_quantized_sizes(const fp4_quant_params_t* p, int64_t rows, int64_t cols,
+                                 size_t* codes_bytes, size_t* scales_bytes);
+fp4_status_t fp4_quantized_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols,
                                  size_t* codes_bytes, size_t* scales_bytes);
 
 /* Device workspace bytes fp4_quantize needs (the per-CTA amax partials of the
@@ -154,8 +160,9 @@ fp4_status_t fp4_quantized_sizes(const fp4_quant_params_t* p, int64_t rows, int6
  * Host only. */
 size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t cols);
 
-/* Quantize a row-major BF16 input `in_bf16` (rows x cols) into `out`
- * ("Pretraining LLMs with NVFP4", App. B.1-B.3; sections 4.2-4.4).
+/* Quantize a row-major BF16 input `in_bf16` (rows x cols, rows ld elements
+ * apart) into `out` ("Pretraining LLMs with NVFP4", App. B.1-B.3; sections
+ * 4.2-4.4). ld < cols or not a multiple of 8: FP4_ERR_SHAPE.
  *   out      : operand descriptor (rows/cols = operand shape, i.e. transposed
  *              for COLWISE); codes, scales and s_dec_global are written.
  *   out_t    : 16x16 with emit_transpose: the transposed operand (cols x rows)
@@ -173,7 +180,7 @@ size_t fp4_workspace_bytes(const fp4_quant_params_t* p, int64_t rows, int64_t co
  * Shapes: block dimension a multiple of the block length; 16x16 needs both
  * dimensions multiples of 16; TCGEN05 layout needs operand rows % 128 == 0 and
  * operand cols % (4 * block) == 0. rows == 0 or cols == 0 is a no-op. */
-fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols, int64_t ld,
                           const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
                           uint64_t* counters, void* ws, size_t ws_bytes, void* stream);
 
@@ -188,7 +195,8 @@ fp4_status_t fp4_quantize(const fp4_quant_params_t* p, const void* in_bf16, int6
  * tensor-scale mode and step, TCGEN05 scale layout; rows and cols multiples
  * of 128; ws at least 2 * fp4_workspace_bytes() bytes. */
 fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
-                               int64_t rows, int64_t cols, const fp4_tensor_t* out_row, const fp4_tensor_t* out_col,
+                               int64_t rows, int64_t cols, int64_t ld, const fp4_tensor_t* out_row,
+                               const fp4_tensor_t* out_col,
                                fp4_amax_state_t* state_row, fp4_amax_state_t* state_col, uint64_t* counters_row,
                                uint64_t* counters_col, void* ws, size_t ws_bytes, void* stream);
 
@@ -200,13 +208,15 @@ fp4_status_t fp4_quantize_dual(const fp4_quant_params_t* p_row, const fp4_quant_
  * array (2048 floats, held by every GPU that loads the library until exit)
  * instead of a caller workspace; calls needing more partials than it holds
  * are rejected with FP4_ERR_WORKSPACE (no shape does: the amax pass caps its
- * partials at 2048). The first call on each device looks up the array's device
- * address, so make it before any stream capture. All calls share the array:
- * calls that overlap on the GPU race on it. Everything else is as for
- * fp4_quantize, and no device memory is allocated or freed. */
+ * partials at 2048). The first call on each device that runs an amax pass
+ * (current scaling or held amax) looks up the array's device address, so make
+ * it before any stream capture; calls with no amax pass (UE8M0, given amax,
+ * per-row scales) never use the array. All calls share the array: calls that
+ * overlap on the GPU race on it. Everything else is as for fp4_quantize, and
+ * no device memory is allocated or freed. */
 fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
-                                  const fp4_tensor_t* out, const fp4_tensor_t* out_t, fp4_amax_state_t* state,
-                                  uint64_t* counters, void* stream);
+                                  int64_t ld, const fp4_tensor_t* out, const fp4_tensor_t* out_t,
+                                  fp4_amax_state_t* state, uint64_t* counters, void* stream);
 
 /* Tensor amax ahead of quantization (App. B.1: the amax that current scaling
  * takes in its first memory pass), as a separate call so that it can run on
@@ -224,11 +234,11 @@ fp4_status_t fp4_quantize_noalloc(const fp4_quant_params_t* p, const void* in_bf
  * the quantizer's own amax kernels. fp4_tensor_amax_dual writes the rowwise
  * operand's amax (out_row) and the colwise one's (out_col, post-RHT when
  * p_col->rht) from one read. */
-fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols,
+fp4_status_t fp4_tensor_amax(const fp4_quant_params_t* p, const void* in_bf16, int64_t rows, int64_t cols, int64_t ld,
                              fp4_amax_state_t* out, void* ws, size_t ws_bytes, void* stream);
 fp4_status_t fp4_tensor_amax_dual(const fp4_quant_params_t* p_row, const fp4_quant_params_t* p_col, const void* in_bf16,
-                                  int64_t rows, int64_t cols, fp4_amax_state_t* out_row, fp4_amax_state_t* out_col,
-                                  void* ws, size_t ws_bytes, void* stream);
+                                  int64_t rows, int64_t cols, int64_t ld, fp4_amax_state_t* out_row,
+                                  fp4_amax_state_t* out_col, void* ws, size_t ws_bytes, void* stream);
 
 /* Decode an operand back to real values, x = e2m1 * s_hat * s_dec,G computed as
  * RN(RN(e2m1 * s_hat) * s_dec,G) in FP32 (section A3; App. B.3), written as
@@ -289,9 +299,25 @@ fp4_status_t fp4_linear_wgrad(const fp4_tensor_t* dyt, const fp4_tensor_t* xt, f
  * leaving the context usable. fp4_device_status() then reports the timeout. */
 fp4_status_t fp4_selftest_wait_timeout(uint32_t limit_us, void* stream);
 
+/* Diagnostic: out[i] = RN(in[i] / 6) in binary32 as the quantizer forms it
+ * (the RN(amax_B / 6) of the block-scale step, App. B.2), for n device floats
+ * (16-byte aligned, no overlap), so that the step can be checked against the
+ * correctly rounded quotient. n < 0: FP4_ERR_SHAPE. */
+fp4_status_t fp4_selftest_div6(const float* in, float* out, int64_t n, void* stream);
+
 /* Synchronise `stream`, then return and clear the current device's status word
- * (FP4_OK when no device-side error was recorded). */
+ * (FP4_OK when no device-side error was recorded). fp4_last_device_status is
+ * the same call under its other name. */
 fp4_status_t fp4_device_status(void* stream);
+fp4_status_t fp4_last_device_status(void* stream);
+
+/* The same status word without synchronising: when `stream` reaches this call,
+ * the status word (an fp4_status_t value) is written to *dst and the word is
+ * cleared, in stream order. dst: 4-byte aligned device memory, or host memory
+ * the device can write (pinned); read it after the stream has passed the call
+ * (an event, or a later synchronisation). Returns FP4_ERR_INVALID_ARG for a
+ * null or misaligned dst; otherwise the launch status. */
+fp4_status_t fp4_device_status_record(int32_t* dst, void* stream);
 
 /* Static description of a status code. */
 const char* fp4_status_string(fp4_status_t s);

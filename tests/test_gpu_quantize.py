@@ -462,3 +462,111 @@ def test_linear_with_amax_on_a_side_stream_equals_the_plain_schedule():
         assert torch.equal(a.bufs[k].s_dec[:1], b.bufs[k].s_dec[:1]), k  # element 0 is the tensor scale
     assert torch.equal(a.counters, b.counters)
     assert torch.equal(ya, yb) and torch.equal(dxa, dxb) and torch.equal(dwa, dwb)
+
+
+# Strided inputs: the operand is a column slice of a wider BF16 buffer (rows ld
+# elements apart), quantized in place. Each case must give exactly the bytes,
+# tensor scale and counters the oracle gives for the dense copy of the slice.
+STRIDED_CASES = [
+    # (name, rows, cols, col offset, buffer width, config)
+    ("rowwise_sr_tc", 256, 384, 64, 640, dict(round=fb.FP4_ROUND_SR, seed=3, tensor_id=3, step=7)),
+    ("rowwise_rne_plain", 40, 96, 8, 200, dict(layout=PLAIN)),
+    ("colwise_rht_sr", 256, 128, 128, 520, dict(orient=fb.FP4_ORIENT_COLWISE, rht=True, round=fb.FP4_ROUND_SR,
+                                                seed=1, tensor_id=4)),
+    ("2d_tma_tiles", 256, 256, 16, 1000, dict(block=fb.FP4_BLOCK_16x16)),
+    ("2d_plain_kernel", 48, 80, 24, 136, dict(block=fb.FP4_BLOCK_16x16, layout=PLAIN)),
+    ("mxfp4", 128, 256, 32, 512, dict(scale_fmt=fb.FP4_SCALE_UE8M0, block=fb.FP4_BLOCK_1x32)),
+    ("ue5m3_held", 128, 512, 256, 1024, dict(scale_fmt=fb.FP4_SCALE_UE5M3, tscale=fb.FP4_TSCALE_HELD,
+                                             target_T=2048.0, round=fb.FP4_ROUND_SR, tensor_id=3)),
+]
+
+
+@pytest.mark.parametrize("case", STRIDED_CASES, ids=[c[0] for c in STRIDED_CASES])
+def test_strided_column_slice_matches_the_dense_copy(case):
+    name, R, C, c0, width, kw = case
+    buf = random_bf16(500 + len(name), (R, width), "student_t4")
+    dense = np.ascontiguousarray(buf[:, c0:c0 + C])
+    x = to_gpu_bf16(buf)[:, c0:c0 + C]
+    assert x.stride(0) == width and not x.is_contiguous()
+    cfg = fb.QuantConfig(**kw)
+    colwise = cfg.orient == fb.FP4_ORIENT_COLWISE
+    OR, OC = (C, R) if colwise else (R, C)
+    out = fb.QTensor.empty(OR, OC, cfg.scale_fmt, cfg.layout)
+    state = fb.AmaxState() if cfg.tscale == fb.FP4_TSCALE_HELD else None
+    ref_state = oracle.HeldState() if state is not None else None
+    counters = torch.zeros(4, dtype=torch.int64, device="cuda")
+    fb.fp4_quantize(cfg, x, out, state=state, counters=counters, ws=new_ws())
+    assert fb.fp4_device_status() == 0
+    ref = oracle_quantize(cfg, dense, state=ref_state)
+    assert_quant_equal(out, ref, cfg.layout, counters=counters, check_sdec=cfg.scale_fmt != fb.FP4_SCALE_UE8M0)
+
+
+def test_strided_dual_and_tensor_amax_match_the_dense_copy():
+    """The one-read rowwise + colwise call, its tensor amax ahead (TMA tile pass)
+    and the given-amax conversion, on a column slice: the same bytes as the
+    dense copy through the oracle."""
+    T, C, c0, width = 256, 384, 128, 768
+    buf = random_bf16(520, (T, width), "log_normal_1e-4_2")
+    dense = np.ascontiguousarray(buf[:, c0:c0 + C])
+    x = to_gpu_bf16(buf)[:, c0:c0 + C]
+    cr = fb.QuantConfig(round=fb.FP4_ROUND_SR, seed=2, tensor_id=3)
+    cc = fb.QuantConfig(round=fb.FP4_ROUND_SR, orient=fb.FP4_ORIENT_COLWISE, rht=True, seed=2, tensor_id=4)
+    ref_r, ref_c = oracle_quantize(cr, dense), oracle_quantize(cc, dense)
+    o_r, o_c = fb.QTensor.empty(T, C), fb.QTensor.empty(C, T)
+    k_r, k_c = torch.zeros(4, dtype=torch.int64, device="cuda"), torch.zeros(4, dtype=torch.int64, device="cuda")
+    fb.fp4_quantize_dual(cr, cc, x, o_r, o_c, counters_row=k_r, counters_col=k_c,
+                         ws=torch.zeros(fb.AMAX_WS_BYTES // 4, dtype=torch.float32, device="cuda"))
+    assert fb.fp4_device_status() == 0
+    assert_quant_equal(o_r, ref_r, TC, counters=k_r)
+    assert_quant_equal(o_c, ref_c, TC, counters=k_c)
+    s_r, s_c = fb.AmaxState(), fb.AmaxState()
+    fb.fp4_tensor_amax_dual(cr, cc, x, s_r, s_c, torch.zeros(fb.AMAX_WS_BYTES // 4, dtype=torch.float32,
+                                                               device="cuda"))
+    assert np.float32(s_r.amax) == np.float32(ref_r["amax"]) and np.float32(s_c.amax) == np.float32(ref_c["amax"])
+    g_r, g_c = fb.QTensor.empty(T, C), fb.QTensor.empty(C, T)
+    giv = dict(tscale=fb.FP4_TSCALE_GIVEN)
+    fb.fp4_quantize_dual(fb.QuantConfig(round=fb.FP4_ROUND_SR, seed=2, tensor_id=3, **giv),
+                         fb.QuantConfig(round=fb.FP4_ROUND_SR, orient=fb.FP4_ORIENT_COLWISE, rht=True, seed=2,
+                                        tensor_id=4, **giv), x, g_r, g_c, s_r, s_c)
+    assert fb.fp4_device_status() == 0
+    assert_quant_equal(g_r, ref_r, TC)
+    assert_quant_equal(g_c, ref_c, TC)
+
+
+def test_device_status_record_is_stream_ordered():
+    """fp4_device_status_record writes the status word in stream order without
+    synchronising: a bounded wait that times out (the self-test) shows up in the
+    record that follows it, and the record after that reads 0 again."""
+    rec = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    fb.fp4_device_status_record(rec[0:1])
+    fb.fp4_selftest_wait_timeout(2000)
+    fb.fp4_device_status_record(rec[1:2])
+    torch.cuda.synchronize()
+    assert rec.cpu().tolist() == [fb._lib.FP4_OK, fb._lib.FP4_ERR_DEVICE_TIMEOUT]
+    assert fb.fp4_device_status() == 0  # the record cleared the word
+
+
+def test_div6_is_correctly_rounded_over_whole_binades():
+    """The quantizer's RN(amax_B / 6) (App. B.2's decode-scale step, one multiply
+    and two fused multiply-adds) equals the correctly rounded binary32 quotient
+    (numpy's IEEE division) for every float of the binades [1, 2), [2^-120,
+    2^-119) (the lowest it takes) and [2^127, 2^128) (the highest), of the
+    binade [2^-122, 2^-121) and of a sample of subnormals, where the IEEE
+    division takes over, and at 0, FLT_MAX and infinity."""
+    import ctypes
+    L = fb._lib.load()
+    mant = np.arange(1 << 23, dtype=np.uint32)
+    parts = [((e + 127) << 23) | mant for e in (0, -120, 127, -122)]
+    parts.append(np.random.default_rng(0).integers(1, 1 << 23, 1 << 16, dtype=np.uint32))  # subnormals
+    parts.append(np.array([0, 0x7F7FFFFF, 0x7F800000], dtype=np.uint32))
+    bits = np.concatenate(parts)
+    a = bits.view(np.float32)
+    want = (a / np.float32(6.0)).astype(np.float32)
+    x = torch.from_numpy(a.copy()).cuda()
+    y = torch.empty_like(x)
+    st = L.fp4_selftest_div6(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), x.numel(),
+                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    fb._lib.check(st, "fp4_selftest_div6")
+    got = y.cpu().numpy()
+    bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
+    assert bad.size == 0, f"{bad.size} mismatches, first inputs {a[bad[:4]].tolist()}"

@@ -32,7 +32,7 @@ def _noalloc(cfg, x, out, state=None, counters=None):
     p = cfg.params()
     d = out.desc()
     st = L.fp4_quantize_noalloc(ctypes.byref(p), ctypes.c_void_p(x.data_ptr()), x.shape[0], x.shape[1],
-                                ctypes.byref(d), None,
+                                fb.row_stride(x), ctypes.byref(d), None,
                                 ctypes.c_void_p(state.buf.data_ptr()) if state is not None else None,
                                 ctypes.c_void_p(counters.data_ptr()) if counters is not None else None,
                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
