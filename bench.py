@@ -1,26 +1,37 @@
 """Benchmark of the FP4 block-scaled quantized linear hot path on GB300.
 
-One step = the whole hot path over one batch of the 1.2B Transformer FFN
-workload (T = 8192 tokens; linears 2048 -> 6144 and 6144 -> 2048): for each
-linear, the five quantized operands (X rowwise and X^T colwise + RHT16 from one
-pass over X, W 16x16 in both orientations, dY rowwise SR and dY^T colwise +
-RHT16 + SR from one pass over dY; each preceded by its tensor amax, computed on
-a second stream while the previous operand is converted) and the three
-block-scaled NVFP4 GEMMs (Fprop, Dgrad, Wgrad).
+One step = the whole hot path over one batch of a workload's linears. By
+default that is the 8B hybrid FFN workload (T = 8192 tokens; linears
+4096 -> 21504 and 21504 -> 4096), the largest configuration of the pages'
+models that the quantizer and GEMM targets are set on. For each linear: the
+five quantized operands (X rowwise and X^T colwise + RHT16 from one pass over
+X, W 16x16 in both orientations, dY rowwise SR and dY^T colwise + RHT16 + SR
+from one pass over dY; each preceded by its tensor amax, computed on a second
+stream while the previous operand is converted) and the three block-scaled
+NVFP4 GEMMs (Fprop, Dgrad, Wgrad). `--workload ue5m3_sweep` runs the UE5M3
+held-amax sweep instead: one 4096 -> 4096 linear whose gradient drifts x10^+-3
+over 100 steps, UE5M3 block scales, the held amax refreshed every 50 steps,
+and the rebiased native GEMMs.
 
 `value` is fwd+bwd GEMM TFLOP/s of the whole step (6 T N K per linear divided
-by the step time, quantization included) with inputs resident in HBM; `e2e`
-is the same metric through the public API (Fp4Linear.step_host) with the
-inputs copied from pinned host memory and the outputs copied back inside the
-timed region.
+by the step time, quantization included) with inputs resident in HBM (larger
+than L2); `e2e` is the same metric through the public API (Fp4Linear.step_host)
+with the inputs copied from pinned host memory and the outputs copied back
+inside the timed region. `roofline` is the dominant kernel, the block-scaled
+GEMM, timed with CUDA events on its own launches in a second pass of the same
+steps; `roofline_quantize` the dominant quantizer kernel (the one-read rowwise
++ colwise quantizer) the same way. `cpu_baseline` is the CPU oracle on this
+machine's cores: every operand of the step quantized in full, GEMM outputs
+sampled and scaled to the full outputs.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1.2b|8b|12b|tiny]
-    python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b|12b|1.2b|tiny|ue5m3_sweep]
+    python bench.py --impl reference ...   # the CPU oracle on a bounded sample of each step
     python bench.py --kernels              # single library calls, each against its roofline
 """
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
 import json
 import os
 import re
@@ -36,11 +47,15 @@ METRIC = "FP4 linear fwd+bwd TFLOP/s; quantize GB/s (% of FP4/HBM roofline)"
 # Nominal dense-rate ratio FP4 : BF16 on GB300 (13.5 : 2.25 PFLOP/s).
 FP4_OVER_BF16 = 6.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Algorithmic bytes per input element of the step's quantizations, current
-# scaling (one amax pass and one conversion pass over the BF16 input, E2M1 codes
-# plus one 8-bit scale per 16 values written per operand): X and dY each yield a
-# rowwise and a colwise operand, W yields W and W^T -- all 2 * 2 + 2 * (1/2 + 1/16).
-BYTES_TWO_OPERANDS = 5.125
+# Algorithmic bytes per input element of one quantize call that reads its input
+# once and writes two operands (E2M1 codes + one 8-bit scale per 16 values
+# each): the one-read rowwise + colwise call and the 16x16 call emitting W and
+# W^T, with the tensor amax given (its own pass is a separate launch) -- 2 + 2 *
+# (1/2 + 1/16). A call that also reads the input for its amax adds 2.
+BYTES_ONE_PASS_TWO_OPERANDS = 3.125
+BYTES_AMAX_PASS = 2.0
+GEMM_LABELS = ("fprop", "dgrad", "wgrad")
+QUANT_LABELS = ("w", "x", "dy")
 
 
 def load_peaks():
@@ -98,61 +113,129 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# --------------------------------------------------------------------------- CPU oracle sample
+# --------------------------------------------------------------------------- CPU oracle
 _INPUT_CACHE: dict = {}
 
 
-def oracle_sample(workload, tokens: int = 16, feats: int = 256) -> dict:
-    """Time the oracle on a bounded sample of one step: for every linear, the
-    first `tokens` tokens and the first `feats` output and input features.
-    Quantization covers X and dY on those tokens (rowwise and colwise + RHT16)
-    and the W / W^T rows the sampled GEMM outputs need (with the tensor amax of
-    the whole weight); the three GEMMs produce Y[tokens x feats],
-    dX[tokens x feats] (summing over all N) and dW[feats x feats]. Returns the
-    GEMM FLOPs covered and the elapsed seconds."""
-    import oracle
+def workload_inputs(workload, which: int) -> dict:
     from workloads import linear_inputs
+    key = (workload.name, which)
+    if key not in _INPUT_CACHE:
+        _INPUT_CACHE[key] = linear_inputs(workload, which)
+    return _INPUT_CACHE[key]
 
+
+def _operand_specs(workload, which: int):
+    """The step's quantized operands of linear `which`: (name, input key,
+    oracle quantize options, operand rows). Tensor ids follow the layer's: 8 *
+    layer + {0 X, 1 X^T, 2 W and W^T, 3 dY, 4 dY^T}."""
+    import oracle
+    lin = workload.linears[which]
+    T, K, N = lin.tokens, lin.k_in, lin.n_out
+    fmt = oracle.FMT_UE5M3 if workload.scale_fmt == "ue5m3" else oracle.FMT_E4M3
+    base = dict(scale_fmt=fmt, seed=workload.sr_seed)
+    rht = dict(rht=workload.rht, seed=workload.rht_seed)
+    t = 8 * which
+    return [
+        ("x", "x", dict(base, tensor_id=t + 0), T),
+        ("xt", "x", dict(base, colwise=True, tensor_id=t + 1, **rht), K),
+        ("w", "w", dict(base, block=oracle.BLOCK_16x16, tensor_id=t + 2), N),
+        ("wt", "w", dict(base, block=oracle.BLOCK_16x16, colwise=True, tensor_id=t + 2), K),
+        ("dy", "dy", dict(base, sr=True, tensor_id=t + 3), T),
+        ("dyt", "dy", dict(base, colwise=True, sr=True, tensor_id=t + 4, **rht), N),
+    ]
+
+
+def oracle_step(workload, quant_frac: float, gemm_samples: int, threads: int, seed: int = 0) -> dict:
+    """Time the CPU oracle on a sample of one step of `workload` with `threads`
+    host threads (the oracle is C behind ctypes, which releases the GIL, so the
+    threads run in parallel) and scale it to the whole step.
+
+    Quantization: the first `quant_frac` of every operand's rows, split into
+    row bands over the threads. Each operand's tensor amax is computed first (a
+    timed pass over the whole tensor, as current scaling does) and handed to the
+    band calls as a held amax, which gives the same scale as current scaling, so
+    the bands do not each repeat it. GEMMs: `gemm_samples` outputs of each of
+    the step's three GEMMs per linear, at random inside the quantized rows,
+    split over the threads; each GEMM's time is scaled by (outputs of the GEMM
+    / outputs sampled). Returns the step's GEMM FLOPs, the measured and the
+    whole-step (scaled) seconds, and a description of the sample."""
+    import numpy as np
+
+    import oracle
     oracle.build()
-    flops, elapsed = 0.0, 0.0
+    rng = np.random.default_rng(seed)
+    pool = cf.ThreadPoolExecutor(max_workers=threads)
+    t_quant = t_quant_scaled = t_gemm = t_gemm_scaled = 0.0
+    flops = 0.0
+    n_gemm = 0
     for which, lin in enumerate(workload.linears):
-        key = (workload.name, which)
-        if key not in _INPUT_CACHE:
-            _INPUT_CACHE[key] = linear_inputs(workload, which)
-        inp = _INPUT_CACHE[key]
-        Ts, Fs = tokens, feats
-        x = inp["x"][:Ts].copy()
-        dy = inp["dy"][:Ts].copy()
+        inp = workload_inputs(workload, which)
+        specs = _operand_specs(workload, which)
+        q = {}
+        # every operand's tensor amax over the whole tensor (one pass each, in parallel)
         t0 = time.perf_counter()
-        qx = oracle.quantize(x, tensor_id=8 * which + 0)
-        qxt = oracle.quantize(x, colwise=True, rht=True, seed=workload.rht_seed, tensor_id=8 * which + 1,
-                              op_rows=(0, Fs))
-        qw = oracle.quantize(inp["w"], block=oracle.BLOCK_16x16, tensor_id=8 * which + 2, op_rows=(0, Fs))
-        qwt = oracle.quantize(inp["w"], block=oracle.BLOCK_16x16, colwise=True, tensor_id=8 * which + 2,
-                              op_rows=(0, Fs))
-        qdy = oracle.quantize(dy, sr=True, seed=workload.sr_seed, tensor_id=8 * which + 3)
-        qdyt = oracle.quantize(dy, colwise=True, rht=True, sr=True, seed=workload.sr_seed,
-                               tensor_id=8 * which + 4, op_rows=(0, Fs))
-        oracle.gemm(qx["codes"], qx["scales"], qx["s_dec"], qw["codes"], qw["scales"], qw["s_dec"])
-        oracle.gemm(qdy["codes"], qdy["scales"], qdy["s_dec"], qwt["codes"], qwt["scales"], qwt["s_dec"])
-        oracle.gemm(qdyt["codes"], qdyt["scales"], qdyt["s_dec"], qxt["codes"], qxt["scales"], qxt["s_dec"])
-        elapsed += time.perf_counter() - t0
-        flops += 2.0 * (Ts * Fs * lin.k_in + Ts * Fs * lin.n_out + Fs * Fs * Ts)
-    return {"flops": flops, "seconds": elapsed}
+        amaxes = list(pool.map(lambda sp: oracle.tensor_amax(inp[sp[1]], colwise=sp[2].get("colwise", False),
+                                                             rht=sp[2].get("rht", False), seed=sp[2].get("seed", 0)),
+                               specs))
+        dt_amax = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        for (name, src, kw, R), amax in zip(specs, amaxes):
+            bits = inp[src]
+            rows = max(16, int(R * quant_frac) // 16 * 16)
+            nb = max(1, min(threads, rows // 16))
+            edges = [rows * i // nb // 16 * 16 for i in range(nb)] + [rows]
+
+            def band(r0, r1, bits=bits, kw=kw, amax=amax):
+                st = oracle.HeldState()
+                st.amax[0], st.valid[0], st.last[0] = amax, 1, 0
+                # held amax, step 1 (not a refresh step): the tensor scale of current scaling
+                return oracle.quantize(bits, held=True, state=st, step=1, op_rows=(r0, r1), **kw)
+
+            parts = list(pool.map(lambda e: band(*e), zip(edges[:-1], edges[1:])))
+            q[name] = ({k: np.concatenate([p[k] for p in parts]) for k in ("codes", "scales")}
+                       | {"s_dec": parts[0]["s_dec"]}, rows)
+        dt = time.perf_counter() - t0
+        t_quant += dt_amax + dt
+        t_quant_scaled += dt_amax + dt / quant_frac
+        for ka, kb in (("x", "w"), ("dy", "wt"), ("dyt", "xt")):
+            (ra, ma), (rb, nbr) = q[ka], q[kb]
+            M = {"x": lin.tokens, "dy": lin.tokens, "dyt": lin.n_out}[ka]
+            N = {"w": lin.n_out, "wt": lin.k_in, "xt": lin.k_in}[kb]
+            K = ra["codes"].shape[1] * 2
+            ms = rng.integers(0, ma, gemm_samples)
+            ns = rng.integers(0, nbr, gemm_samples)
+            chunks = np.array_split(np.arange(gemm_samples), threads)
+            fmt = oracle.FMT_UE5M3 if workload.scale_fmt == "ue5m3" else oracle.FMT_E4M3
+            t0 = time.perf_counter()
+            list(pool.map(lambda c: oracle.gemm(ra["codes"], ra["scales"], ra["s_dec"], rb["codes"], rb["scales"],
+                                                rb["s_dec"], scale_fmt=fmt, pairs=(ms[c], ns[c])),
+                          [c for c in chunks if c.size]))
+            dt = time.perf_counter() - t0
+            t_gemm += dt
+            t_gemm_scaled += dt * (M * N) / gemm_samples
+            flops += 2.0 * M * N * K
+            n_gemm += 1
+    pool.shutdown()
+    return {"flops": flops, "seconds_measured": t_quant + t_gemm, "seconds_step": t_quant_scaled + t_gemm_scaled,
+            "quant_seconds_step": t_quant_scaled, "gemm_seconds_step": t_gemm_scaled,
+            "sample": f"{quant_frac:g} of every operand's rows quantized (tensor amax over the whole tensor) and "
+                      f"{gemm_samples} sampled outputs of each of the {n_gemm} GEMMs, scaled to the whole step"}
 
 
-def cpu_baseline_entry(workload, tokens: int, feats: int, min_seconds: float = 10.0) -> dict:
-    flops = secs = 0.0
-    reps = 0
-    while secs < min_seconds and reps < 20:
-        s = oracle_sample(workload, tokens, feats)
-        flops += s["flops"]
-        secs += s["seconds"]
-        reps += 1
-    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x (every linear of the step on {tokens} tokens and {feats} x {feats} output/input "
-                      f"features: quantizations of those slices plus the three GEMMs), single-threaded C oracle, "
-                      f"{secs:.1f} s"}
+def cpu_baseline_entry(workload) -> dict:
+    """The oracle on this machine's host cores: every operand quantized in full
+    and GEMM outputs sampled (all cores); plus the same on one thread over a
+    sixteenth of the rows, for the single-thread figure."""
+    cores = os.cpu_count() or 1
+    full = oracle_step(workload, 1.0, 256 * cores, cores)
+    one = oracle_step(workload, 1.0 / 16, 64, 1, seed=1)
+    return {"value": full["flops"] / full["seconds_step"] / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "sample": full["sample"] + f"; {full['seconds_measured']:.1f} s measured on "
+                                                          f"{cores} threads",
+            "step_seconds": full["seconds_step"], "quantize_seconds_per_step": full["quant_seconds_step"],
+            "single_thread": {"value": one["flops"] / one["seconds_step"] / 1e12, "cores": 1,
+                              "sample": one["sample"] + f"; {one['seconds_measured']:.1f} s measured"}}
 
 
 # --------------------------------------------------------------------------- distributed
@@ -189,27 +272,29 @@ def max_over_ranks(dist, v: float) -> float:
 
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, workload):
+    """The CPU oracle as the reference arm: each step quantizes a sixteenth of
+    every operand's rows and samples GEMM outputs on all host cores, scaled to
+    the whole step. Rank 0 alone runs it."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    times, flops = [], 0.0
-    for _ in range(args.warmup):
-        oracle_sample(workload, args.ref_tokens, args.ref_feats)
-    for _ in range(args.steps):
-        s = oracle_sample(workload, args.ref_tokens, args.ref_feats)
-        times.append(s["seconds"])
-        flops = s["flops"]
-    total = sum(times)
-    value = flops * len(times) / total / 1e12
+    cores = os.cpu_count() or 1
+    frac, samples = 1.0 / 16, 16 * cores
+    for i in range(args.warmup):
+        oracle_step(workload, frac, samples, cores, seed=100 + i)
+    steps = [oracle_step(workload, frac, samples, cores, seed=i) for i in range(args.steps)]
+    flops = steps[0]["flops"]
+    sec = sum(s["seconds_step"] for s in steps) / len(steps)
+    value = flops / sec / 1e12
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64 (oracle)", "data": "synthetic",
-            "impl": "reference",
-            "config": {"workload": workload.name, "sample_tokens": args.ref_tokens,
-                       "sample_features": args.ref_feats},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: every linear on {args.ref_tokens} tokens and "
-                                       f"{args.ref_feats} x {args.ref_feats} features, single-threaded C oracle"},
+            "warmup": args.warmup, "ms_per_step": 1e3 * sec, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 steps, f64 GEMM sums (oracle)",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload.name, "tokens": workload.linears[0].tokens,
+                       "linears_k_n": [[l.k_in, l.n_out] for l in workload.linears]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": steps[0]["sample"] + f", {cores} threads; each step "
+                                                            f"{sum(s['seconds_measured'] for s in steps) / len(steps):.1f} s measured"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -220,50 +305,63 @@ def run_gpu(args, workload):
     import torch
 
     import fp4_block_scaled_02_gb300 as fb
-    from workloads import linear_inputs
 
     dist, rank, world = dist_setup()
     dev = torch.cuda.current_device()
     fb._lib.load()
     stream = torch.cuda.current_stream()
+    sweep = workload.held
+    ue = workload.scale_fmt == "ue5m3"
+    target_T = workload.targets[0]
+
+    def upload(bits):
+        return torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
 
     # inputs: seeded synthetic BF16, uploaded once (resident in HBM)
     layers, host = [], []
     for which, lin in enumerate(workload.linears):
-        inp = linear_inputs(workload, which)
-        dev_in = {k: torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16) for k, v in inp.items()}
-        L = fb.Fp4Linear(lin.tokens, lin.k_in, lin.n_out, rht=workload.rht, seed=workload.rht_seed, layer=which)
+        inp = workload_inputs(workload, which)
+        dev_in = {k: upload(v) for k, v in inp.items()}
+        if sweep:
+            # the sweep's gradient of step s: the base gradient times
+            # 10^(-3 + 6 s / (steps - 1)) rounded to BF16 (FP32 product, RNE)
+            base = dev_in["dy"].float()
+            dev_in["dy_steps"] = [(base * torch.tensor(10.0 ** (-3.0 + 6.0 * s / (workload.steps - 1)),
+                                                       dtype=torch.float32, device="cuda")).to(torch.bfloat16)
+                                  for s in range(workload.steps)]
+            del base
+        L = fb.Fp4Linear(lin.tokens, lin.k_in, lin.n_out, rht=workload.rht, seed=workload.rht_seed, layer=which,
+                         scale_fmt=fb.FP4_SCALE_UE5M3 if ue else fb.FP4_SCALE_E4M3, held=sweep, target_T=target_T)
         outs = {"y": torch.empty((lin.tokens, lin.n_out), dtype=torch.bfloat16, device="cuda"),
                 "dx": torch.empty((lin.tokens, lin.k_in), dtype=torch.bfloat16, device="cuda"),
                 "dw": torch.empty((lin.n_out, lin.k_in), dtype=torch.float32, device="cuda")}
         layers.append((lin, L, dev_in, outs))
-        host.append({k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-                     for k, v in inp.items()})
+        h = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in inp.items()}
+        if sweep:
+            # two pinned gradients (steps 0 and 99) alternate in the end-to-end run
+            h["dy_steps"] = [dev_in["dy_steps"][0].cpu().pin_memory(), dev_in["dy_steps"][-1].cpu().pin_memory()]
+        host.append(h)
 
-    gemm_flops = sum(3 * 2.0 * lin.tokens * lin.k_in * lin.n_out for lin, *_ in layers)
-    quant_bytes = sum(BYTES_TWO_OPERANDS * (lin.tokens * (lin.k_in + lin.n_out) + lin.n_out * lin.k_in)
-                      for lin, *_ in layers)
-    # per linear: 3 x (amax + quantize) + 3 GEMMs; with the amaxes on a side
-    # stream, each amax launch becomes two (tile pass + finalize)
-    launches_per_step = sum(12 if L.side is not None else 9 for _, L, _, _ in layers)
-    q_launches = launches_per_step - 3 * len(layers)
+    gemm_flops = workload.gemm_flops_per_step()
+    # kernels launched per step: per linear, each quantize call is an amax launch
+    # plus a conversion launch (with the amaxes on the side stream: a tile pass and
+    # a finalize kernel each); the UE5M3 GEMMs run the rebias pass, the native
+    # kernel and the emulated fallback (which returns at once) each
+    per_linear = (12 if layers[0][1].side is not None else 6 + (9 if ue else 3))
+    launches_per_step = per_linear * len(layers)
 
-    def step(ev=None):
+    def dy_of(di, i):
+        return di["dy_steps"][i % workload.steps] if sweep else di["dy"]
+
+    def step(i, mark=None):
         for lin, L, di, o in layers:
-            if ev is not None:
-                ev.append(torch.cuda.Event(enable_timing=True))
-                ev[-1].record(stream)
-            L.quantize_all(di["x"], di["w"], di["dy"], stream=stream)
-            if ev is not None:
-                ev.append(torch.cuda.Event(enable_timing=True))
-                ev[-1].record(stream)
-            L.gemms(o["y"], o["dx"], o["dw"], stream=stream)
-            if ev is not None:
-                ev.append(torch.cuda.Event(enable_timing=True))
-                ev[-1].record(stream)
+            L.step(di["x"], di["w"], dy_of(di, i), o["y"], o["dx"], o["dw"], step=i if sweep else 0,
+                   stream=stream, mark=mark)
 
+    it = 0
     for _ in range(args.warmup):
-        step()
+        step(it)
+        it += 1
     torch.cuda.synchronize()
     status = fb.fp4_device_status()
     if status != 0:
@@ -275,46 +373,93 @@ def run_gpu(args, workload):
     time.sleep(0.3)
     barrier(dist)
     torch.cuda.synchronize()
+    timed_steps = list(range(it, it + args.steps))
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in timed_steps:
+        step(i)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     ms = max_over_ranks(dist, start.elapsed_time(end))
-    # the quantize / GEMM split for the roofline: the same steps again with
-    # events between the groups (kept out of the timed steps above: an event
-    # between two kernels stops the second from launching early)
+    it += args.steps
+    # per-kernel times: the same steps again with an event before and after each
+    # launch on the stream (kept out of the timed steps above: an event between
+    # two kernels stops the second from launching early)
     evs = []
-    for _ in range(args.steps):
-        step(evs)
-    torch.cuda.synchronize()
+
+    def mark(label):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        evs.append((label, e))
+
+    per_label = {}
+    for n in range(args.steps):
+        evs.clear()
+        step(timed_steps[n], mark=mark)
+        torch.cuda.synchronize()
+        open_ = {}
+        li = 0
+        for label, e in evs:
+            if label.endswith("/end"):
+                name = label[:-4]
+                per_label.setdefault((li // 6, name), []).append(open_.pop(name).elapsed_time(e))
+                li += 1
+            else:
+                open_[label] = e
     clk = clocks.stop()
-    q_ms = sum(evs[i].elapsed_time(evs[i + 1]) for i in range(0, len(evs), 3))
-    g_ms = sum(evs[i + 1].elapsed_time(evs[i + 2]) for i in range(0, len(evs), 3))
-    ms_step = ms / args.steps
-    value = world * gemm_flops / (ms_step * 1e-3) / 1e12
-    gemm_tflops = gemm_flops * args.steps / (g_ms * 1e-3) / 1e12
-    quant_gbs = quant_bytes * args.steps / (q_ms * 1e-3) / 1e9
     status = fb.fp4_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
+    ms_step = ms / args.steps
+    value = world * gemm_flops / (ms_step * 1e-3) / 1e12
+
+    # the dominant kernels against their rooflines
+    def gemm_shape(lin, name):
+        return {"fprop": (lin.tokens, lin.n_out, lin.k_in), "dgrad": (lin.tokens, lin.k_in, lin.n_out),
+                "wgrad": (lin.n_out, lin.k_in, lin.tokens)}[name]
+
+    g_flop = g_ms = q_bytes = q_ms = 0.0
+    g_n = q_n = 0
+    for (li, name), times in per_label.items():
+        lin = layers[li][0]
+        t = sum(times)
+        if name in GEMM_LABELS:
+            M, N, K = gemm_shape(lin, name)
+            g_flop += 2.0 * M * N * K * len(times)
+            g_ms += t
+            g_n += len(times)
+        elif name in ("x", "dy"):
+            elems = lin.tokens * (lin.k_in if name == "x" else lin.n_out)
+            for s in timed_steps:
+                # held scaling reads the input a second time for its amax on refresh steps
+                refresh = sweep and s % 50 == 0
+                q_bytes += elems * (BYTES_ONE_PASS_TWO_OPERANDS + (BYTES_AMAX_PASS if refresh else 0.0))
+            q_ms += t
+            q_n += len(times)
+    all_quant_ms = sum(sum(v) for (li, n), v in per_label.items() if n in QUANT_LABELS)
+    gemm_tflops = g_flop / (g_ms * 1e-3) / 1e12
+    dual_gbs = q_bytes / (q_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API: pinned host inputs in, outputs back
-    h2d = sum(t.numel() * t.element_size() for h in host for t in h.values())
+    def h2d_bytes():
+        return sum(t.numel() * t.element_size() for h in host for k, t in h.items() if k != "dy_steps")
+
     host_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in o.items()}
                 for (_, _, _, o) in layers]
+    h2d = h2d_bytes()
     d2h = sum(t.numel() * t.element_size() for h in host_out for t in h.values())
 
     # Fp4Linear.step_host: input copies, the step and output copies on their own
     # streams, so one linear's copies overlap the other's compute
-    def e2e_step():
+    def e2e_step(i):
         for (lin, L, di, o), h, ho in zip(layers, host, host_out):
-            L.step_host(h["x"], h["w"], h["dy"], ho["y"], ho["dx"], ho["dw"], stream=stream)
+            dy_h = h["dy_steps"][i % 2] if sweep else h["dy"]
+            L.step_host(h["x"], h["w"], dy_h, ho["y"], ho["dx"], ho["dw"], step=i if sweep else 0, stream=stream)
 
     for _ in range(max(1, args.warmup)):
-        e2e_step()
+        e2e_step(it)
+        it += 1
     torch.cuda.synchronize()
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -322,13 +467,16 @@ def run_gpu(args, workload):
     for _, L, _, _ in layers:
         L.h2d_stream.wait_event(e0)  # no copy starts before the timed region
     for _ in range(args.steps):
-        e2e_step()
+        e2e_step(it)
+        it += 1
     for _, L, _, _ in layers:
         stream.wait_event(L.ev_out)  # ... and the last output copies end inside it
     e1.record(stream)
     torch.cuda.synchronize()
     e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.steps
     e2e_value = world * gemm_flops / (e_ms * 1e-3) / 1e12
+    if fb.fp4_device_status() != 0:
+        raise RuntimeError("device status after the end-to-end run")
 
     if rank != 0:
         return
@@ -336,29 +484,40 @@ def run_gpu(args, workload):
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     hbm_peak = peaks["hbm_gbs"]
     traffic = load_traffic()
+    wl = args.workload
     gemm_roof = {"bound": "tensor", "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
-                 "frac": gemm_tflops / fp4_peak, "traffic": traffic.get("gemm"),
+                 "frac": gemm_tflops / fp4_peak, "traffic": traffic.get(f"gemm_nvfp4_kernel@{wl}"),
                  "peak_source": f"{src} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
-                 "kernel": "gemm_nvfp4_kernel (6 launches per step)"}
-    quant_roof = {"bound": "hbm", "achieved": quant_gbs, "peak": hbm_peak, "unit": "GB/s",
-                  "frac": quant_gbs / hbm_peak, "traffic": traffic.get("quantize"),
+                 "kernel": f"gemm_nvfp4_kernel ({g_n // args.steps} launches per step: Fprop, Dgrad, Wgrad of each "
+                           f"linear), CUDA events around each launch",
+                 "ms_per_launch": g_ms / max(1, g_n)}
+    quant_roof = {"bound": "hbm", "achieved": dual_gbs, "peak": hbm_peak, "unit": "GB/s",
+                  "frac": dual_gbs / hbm_peak, "traffic": traffic.get(f"quantize_dual_kernel@{wl}"),
                   "peak_source": f"{src} hbm_gbs",
-                  "kernel": f"amax + quantize kernels ({q_launches} launches per step)"}
-    dominant, other = (gemm_roof, quant_roof) if g_ms >= q_ms else (quant_roof, gemm_roof)
-    cpu = cpu_baseline_entry(workload, args.ref_tokens, args.ref_feats) if not args.no_cpu_baseline else None
+                  "kernel": f"quantize_dual_kernel ({q_n // args.steps} launches per step: X and dY of each linear, "
+                            f"{BYTES_ONE_PASS_TWO_OPERANDS} B per input element"
+                            + (", + 2 on held-amax refresh steps" if sweep else ", tensor amax given") + ")",
+                  "ms_per_launch": q_ms / max(1, q_n)}
+    cpu = None if args.no_cpu_baseline else cpu_baseline_entry(workload)
     lin_desc = [[l.k_in, l.n_out] for l in workload.linears]
+    recipe = ("UE5M3: 1x16 UE5M3 acts/grads, 16x16 weights, held amax refreshed every 50 steps "
+              f"(T = {target_T:g}), SR on dY, no RHT, rebiased native GEMMs"
+              if sweep else "NVFP4: 1x16 E4M3 acts/grads, 16x16 weights, current scaling, SR on dY, "
+                            "RHT16 on Wgrad inputs")
+    cfg = {"workload": workload.name, "tokens": workload.linears[0].tokens, "linears_k_n": lin_desc,
+           "recipe": recipe,
+           "l2": "inputs larger than L2 (%.0f MB of BF16 inputs per step)" % (h2d / 1e6),
+           "parallelism": f"replicas x{world}"}
+    if sweep:
+        cfg["sweep_steps_timed"] = [timed_steps[0], timed_steps[-1]]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1 (fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": workload.name, "tokens": workload.linears[0].tokens, "linears_k_n": lin_desc,
-                   "recipe": "NVFP4: 1x16 E4M3 acts/grads, 16x16 weights, current scaling, SR on dY, "
-                             "RHT16 on Wgrad inputs",
-                   "l2": "inputs larger than L2 (%.0f MB of BF16 inputs per step)" % (h2d / 1e6),
-                   "parallelism": f"replicas x{world}"},
-        "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs,
-        "ms_gemm_per_step": g_ms / args.steps, "ms_quantize_per_step": q_ms / args.steps,
-        "roofline": dominant, "roofline_other": other,
+        "config": cfg,
+        "gemm_tflops": gemm_tflops, "quantize_dual_gbs": dual_gbs,
+        "ms_gemm_per_step": g_ms / args.steps, "ms_quantize_calls_per_step": all_quant_ms / args.steps,
+        "roofline": gemm_roof, "roofline_quantize": quant_roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e_ms},
@@ -369,7 +528,8 @@ def run_gpu(args, workload):
 
 
 def load_traffic() -> dict:
-    """Per-launch DRAM bytes from the committed ncu summary (profiles/traffic.json), if present."""
+    """Per-launch DRAM bytes (kernel@workload) from the committed ncu summaries
+    (profiles/traffic.json), if present."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(path):
         try:
@@ -466,6 +626,11 @@ def run_kernels(args):
             orient=fb.FP4_ORIENT_COLWISE, rht=True), x, o_r, o_c, ws=ws), 5.125),
         "dual_sr_rht": (lambda: fb.fp4_quantize_dual(fb.QuantConfig(round=SR), fb.QuantConfig(
             round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True), x, o_r, o_c, ws=ws), 5.125),
+        # the conversion pass alone (tensor amax given, as in the step)
+        "dual_sr_rht_given": (lambda: fb.fp4_quantize_dual(
+            fb.QuantConfig(round=SR, tscale=fb.FP4_TSCALE_GIVEN),
+            fb.QuantConfig(round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True, tscale=fb.FP4_TSCALE_GIVEN),
+            x, o_r, o_c, st_r, st_c), 3.125),
         "mxfp4_rows": (lambda: fb.fp4_quantize(fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE8M0, block=fb.FP4_BLOCK_1x32),
                                                x, o_mx), 2.53125),
         # per-row tensor scales: one pass, so the input is read once (2 + 0.5625 B/elem)
@@ -479,6 +644,9 @@ def run_kernels(args):
     o_mx = fb.QTensor.empty(T, C, fb.FP4_SCALE_UE8M0)
     o_rr = fb.QTensor.empty(T, C, per_row=True)
     st_r, st_c = fb.AmaxState(), fb.AmaxState()
+    # the given-amax calls read the records a tensor-amax call leaves
+    fb.fp4_tensor_amax_dual(fb.QuantConfig(), fb.QuantConfig(orient=fb.FP4_ORIENT_COLWISE, rht=True), x, st_r, st_c,
+                            ws)
     for name, (fn, bpe) in quants.items():
         if not wanted(f"quantize_{name}_{T}x{C}"):
             continue
@@ -507,9 +675,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="1.2b")
-    ap.add_argument("--ref-tokens", type=int, default=16)
-    ap.add_argument("--ref-feats", type=int, default=256)
+    ap.add_argument("--workload", default="8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="time single library calls instead of the step")
     ap.add_argument("--only", default=None, help="with --kernels: time only the calls whose key matches this regex")

@@ -26,7 +26,8 @@ from ._lib import (FP4_BLOCK_1x16, FP4_BLOCK_1x32, FP4_BLOCK_16x16, FP4_LAYOUT_P
 
 __all__ = ["QTensor", "QuantConfig", "AmaxState", "fp4_quantize", "fp4_quantize_dual", "fp4_dequantize", "fp4_gemm",
            "fp4_gemm_workspace_bytes", "fp4_tensor_amax", "fp4_tensor_amax_dual", "fp4_linear_fprop", "fp4_linear_dgrad", "fp4_linear_wgrad", "fp4_device_status",
-           "fp4_workspace_bytes", "fp4_quantized_sizes", "Fp4Error", "Fp4Linear"]
+           "fp4_device_status_record", "fp4_workspace_bytes", "fp4_quantized_sizes", "row_stride", "Fp4Error",
+           "Fp4Linear"]
 
 
 def _ptr(t: torch.Tensor | None):
@@ -126,16 +127,25 @@ def fp4_workspace_bytes(cfg: QuantConfig, rows: int, cols: int) -> int:
     return _lib.load().fp4_workspace_bytes(ctypes.byref(p), rows, cols)
 
 
+def row_stride(x: torch.Tensor) -> int:
+    """The row stride (ld, in elements) of a 2-D BF16 matrix whose rows are
+    contiguous, e.g. a column slice of a wider buffer."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and (x.stride(1) == 1 or x.shape[1] <= 1), \
+        "rows must be contiguous"
+    return x.stride(0) if x.shape[0] > 1 else x.shape[1]
+
+
 def fp4_quantize(cfg: QuantConfig, x: torch.Tensor, out: QTensor, out_t: QTensor | None = None,
                  state: AmaxState | None = None, counters: torch.Tensor | None = None,
                  ws: torch.Tensor | None = None, stream=None) -> None:
-    """Quantize the row-major BF16 matrix `x` into `out` (see fp4_quantize in fp4bs.h)."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    """Quantize the row-major BF16 matrix `x` into `out` (see fp4_quantize in
+    fp4bs.h); `x` may be a view whose rows lie further apart than its width."""
+    ld = row_stride(x)
     p = cfg.params()
     d = out.desc()
     dt = out_t.desc() if out_t is not None else None
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
-    st = _lib.load().fp4_quantize(ctypes.byref(p), _ptr(x), x.shape[0], x.shape[1], ctypes.byref(d),
+    st = _lib.load().fp4_quantize(ctypes.byref(p), _ptr(x), x.shape[0], x.shape[1], ld, ctypes.byref(d),
                                   ctypes.byref(dt) if dt is not None else None,
                                   _ptr(state.buf) if state is not None else None, _ptr(counters), _ptr(ws),
                                   ws_bytes, _stream(stream))
@@ -147,11 +157,11 @@ def fp4_quantize_dual(cfg_row: QuantConfig, cfg_col: QuantConfig, x: torch.Tenso
                       counters_row: torch.Tensor | None = None, counters_col: torch.Tensor | None = None,
                       ws: torch.Tensor | None = None, stream=None) -> None:
     """Rowwise and colwise quantization of `x` in one pass (see fp4_quantize_dual in fp4bs.h)."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    ld = row_stride(x)
     pr, pc = cfg_row.params(), cfg_col.params()
     dr, dc = out_row.desc(), out_col.desc()
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
-    st = _lib.load().fp4_quantize_dual(ctypes.byref(pr), ctypes.byref(pc), _ptr(x), x.shape[0], x.shape[1],
+    st = _lib.load().fp4_quantize_dual(ctypes.byref(pr), ctypes.byref(pc), _ptr(x), x.shape[0], x.shape[1], ld,
                                        ctypes.byref(dr), ctypes.byref(dc),
                                        _ptr(state_row.buf) if state_row is not None else None,
                                        _ptr(state_col.buf) if state_col is not None else None,
@@ -165,9 +175,9 @@ AMAX_WS_BYTES = 2 * 2048 * 4  # workspace of fp4_tensor_amax / fp4_tensor_amax_d
 def fp4_tensor_amax(cfg: QuantConfig, x: torch.Tensor, out: AmaxState, ws: torch.Tensor, stream=None) -> None:
     """Tensor amax of the operand `cfg` describes into `out` (fp4_tensor_amax in fp4bs.h), for a later
     fp4_quantize with tscale FP4_TSCALE_GIVEN."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    ld = row_stride(x)
     p = cfg.params()
-    _lib.check(_lib.load().fp4_tensor_amax(ctypes.byref(p), _ptr(x), x.shape[0], x.shape[1], _ptr(out.buf),
+    _lib.check(_lib.load().fp4_tensor_amax(ctypes.byref(p), _ptr(x), x.shape[0], x.shape[1], ld, _ptr(out.buf),
                                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
                "fp4_tensor_amax")
 
@@ -175,9 +185,9 @@ def fp4_tensor_amax(cfg: QuantConfig, x: torch.Tensor, out: AmaxState, ws: torch
 def fp4_tensor_amax_dual(cfg_row: QuantConfig, cfg_col: QuantConfig, x: torch.Tensor, out_row: AmaxState,
                          out_col: AmaxState, ws: torch.Tensor, stream=None) -> None:
     """Rowwise and colwise operand amaxes of `x` from one read (fp4_tensor_amax_dual in fp4bs.h)."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    ld = row_stride(x)
     pr, pc = cfg_row.params(), cfg_col.params()
-    _lib.check(_lib.load().fp4_tensor_amax_dual(ctypes.byref(pr), ctypes.byref(pc), _ptr(x), x.shape[0], x.shape[1],
+    _lib.check(_lib.load().fp4_tensor_amax_dual(ctypes.byref(pr), ctypes.byref(pc), _ptr(x), x.shape[0], x.shape[1], ld,
                                                 _ptr(out_row.buf), _ptr(out_col.buf), _ptr(ws),
                                                 ws.numel() * ws.element_size(), _stream(stream)),
                "fp4_tensor_amax_dual")
@@ -239,7 +249,20 @@ def fp4_device_status(stream=None) -> int:
     return _lib.load().fp4_device_status(_stream(stream))
 
 
+def fp4_device_status_record(dst: torch.Tensor, stream=None) -> None:
+    """In stream order, write the device status word into dst[0] (int32, device
+    or pinned host memory) and clear it, without synchronising
+    (fp4_device_status_record in fp4bs.h)."""
+    assert dst.dtype == torch.int32 and dst.numel() >= 1
+    _lib.check(_lib.load().fp4_device_status_record(_ptr(dst), _stream(stream)), "fp4_device_status_record")
+
+
 # --------------------------------------------------------------------------- linear layer
+def _mark(mark, label: str) -> None:
+    if mark is not None:
+        mark(label)
+
+
 @dataclass
 class Fp4Linear:
     """One FP4 quantized linear layer Y = X W^T with its backward GEMMs
@@ -310,16 +333,20 @@ class Fp4Linear:
         base.update(kw)
         return QuantConfig(**base)
 
-    def quantize_all(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor, step: int = 0, stream=None):
+    def quantize_all(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor, step: int = 0, stream=None,
+                     mark=None):
         """X -> X (rowwise) and X^T (colwise + RHT) in one pass; W -> W and W^T
         (16x16); dY -> dY (rowwise, SR) and dY^T (colwise + RHT, SR) in one pass.
-        Falls back to separate calls for shapes the one-pass kernel does not take."""
+        Falls back to separate calls for shapes the one-pass kernel does not take.
+        `mark`, if given, is called with a label before ("x") and after
+        ("x/end") each call issued on the caller's stream (for timing)."""
         b, c = self.bufs, self.counters
         rht = self.rht
         dual_ok = self.tokens % 128 == 0 and self.k_in % 128 == 0 and self.n_out % 128 == 0
         if self.side is not None:
-            self._quantize_all_overlapped(x, w, dy, step, stream)
+            self._quantize_all_overlapped(x, w, dy, step, stream, mark)
             return
+        _mark(mark, "x")
         if dual_ok:
             fp4_quantize_dual(self._cfg(0, step), self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x,
                               b["x"], b["xt"], self.states[0], self.states[1], c[0], c[1], ws=self.ws,
@@ -329,8 +356,12 @@ class Fp4Linear:
                          stream=stream)
             fp4_quantize(self._cfg(1, step, orient=FP4_ORIENT_COLWISE, rht=rht), x, b["xt"], state=self.states[1],
                          counters=c[1], ws=self.ws, stream=stream)
+        _mark(mark, "x/end")
+        _mark(mark, "w")
         fp4_quantize(self._cfg(2, step, block=FP4_BLOCK_16x16, emit_transpose=True), w, b["w"], b["wt"],
                      state=self.states[2], counters=c[2], ws=self.ws, stream=stream)
+        _mark(mark, "w/end")
+        _mark(mark, "dy")
         if dual_ok:
             fp4_quantize_dual(self._cfg(3, step, round=FP4_ROUND_SR),
                               self._cfg(4, step, orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR), dy,
@@ -341,8 +372,9 @@ class Fp4Linear:
                          ws=self.ws, stream=stream)
             fp4_quantize(self._cfg(4, step, orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR), dy, b["dyt"],
                          state=self.states[4], counters=c[4], ws=self.ws, stream=stream)
+        _mark(mark, "dy/end")
 
-    def _quantize_all_overlapped(self, x, w, dy, step, stream):
+    def _quantize_all_overlapped(self, x, w, dy, step, stream, mark=None):
         # side stream: the tensor amaxes of W (smallest, first), X and dY; main
         # stream: W, X and dY quantized with them as each becomes ready, so only
         # W's amax pass is not hidden behind a conversion pass
@@ -367,29 +399,40 @@ class Fp4Linear:
                              stream=side)
         self.ev_amax[2].record(side)
         main.wait_event(self.ev_amax[0])
+        _mark(mark, "w")
         fp4_quantize(self._cfg(2, step, emit_transpose=True, **w_cfg, **giv), w, b["w"], b["wt"], state=g[2],
                      counters=c[2], stream=main)
+        _mark(mark, "w/end")
         main.wait_event(self.ev_amax[1])
+        _mark(mark, "x")
         fp4_quantize_dual(self._cfg(0, step, **giv), self._cfg(1, step, **x_c, **giv), x, b["x"], b["xt"], g[0], g[1],
                           c[0], c[1], stream=main)
+        _mark(mark, "x/end")
         main.wait_event(self.ev_amax[2])
+        _mark(mark, "dy")
         fp4_quantize_dual(self._cfg(3, step, **dy_r, **giv), self._cfg(4, step, **dy_c, **giv), dy, b["dy"], b["dyt"],
                           g[3], g[4], c[3], c[4], stream=main)
+        _mark(mark, "dy/end")
 
-    def gemms(self, y: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor, stream=None):
+    def gemms(self, y: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor, stream=None, mark=None):
+        """Fprop, Dgrad and Wgrad (`mark` as for quantize_all)."""
         b = self.bufs
-        if self.gemm_ws is not None:
-            fp4_gemm(b["x"], b["w"], y, stream=stream, ws=self.gemm_ws)
-            fp4_gemm(b["dy"], b["wt"], dx, stream=stream, ws=self.gemm_ws)
-            fp4_gemm(b["dyt"], b["xt"], dw, stream=stream, ws=self.gemm_ws)
-            return
-        fp4_linear_fprop(b["x"], b["w"], y, stream=stream)
-        fp4_linear_dgrad(b["dy"], b["wt"], dx, stream=stream)
-        fp4_linear_wgrad(b["dyt"], b["xt"], dw, stream=stream)
+        for name, (a_, b_), out in (("fprop", ("x", "w"), y), ("dgrad", ("dy", "wt"), dx),
+                                    ("wgrad", ("dyt", "xt"), dw)):
+            _mark(mark, name)
+            if self.gemm_ws is not None:
+                fp4_gemm(b[a_], b[b_], out, stream=stream, ws=self.gemm_ws)
+            elif name == "fprop":
+                fp4_linear_fprop(b[a_], b[b_], out, stream=stream)
+            elif name == "dgrad":
+                fp4_linear_dgrad(b[a_], b[b_], out, stream=stream)
+            else:
+                fp4_linear_wgrad(b[a_], b[b_], out, stream=stream)
+            _mark(mark, name + "/end")
 
-    def step(self, x, w, dy, y, dx, dw, step: int = 0, stream=None):
-        self.quantize_all(x, w, dy, step=step, stream=stream)
-        self.gemms(y, dx, dw, stream=stream)
+    def step(self, x, w, dy, y, dx, dw, step: int = 0, stream=None, mark=None):
+        self.quantize_all(x, w, dy, step=step, stream=stream, mark=mark)
+        self.gemms(y, dx, dw, stream=stream, mark=mark)
 
     def state_dict(self) -> dict:
         """The layer's only state across steps: the five held-amax records

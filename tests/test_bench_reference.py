@@ -1,5 +1,6 @@
 """bench.py's reference arm (the oracle on the host cores) on the CPU: one
-JSON line with the driver contract's keys, on a small sample of the 1.2B step."""
+JSON line with the driver contract's keys, for one step of the 1.2B workload
+(a sixteenth of every operand quantized, GEMM outputs sampled, all cores)."""
 import json
 import os
 import subprocess
@@ -13,9 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 @pytest.mark.timeout(600)
 def test_reference_arm_prints_one_contract_line():
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
-                        "--ref-tokens", "16", "--ref-feats", "128"], cwd=ROOT, env=env, capture_output=True,
-                       text=True, timeout=580)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "1.2b", "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=580)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1, r.stdout
@@ -25,7 +25,7 @@ def test_reference_arm_prints_one_contract_line():
         assert k in d, k
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
     assert d["value"] > 0 and d["steps"] == 1 and d["n_gpus"] == 1
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == os.cpu_count()
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("1.2B")
