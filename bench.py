@@ -661,6 +661,22 @@ def run_kernels(args):
         gbs = 5.125 * w.numel() / (ms * 1e-3) / 1e9
         res["quantize_2d_both_12288x4608"] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
                                               "frac": round(gbs / hbm_peak, 3)}
+    if wanted("quantize_2d_plain_12240x4608"):
+        # rows not a multiple of 64: the 16x16 kernel without TMA tiles (plain scale layout)
+        w = torch.randn((12240, 4608), dtype=torch.bfloat16, device="cuda")
+        lay = dict(layout=fb.FP4_LAYOUT_PLAIN)
+        o1, o2 = fb.QTensor.empty(12240, 4608, **lay), fb.QTensor.empty(4608, 12240, **lay)
+        ms = time_ms(lambda: fb.fp4_quantize(fb.QuantConfig(block=fb.FP4_BLOCK_16x16, emit_transpose=True, **lay), w,
+                                             o1, o2, ws=ws))
+        gbs = 5.125 * w.numel() / (ms * 1e-3) / 1e9
+        res["quantize_2d_plain_12240x4608"] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                                               "frac": round(gbs / hbm_peak, 3)}
+    if wanted(f"dequantize_{T}x{C}"):
+        fb.fp4_quantize(fb.QuantConfig(), x, o_r, ws=ws)
+        y = torch.empty((T, C), dtype=torch.bfloat16, device="cuda")
+        ms = time_ms(lambda: fb.fp4_dequantize(o_r, y))
+        gbs = (0.5625 + 2.0) * T * C / (ms * 1e-3) / 1e9  # codes + scales read, BF16 written
+        res[f"dequantize_{T}x{C}"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 3)}
     status = fb.fp4_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
