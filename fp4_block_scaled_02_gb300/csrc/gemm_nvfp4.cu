@@ -70,7 +70,7 @@ struct GemmParams {
     int* status;
     const int8_t* a_off;      // rebiased UE5M3: per-row power-of-two offsets of A and B
     const int8_t* b_off;
-    const uint8_t* rb_flags;  // rebiased UE5M3: return at once when any of the rb_nflags bytes is set
+    const uint8_t* rb_flags;  // rebiased UE5M3: per 128-row tile, 1 = a row did not fit (emulated kernel's tile)
     int64_t rb_nflags;
     int a_sdec_rows;          // a_sdec holds one decode scale per row of A (App. B.1, per-row scaling)
 };
@@ -143,12 +143,9 @@ template <class Cfg, bool OUT32>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
-    // some row could not be rebiased: the emulated kernel takes this product
-    // (uniform across the grid, before any barrier or tensor memory is set up)
-    if (Cfg::RB) {
-        pdl_wait();
-        if (rb_any_flag(p.rb_flags, p.rb_nflags)) return;
-    }
+    // rebiased UE5M3: the flags of the rebias pass decide which output tiles
+    // this kernel computes (every role skips the same ones)
+    if (Cfg::RB) pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,6 +200,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                if (Cfg::RB && rb_tile_flagged(p.rb_flags, p.M / 128, tile % num_m, tile / num_m, Cfg::BN / 128))
+                    continue;
                 const int64_t mb = tile % num_m, nb = tile / num_m;
                 for (int kb = 0; kb < num_k; ++kb, ++it) {
                     const int s = (int)(it % Cfg::STAGES);
@@ -234,6 +233,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t it = 0, chunk = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                if (Cfg::RB && rb_tile_flagged(p.rb_flags, p.M / 128, tile % num_m, tile / num_m, Cfg::BN / 128))
+                    continue;
                 uint32_t d_tmem = tmem;
                 for (int kb = 0; kb < num_k; ++kb, ++it) {
                     const bool first = kb % Cfg::CHUNK_STAGES == 0;
@@ -293,6 +294,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                if (Cfg::RB && rb_tile_flagged(p.rb_flags, p.M / 128, tile % num_m, tile / num_m, Cfg::BN / 128))
+                    continue;
                 for (int kb = 0; kb < num_k; ++kb, ++it) {
                     const int s = (int)(it % Cfg::STAGES);
                     const uint32_t ph = (it / Cfg::STAGES) & 1u;
@@ -336,6 +339,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         uint32_t chunk = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            if (Cfg::RB && rb_tile_flagged(p.rb_flags, p.M / 128, tile % num_m, tile / num_m, Cfg::BN / 128))
+                continue;
             const int64_t mb = tile % num_m, nb = tile / num_m;
             float acc[Cfg::EPI_COLS];
 #pragma unroll
@@ -597,11 +602,13 @@ __device__ __forceinline__ void ue5m3_normalize(uint32_t code, int& E, int& f) {
 // (part, t) owns row t of the tile in the chunks c = part mod kRbParts; the
 // row's four scales per 512-byte chunk sit at bytes 16 (t % 32) + 4 (t / 32)
 // .. + 3, so the 128 threads of a part read a chunk in one coalesced sweep.
+// Each thread issues kRbBatch independent loads before it uses any (the pass
+// has few CTAs, so it is bound by load latency, not bandwidth).
 // Pass 1 finds the row's largest key 8 E + f and smallest E over its nonzero
 // scales; the offset o puts the largest scale at E4M3 exponent 8 (7 if its
 // mantissa is 7: 0x7F is not a number) and the row fits if the smallest then
 // stays normal (E - o >= -6). Pass 2 writes code ((E - o + 7) << 3) | f, 0 for 0.
-constexpr int kRbParts = 4;
+constexpr int kRbParts = 8, kRbBatch = 8;
 __global__ void __launch_bounds__(128 * kRbParts)
     rebias_ue5m3_kernel(const uint8_t* __restrict__ a_sc, int64_t a_tiles, const uint8_t* __restrict__ b_sc,
                         uint8_t* __restrict__ a_out, uint8_t* __restrict__ b_out, int8_t* __restrict__ a_off,
@@ -616,18 +623,25 @@ __global__ void __launch_bounds__(128 * kRbParts)
     const int woff = 16 * (t & 31) + 4 * (t >> 5);
     int kmax = -1024, emin = 1024;
     bool bad = false;
-#pragma unroll 4
-    for (int64_t c = part; c < nchunks; c += kRbParts) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(src + c * 512 + woff);
+    for (int64_t c0 = part; c0 < nchunks; c0 += (int64_t)kRbParts * kRbBatch) {
+        uint32_t w[kRbBatch];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t code = (w >> (8 * j)) & 0xFFu;
-            if (code == 0u) continue;
-            bad |= code == 0xFFu;
-            int E, f;
-            ue5m3_normalize(code, E, f);
-            kmax = max(kmax, 8 * E + f);
-            emin = min(emin, E);
+        for (int u = 0; u < kRbBatch; ++u) {
+            const int64_t c = c0 + (int64_t)u * kRbParts;
+            w[u] = c < nchunks ? *reinterpret_cast<const uint32_t*>(src + c * 512 + woff) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kRbBatch; ++u) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t code = (w[u] >> (8 * j)) & 0xFFu;
+                if (code == 0u) continue;
+                bad |= code == 0xFFu;
+                int E, f;
+                ue5m3_normalize(code, E, f);
+                kmax = max(kmax, 8 * E + f);
+                emin = min(emin, E);
+            }
         }
     }
     kmax_s[part][t] = kmax;
@@ -647,20 +661,29 @@ __global__ void __launch_bounds__(128 * kRbParts)
     if (part == 0) (is_a ? a_off : b_off)[rt * 128 + t] = (int8_t)o;
     const int any_bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) flags[blockIdx.x] = any_bad ? 1 : 0;
-#pragma unroll 4
-    for (int64_t c = part; c < nchunks; c += kRbParts) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(src + c * 512 + woff);
-        uint32_t out = 0u;
+    for (int64_t c0 = part; c0 < nchunks; c0 += (int64_t)kRbParts * kRbBatch) {
+        uint32_t w[kRbBatch];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t code = (w >> (8 * j)) & 0xFFu;
-            if (code == 0u || code == 0xFFu) continue;
-            int E, f;
-            ue5m3_normalize(code, E, f);
-            const int e4 = min(max(E - o + 7, 0), 15);  // in 1..15 when the row fits
-            out |= (uint32_t)((e4 << 3) | f) << (8 * j);
+        for (int u = 0; u < kRbBatch; ++u) {
+            const int64_t c = c0 + (int64_t)u * kRbParts;
+            w[u] = c < nchunks ? *reinterpret_cast<const uint32_t*>(src + c * 512 + woff) : 0u;
         }
-        *reinterpret_cast<uint32_t*>(dst + c * 512 + woff) = out;
+#pragma unroll
+        for (int u = 0; u < kRbBatch; ++u) {
+            const int64_t c = c0 + (int64_t)u * kRbParts;
+            if (c >= nchunks) break;
+            uint32_t out = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t code = (w[u] >> (8 * j)) & 0xFFu;
+                if (code == 0u || code == 0xFFu) continue;
+                int E, f;
+                ue5m3_normalize(code, E, f);
+                const int e4 = min(max(E - o + 7, 0), 15);  // in 1..15 when the row fits
+                out |= (uint32_t)((e4 << 3) | f) << (8 * j);
+            }
+            *reinterpret_cast<uint32_t*>(dst + c * 512 + woff) = out;
+        }
     }
 }
 

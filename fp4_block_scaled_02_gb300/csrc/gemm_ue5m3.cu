@@ -49,7 +49,7 @@ struct EmuParams {
     int64_t M, N, K;
     int accumulate;
     int* status;
-    const uint8_t* rb_flags;  // nullable: return at once when none of the rb_nflags bytes is set
+    const uint8_t* rb_flags;  // nullable: after a rebias pass, compute only the flagged tiles (none set: return)
     int64_t rb_nflags;
 };
 
@@ -134,7 +134,9 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
     gemm_ue5m3_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const EmuParams p) {
     using C = EmuCfg;
-    // the rebiased native kernel took this product (uniform across the grid)
+    // after a rebias pass: the native kernel took every output tile when no
+    // row was flagged (uniform across the grid); otherwise this kernel computes
+    // the flagged tiles only (every role skips the same others)
     if (p.rb_flags != nullptr) {
         pdl_wait();
         if (!rb_any_flag(p.rb_flags, p.rb_nflags)) return;
@@ -191,6 +193,8 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
+                    continue;
                 const int64_t mb = tile % num_m, nb = tile / num_m;
                 for (int kb = 0; kb < num_k; ++kb, ++it) {
                     const int s = (int)(it % C::RAW_STAGES);
@@ -218,6 +222,8 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         uint32_t it_raw = 0, it_dec = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
+                continue;
             for (int kb = 0; kb < num_k && ok; ++kb, ++it_raw) {
                 const int rs = (int)(it_raw % C::RAW_STAGES);
                 if (!tc::mbar_wait(raw_full(rs), (it_raw / C::RAW_STAGES) & 1u, p.status)) {
@@ -249,6 +255,8 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
             uint32_t it_dec = 0, chunk = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
+                    continue;
                 for (int kb = 0; kb < num_k && ok; ++kb, ++chunk) {
                     // one raw stage = one accumulator chunk
                     const int buf = (int)(chunk & 1u);
@@ -287,6 +295,8 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         uint32_t chunk = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
+                continue;
             const int64_t mb = tile % num_m, nb = tile / num_m;
             const int64_t m = mb * C::BM + q * 32 + lane;
             for (int kb = 0; kb < num_k; ++kb, ++chunk) {

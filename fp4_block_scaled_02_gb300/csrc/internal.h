@@ -147,6 +147,17 @@ cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
 // out[i] = the quantizer's RN(in[i] / 6) for i < n (diagnostic).
 cudaError_t launch_div6_selftest(const float* in, float* out, int64_t n, cudaStream_t stream);
+// Rebiased UE5M3 products: whether output tile (mb, nb) -- 128 rows of A, and
+// b_tiles_per_tile 128-row tiles of B -- holds a row that did not fit one E4M3
+// offset (flags: one byte per 128-row tile, A's tiles first). Such tiles are
+// computed by the emulated kernel, all others by the native one.
+__device__ __forceinline__ bool rb_tile_flagged(const uint8_t* flags, int64_t a_tiles, int64_t mb, int64_t nb,
+                                                int b_tiles_per_tile) {
+    bool bad = flags[mb] != 0;
+    for (int h = 0; h < b_tiles_per_tile; ++h) bad |= flags[a_tiles + nb * b_tiles_per_tile + h] != 0;
+    return bad;
+}
+
 // Any of the n bytes at f nonzero (every thread of the calling warp gets the answer).
 __device__ __forceinline__ bool rb_any_flag(const uint8_t* f, int64_t n) {
     bool any = false;

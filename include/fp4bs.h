@@ -268,16 +268,18 @@ fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int
  * block scales as E4M3 scales times one power of two per row,
  * s = e4m3 * 2^o_row exactly, the native kind::mxf4nvf4 GEMM runs on the E4M3
  * scales and multiplies output (m, n) by 2^(o_m + o_n) before alpha, which
- * gives the same sum as the UE5M3-scaled products. If some row's nonzero scales
- * span more than E4M3's 15 binades, the emulated kernel computes the product
- * instead; the choice is made on the device (no host synchronisation), and the
- * kernel not chosen returns at once. ws: device, 16-byte aligned, at least
+ * gives the same sum as the UE5M3-scaled products. A row whose nonzero scales
+ * span more than E4M3's 15 binades cannot be rebiased: the output tiles its
+ * 128-row tile touches are computed by the emulated kernel, all others by the
+ * native one; the split is made on the device (no host synchronisation), and
+ * the emulated kernel returns at once when no row was flagged. ws: device, 16-byte aligned, at least
  * fp4_gemm_workspace_bytes(a, b) bytes (about (M + N) * K / 16), owned by the
  * caller, overwritten, not to be shared by calls in flight at the same time.
  * Too small or NULL: FP4_ERR_WORKSPACE. Other scale formats ignore ws and run
  * exactly as fp4_gemm. After the stream has run the call, byte t of ws
  * (t < M / 128 + N / 128, A's 128-row tiles first) is 1 if tile t held a row
- * that did not fit and 0 otherwise: all zero means the native kernel ran. */
+ * that did not fit and 0 otherwise: all zero means the native kernel computed
+ * every output. */
 size_t fp4_gemm_workspace_bytes(const fp4_tensor_t* a, const fp4_tensor_t* b);
 fp4_status_t fp4_gemm_ws(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int out_fp32, int accumulate,
                          void* ws, size_t ws_bytes, void* stream);

@@ -286,7 +286,8 @@ def test_gemm_ue5m3_rebias_edges_and_fallback():
     mantissa 7 (placed at E4M3 exponent 7) and the smallest 13 binades below;
     mantissa <= 6 (exponent 8) with the smallest 14 binades below; UE5M3
     subnormal scales. All fit and run natively. One more binade in a single row
-    sends the whole product to the emulated kernel. Both give the oracle's sums."""
+    sends the output tiles of its 128-row tile to the emulated kernel while the
+    native kernel computes the rest. Every output gives the oracle's sums."""
     M, N, K = 256, 256, 512
     ra, _ = _operand(45, M, K, "normal", fmt=UE)
     rb, _ = _operand(46, N, K, "weight", fmt=UE)
