@@ -28,10 +28,11 @@
 //   warps 3..   : epilogue -- BN / 32 warps; warp w reads TMEM lane quadrant
 //                 w % 4 and 128 of the BN accumulator columns (tcgen05.ld),
 //                 scales by alpha and stores BF16 / FP32.
-// Measured on GB300: a kind::mxf4nvf4 MMA with M = 128 takes about the same
-// time for N = 128 and N = 256, so BN = 256 tiles (one 256-column accumulator)
-// double the work per instruction; BN = 128 tiles (two accumulators) remain for
-// N not divisible by 256.
+// Measured on GB300: a kind::mxf4nvf4 MMA with M = 128, K = 64 takes ~128
+// cycles at N = 256 and ~64 at N = 128 (the same rate); the wider tile reads
+// fewer operand bytes per output (384 rows per 128 x 256 tile, 256 per 128 x
+// 128), so BN = 256 tiles (one 256-column accumulator) are used where N allows
+// and BN = 128 tiles (two accumulators) otherwise.
 // K is accumulated in chunks of 2048 values (CHUNK_STAGES stages): each chunk
 // starts a fresh accumulator and the epilogue adds the chunk partials in FP32
 // registers with round-to-nearest. Measured on GB300 with all-positive

@@ -43,9 +43,10 @@ def _check(c_gpu, c_ref, s, bf16):
                              f"gpu {c_gpu.reshape(-1)[i]}, ref {c_ref.reshape(-1)[i]}, tol {tol.reshape(-1)[i]}")
 
 
-# N % 256 == 0 runs 128 x 256 tiles, other N 128 x 128 tiles; K = 1280 ends in a
-# partial accumulator chunk
-SHAPES = [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (1280, 1152, 768), (640, 1024, 1280)]
+# N % 256 == 0 runs 128 x 256 tiles, other N 128 x 128 tiles; K = 1280 and 2560
+# end in a partial accumulator chunk
+SHAPES = [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (1280, 1152, 768), (640, 1024, 1280),
+          (512, 768, 2560)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -82,7 +83,8 @@ MX = fb.FP4_SCALE_UE8M0
 # MXFP4 ("Pretraining Large Language Models with NVFP4", A3): UE8M0 scales per
 # 32 values, tcgen05 kind::mxf4; N % 256 selects the tile width as for NVFP4 and
 # K = 2304 ends in a partial accumulator chunk
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (640, 1024, 2304)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (384, 256, 1024), (640, 1024, 2304),
+                                   (512, 768, 2560)])
 @pytest.mark.parametrize("out32", [False, True])
 def test_gemm_mxfp4_full_output(M, N, K, out32):
     ra, a = _operand(41, M, K, "student_t4", fmt=MX, block=fb.FP4_BLOCK_1x32)
@@ -144,7 +146,7 @@ def test_gemm_zero_operand_gives_zero():
     assert torch.count_nonzero(d).item() == 0
 
 
-@pytest.mark.parametrize("K", [2048, 8192, 21504])
+@pytest.mark.parametrize("K", [2048, 8192, 8448, 21504])
 def test_gemm_all_positive_products_within_bound(K):
     """All-positive products are the worst case for an accumulator that loses
     low bits as it adds: the losses never cancel. With every code positive and
@@ -152,7 +154,8 @@ def test_gemm_all_positive_products_within_bound(K):
     and the FP32 result must still lie within 2^-20 * sum |a b| of the exact sum
     (App. B.3: FP32 accumulation of the block-scaled products). K runs up to
     21504, the longest dot product of the workloads (the 8B down-projection's
-    Fprop and its up-projection's Dgrad)."""
+    Fprop and its up-projection's Dgrad); K = 8448 = 33 * 256 ends in a partial
+    accumulator chunk of one stage."""
     M, N = 256, 256
     rng = np.random.default_rng(K)
 
@@ -261,7 +264,8 @@ def _took_native(ws, a, b) -> bool:
     return int(ws[: a.rows // 128 + b.rows // 128].sum().item()) == 0
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1280, 1152, 768), (512, 1024, 2304)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1280, 1152, 768), (512, 1024, 2304),
+                                   (512, 1024, 2048)])
 @pytest.mark.parametrize("out32", [False, True])
 def test_gemm_ue5m3_rebiased_native_full_output(M, N, K, out32):
     """UE5M3 operands on the native MMA after the per-row rebias onto E4M3."""
