@@ -644,6 +644,20 @@ def run_kernels(args):
     o_mx = fb.QTensor.empty(T, C, fb.FP4_SCALE_UE8M0)
     o_rr = fb.QTensor.empty(T, C, per_row=True)
     st_r, st_c = fb.AmaxState(), fb.AmaxState()
+    # held scaling ([UE] method details): refreshed at step 0, then timed on step 1, a
+    # non-refresh step -- one pass over the input, the amax pass only a guard launch
+    HELD = dict(tscale=fb.FP4_TSCALE_HELD, refresh_every=50)
+    sh_r, sh_c, sh_d = fb.AmaxState(), fb.AmaxState(), fb.AmaxState()
+    fb.fp4_quantize(fb.QuantConfig(step=0, **HELD), x, o_r, state=sh_r, ws=ws)
+    fb.fp4_quantize_dual(fb.QuantConfig(step=0, round=SR, **HELD),
+                         fb.QuantConfig(step=0, round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True, **HELD),
+                         x, o_r, o_c, sh_d, sh_c, ws=ws)
+    quants["rows_held_rne_step1"] = (lambda: fb.fp4_quantize(fb.QuantConfig(step=1, **HELD), x, o_r, state=sh_r,
+                                                             ws=ws), 2.5625)
+    quants["dual_held_sr_rht_step1"] = (lambda: fb.fp4_quantize_dual(
+        fb.QuantConfig(step=1, round=SR, **HELD),
+        fb.QuantConfig(step=1, round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True, **HELD),
+        x, o_r, o_c, sh_d, sh_c, ws=ws), 3.125)
     # the given-amax calls read the records a tensor-amax call leaves
     fb.fp4_tensor_amax_dual(fb.QuantConfig(), fb.QuantConfig(orient=fb.FP4_ORIENT_COLWISE, rht=True), x, st_r, st_c,
                             ws)

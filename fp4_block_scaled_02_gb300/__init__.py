@@ -449,36 +449,44 @@ class Fp4Linear:
 
     def step_host(self, x_h, w_h, dy_h, y_h, dx_h, dw_h, step: int = 0, stream=None):
         """`step` from pinned host tensors to pinned host tensors. The inputs are
-        copied to this layer's device buffers on a host-to-device stream, the
-        step runs on `stream` once they have landed, and the outputs are copied
-        back on a device-to-host stream once it is done. The call returns at once;
-        the next call's input copies wait only for this step to finish reading
-        the device inputs and its step only for the previous output copies, so
-        successive calls (of this and of other layers) overlap copies with
-        compute. `h2d_stream` can be made to wait on an event first; `ev_out`
-        marks the end of the output copies."""
+        copied to device buffers on a host-to-device stream, the step runs on
+        `stream` once they have landed, and the outputs are copied back on a
+        device-to-host stream once it is done. The call returns at once. Two sets
+        of device buffers alternate between calls, so one call's step runs while
+        the next call's inputs come in and the previous call's outputs go out: a
+        call's input copies wait only for the step two calls back to finish
+        reading that set's inputs, and its step only for that step's output
+        copies. `h2d_stream` can be made to wait on an event first; `ev_out` marks
+        the end of the latest call's output copies (the copies run in order, so
+        of all earlier ones too)."""
         dev = self.device
         if not hasattr(self, "h2d_stream"):
             self.h2d_stream = torch.cuda.Stream(device=dev)
             self.d2h_stream = torch.cuda.Stream(device=dev)
-            self.ev_in, self.ev_done, self.ev_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
-            self.dev_in = {k: torch.empty(t.shape, dtype=t.dtype, device=dev)
-                           for k, t in (("x", x_h), ("w", w_h), ("dy", dy_h))}
-            self.dev_out = {k: torch.empty(t.shape, dtype=t.dtype, device=dev)
-                            for k, t in (("y", y_h), ("dx", dx_h), ("dw", dw_h))}
+            self.host_slots = [
+                {"in": {k: torch.empty(t.shape, dtype=t.dtype, device=dev)
+                        for k, t in (("x", x_h), ("w", w_h), ("dy", dy_h))},
+                 "out": {k: torch.empty(t.shape, dtype=t.dtype, device=dev)
+                         for k, t in (("y", y_h), ("dx", dx_h), ("dw", dw_h))},
+                 "ev_in": torch.cuda.Event(), "ev_done": torch.cuda.Event(), "ev_out": torch.cuda.Event()}
+                for _ in range(2)]
+            self.host_calls = 0
         main = torch.cuda.current_stream() if stream is None else stream
-        di, do = self.dev_in, self.dev_out
-        self.h2d_stream.wait_event(self.ev_done)  # the previous step has read the device inputs
+        slot = self.host_slots[self.host_calls % 2]
+        self.host_calls += 1
+        di, do = slot["in"], slot["out"]
+        self.h2d_stream.wait_event(slot["ev_done"])  # the step two calls back has read these inputs
         with torch.cuda.stream(self.h2d_stream):
             for k, t in (("x", x_h), ("w", w_h), ("dy", dy_h)):
                 di[k].copy_(t, non_blocking=True)
-        self.ev_in.record(self.h2d_stream)
-        main.wait_event(self.ev_in)
-        main.wait_event(self.ev_out)  # the previous output copies have read the device outputs
+        slot["ev_in"].record(self.h2d_stream)
+        main.wait_event(slot["ev_in"])
+        main.wait_event(slot["ev_out"])  # ... and its output copies have read these outputs
         self.step(di["x"], di["w"], di["dy"], do["y"], do["dx"], do["dw"], step=step, stream=main)
-        self.ev_done.record(main)
-        self.d2h_stream.wait_event(self.ev_done)
+        slot["ev_done"].record(main)
+        self.d2h_stream.wait_event(slot["ev_done"])
         with torch.cuda.stream(self.d2h_stream):
             for k, t in (("y", y_h), ("dx", dx_h), ("dw", dw_h)):
                 t.copy_(do[k], non_blocking=True)
-        self.ev_out.record(self.d2h_stream)
+        slot["ev_out"].record(self.d2h_stream)
+        self.ev_out = slot["ev_out"]
