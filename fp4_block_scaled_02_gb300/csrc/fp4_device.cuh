@@ -99,8 +99,6 @@ __device__ __forceinline__ uint32_t zero_mag_count8(uint32_t w) {
     return 8u - (uint32_t)__popc((t | (t >> 1) | (t >> 2)) & 0x11111111u);
 }
 
-// Count of values that saturate (|v| > 6 before rounding).
-__device__ __forceinline__ uint32_t e2m1_saturates(float v) { return fabsf(v) > 6.0f ? 1u : 0u; }
 
 // ---------------------------------------------------------------------------
 // Block-scale formats with a 3-bit mantissa, encoded round-to-nearest-even and
@@ -327,6 +325,30 @@ __device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
     f2 r;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
+}
+
+// Number of the N values with |x| > 6 before rounding, i.e. that saturate to
+// +-6. RN(|x| * 2^100 - 6 * 2^100) from one fused multiply-add carries the sign
+// of |x| - 6 (zero only for |x| == 6) and, when positive, is at least
+// ulp(6) * 2^100 > 1 (+inf if it overflows), so clamped to [0, 1] it is
+// exactly 1 for a saturating value and 0 otherwise; N such terms sum exactly in
+// FP32. One FMA-pipe instruction per value and a packed adder tree, in place of
+// a compare and an integer add per value.
+template <int N>
+__device__ __forceinline__ uint32_t e2m1_saturating_count(const float* x) {
+    static_assert(N == 16 || N == 32, "16 or 32 values");
+    f2 a[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i)
+        a[i] = f2_pack(__saturatef(__fmaf_rn(fabsf(x[2 * i]), 0x1p100f, -0x1.8p102f)),
+                       __saturatef(__fmaf_rn(fabsf(x[2 * i + 1]), 0x1p100f, -0x1.8p102f)));
+#pragma unroll
+    for (int w = N / 4; w >= 1; w /= 2)
+#pragma unroll
+        for (int i = 0; i < w; ++i) a[i] = f2_add(a[i], a[i + w]);
+    float lo, hi;
+    f2_unpack(a[0], lo, hi);
+    return (uint32_t)__fadd_rn(lo, hi);
 }
 
 // x[i] = RN(v[i] * m) for 16 values, two per instruction.

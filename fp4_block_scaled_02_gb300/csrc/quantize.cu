@@ -213,10 +213,7 @@ __device__ __forceinline__ uint32_t quantize_block16(const float v[16], float vm
         for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(__fmul_rn(v[i], 0.25f), enc_l);
         xmax = __fmul_rn(amax_b, enc_l);
     }
-    if (xmax > 6.0f) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[i]);
-    }
+    if (xmax > 6.0f) cnt.esat += e2m1_saturating_count<16>(x);
     if (SR) {
         uint4 r[2];
         sr_block_bits(c0, q.tensor_id, q.step_lo, q.round_key, r);
@@ -604,10 +601,7 @@ __global__ void __launch_bounds__(kThreads) quantize_2d_kernel(QParams q) {
             lo = e2m1_rne_x8(x);
             hi = e2m1_rne_x8(x + 8);
             if (active) {
-                if (__fmul_rn(amax_t, s_enc_l) > 6.0f) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) cnt.esat += e2m1_saturates(x[e]);
-                }
+                if (__fmul_rn(amax_t, s_enc_l) > 6.0f) cnt.esat += e2m1_saturating_count<16>(x);
                 cnt.eunder += zero_mag_count8(lo) + zero_mag_count8(hi) - nzero;
             }
         }
@@ -757,12 +751,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     cw[h][1] = e2m1_rne_x8(x[h] + 8);
                 }
             }
-            if (__fmul_rn(amax, enc_l) > 6.0f) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) cnt.esat += e2m1_saturates(x[h][i]);
-            }
+            if (__fmul_rn(amax, enc_l) > 6.0f)
+                cnt.esat += e2m1_saturating_count<16>(x[0]) + e2m1_saturating_count<16>(x[1]);
             if (!q.count_t)
                 cnt.eunder += zero_mag_count16(cw[0][0], cw[0][1]) + zero_mag_count16(cw[1][0], cw[1][1]) - nzero;
         }
@@ -870,10 +860,7 @@ __global__ void __launch_bounds__(kThreads) quantize_mx_rows_kernel(QParams q) {
             scale16(v + 16, inv, x + 16);
 #pragma unroll
             for (int e = 0; e < 32; ++e) nzero += (__float_as_uint(v[e]) << 1) == 0u ? 1u : 0u;
-            if (__fmul_rn(amax_b, inv) > 6.0f) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) cnt.esat += e2m1_saturates(x[e]);
-            }
+            if (__fmul_rn(amax_b, inv) > 6.0f) cnt.esat += e2m1_saturating_count<32>(x);
             uint32_t w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) w[k] = e2m1_rne_x8(x + 8 * k);
