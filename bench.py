@@ -648,10 +648,12 @@ def run_kernels(args):
     # non-refresh step -- one pass over the input, the amax pass only a guard launch
     HELD = dict(tscale=fb.FP4_TSCALE_HELD, refresh_every=50)
     sh_r, sh_c, sh_d = fb.AmaxState(), fb.AmaxState(), fb.AmaxState()
-    fb.fp4_quantize(fb.QuantConfig(step=0, **HELD), x, o_r, state=sh_r, ws=ws)
-    fb.fp4_quantize_dual(fb.QuantConfig(step=0, round=SR, **HELD),
-                         fb.QuantConfig(step=0, round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True, **HELD),
-                         x, o_r, o_c, sh_d, sh_c, ws=ws)
+    if wanted(f"quantize_rows_held_rne_step1_{T}x{C}"):
+        fb.fp4_quantize(fb.QuantConfig(step=0, **HELD), x, o_r, state=sh_r, ws=ws)
+    if wanted(f"quantize_dual_held_sr_rht_step1_{T}x{C}"):
+        fb.fp4_quantize_dual(fb.QuantConfig(step=0, round=SR, **HELD),
+                             fb.QuantConfig(step=0, round=SR, orient=fb.FP4_ORIENT_COLWISE, rht=True, **HELD),
+                             x, o_r, o_c, sh_d, sh_c, ws=ws)
     quants["rows_held_rne_step1"] = (lambda: fb.fp4_quantize(fb.QuantConfig(step=1, **HELD), x, o_r, state=sh_r,
                                                              ws=ws), 2.5625)
     quants["dual_held_sr_rht_step1"] = (lambda: fb.fp4_quantize_dual(
