@@ -480,6 +480,7 @@ def run_gpu(args, workload):
 
     if rank != 0:
         return
+    counts = event_counts(workload, layers, dy_of)
     peaks, src = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     hbm_peak = peaks["hbm_gbs"]
@@ -523,8 +524,67 @@ def run_gpu(args, workload):
                 "ms_per_step": e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
+        "event_counts": counts,
     }
     print(json.dumps(line), flush=True)
+
+
+COUNTER_ORDER = ["elem_sat", "elem_underflow", "scale_sat", "scale_underflow"]
+LAYER_ROWS = ["x", "xt", "w", "dy", "dyt"]  # Fp4Linear.counters rows (W: both orientations, each element once)
+
+
+def event_counts(workload, layers, dy_of):
+    """The four event counters of every quantized tensor, outside the timed
+    region (the pages argue from saturation and underflow events). Fixed-shape
+    workloads: one step's counters per tensor with the step's own recipe, and
+    the MXFP4 1x32 power-of-two-scale quantizer (rowwise) on the same X, W and dY.
+    The held-amax sweep: a fresh layer per target T, stepped through every step
+    of the sweep in order, dY's rowwise and colwise counters at each step."""
+    import torch
+
+    import fp4_block_scaled_02_gb300 as fb
+
+    out = {"order": COUNTER_ORDER}
+    if not workload.held:
+        nv, mx, elems = [], [], []
+        for lin, L, di, o in layers:
+            L.counters.zero_()
+            L.step(di["x"], di["w"], di["dy"], o["y"], o["dx"], o["dw"], step=0)
+            torch.cuda.synchronize()
+            c = L.counters.cpu().tolist()
+            nv.append({name: c[i] for i, name in enumerate(LAYER_ROWS)})
+            m = {}
+            for name in ("x", "w", "dy"):
+                t = di[name]
+                q = fb.QTensor.empty(t.shape[0], t.shape[1], fb.FP4_SCALE_UE8M0)
+                cnt = torch.zeros(4, dtype=torch.int64, device="cuda")
+                fb.fp4_quantize(fb.QuantConfig(scale_fmt=fb.FP4_SCALE_UE8M0, block=fb.FP4_BLOCK_1x32), t, q,
+                                counters=cnt, ws=L.ws)
+                m[name] = cnt.cpu().tolist()
+                del q
+            mx.append(m)
+            elems.append({"x": lin.tokens * lin.k_in, "w": lin.n_out * lin.k_in, "dy": lin.tokens * lin.n_out})
+        out.update({"nvfp4": nv, "mxfp4_1x32_rowwise": mx, "elements": elems})
+    else:
+        lin, L0, di, o = layers[0]
+        per_T = {}
+        for T in workload.targets:
+            L = fb.Fp4Linear(lin.tokens, lin.k_in, lin.n_out, rht=workload.rht, seed=workload.rht_seed,
+                             scale_fmt=L0.scale_fmt, held=True, target_T=T)
+            rows = {"dy": [], "dyt": []}
+            for s in range(workload.steps):
+                L.counters.zero_()
+                L.step(di["x"], di["w"], dy_of(di, s), o["y"], o["dx"], o["dw"], step=s)
+                c = L.counters.cpu().tolist()
+                rows["dy"].append(c[3])
+                rows["dyt"].append(c[4])
+            per_T[f"{T:g}"] = rows
+            del L
+        out.update({"steps": workload.steps, "per_step": per_T,
+                    "elements": {"dy": lin.tokens * lin.n_out}})
+    if fb.fp4_device_status() != 0:
+        raise RuntimeError("device status after the event-count pass")
+    return out
 
 
 def load_traffic() -> dict:
