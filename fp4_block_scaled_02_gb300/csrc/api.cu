@@ -300,8 +300,12 @@ fp4_status_t prepare_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d,
 // UE5M3 rebias workspace: per-tile "does not fit" bytes, per-row offsets of A
 // and B, rebiased scales of A and B (each part 16-byte aligned).
 struct RebiasLayout {
-    size_t off_a, off_b, sc_a, sc_b, total;
+    size_t off_a, off_b, sc_a, sc_b, cnt, split, total;
+    int64_t split_tiles;
 };
+// fp4_gemm_ws's workspace: flags, per-row offsets, rebiased scales, then for
+// the emulated fallback 4 counters per split tile and the FP32 partial tiles
+// (at most one per tile and 256-value stage, and kEmuSplitMaxTiles).
 RebiasLayout rebias_layout(int64_t M, int64_t N, int64_t K) {
     auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
     RebiasLayout l{};
@@ -309,7 +313,11 @@ RebiasLayout rebias_layout(int64_t M, int64_t N, int64_t K) {
     l.off_b = l.off_a + up16((size_t)M);
     l.sc_a = l.off_b + up16((size_t)N);
     l.sc_b = l.sc_a + up16((size_t)(M * (K / 16)));
-    l.total = l.sc_b + up16((size_t)(N * (K / 16)));
+    l.cnt = l.sc_b + up16((size_t)(N * (K / 16)));
+    const int64_t work = (M / 128) * (N / 128) * (K / 256);
+    l.split_tiles = work < kEmuSplitMaxTiles ? work : kEmuSplitMaxTiles;
+    l.split = l.cnt + up16((size_t)(4 * kEmuSplitMaxTiles) * sizeof(uint32_t));
+    l.total = l.split + (size_t)l.split_tiles * 128 * 128 * sizeof(float);
     return l;
 }
 
@@ -561,7 +569,9 @@ fp4_status_t fp4_gemm_ws(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, 
     int8_t* b_off = reinterpret_cast<int8_t*>(w + l.off_b);
     uint8_t* a_sc = w + l.sc_a;
     uint8_t* b_sc = w + l.sc_b;
-    cudaError_t e = launch_rebias_ue5m3(j.a_scales, j.M, j.b_scales, j.N, j.K, a_sc, b_sc, a_off, b_off, flags, st);
+    uint32_t* split_cnt = reinterpret_cast<uint32_t*>(w + l.cnt);
+    cudaError_t e = launch_rebias_ue5m3(j.a_scales, j.M, j.b_scales, j.N, j.K, a_sc, b_sc, a_off, b_off, flags,
+                                        split_cnt, 4 * kEmuSplitMaxTiles, st);
     if (e != cudaSuccess) return from_cuda(e);
     // native MMA on the rebiased scales, unless a row did not fit; then the
     // emulated kernel (which reads the UE5M3 scales) runs instead
@@ -578,6 +588,9 @@ fp4_status_t fp4_gemm_ws(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, 
     je.rb_flags = flags;
     je.rb_nflags = jn.rb_nflags;
     je.rb_emulated = 1;
+    je.split_cnt = split_cnt;
+    je.split_buf = reinterpret_cast<float*>(w + l.split);
+    je.split_cap = l.split_tiles;
     return from_cuda(launch_gemm_ue5m3(je, st));
 }
 

@@ -613,8 +613,11 @@ constexpr int kRbParts = 8, kRbBatch = 8;
 __global__ void __launch_bounds__(128 * kRbParts)
     rebias_ue5m3_kernel(const uint8_t* __restrict__ a_sc, int64_t a_tiles, const uint8_t* __restrict__ b_sc,
                         uint8_t* __restrict__ a_out, uint8_t* __restrict__ b_out, int8_t* __restrict__ a_off,
-                        int8_t* __restrict__ b_off, int64_t nchunks, uint8_t* __restrict__ flags) {
+                        int8_t* __restrict__ b_off, int64_t nchunks, uint8_t* __restrict__ flags,
+                        uint32_t* __restrict__ clear, int64_t n_clear) {
     pdl_begin();
+    if (blockIdx.x == 0)
+        for (int64_t i = threadIdx.x; i < n_clear; i += blockDim.x) clear[i] = 0u;
     __shared__ int kmax_s[kRbParts][128], emin_s[kRbParts][128];
     const bool is_a = blockIdx.x < a_tiles;
     const int64_t rt = is_a ? blockIdx.x : blockIdx.x - a_tiles;
@@ -710,11 +713,11 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t st
 
 cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_t* b_scales, int64_t N, int64_t K,
                                 uint8_t* a_out, uint8_t* b_out, int8_t* a_off, int8_t* b_off, uint8_t* flags,
-                                cudaStream_t st) {
+                                uint32_t* clear, int64_t n_clear, cudaStream_t st) {
     const int64_t tiles = M / 128 + N / 128;
     if (tiles <= 0 || tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     (void)launch_pdl(rebias_ue5m3_kernel, (unsigned)tiles, 128 * kRbParts, 0, st, a_scales, M / 128, b_scales, a_out, b_out,
-                                                                    a_off, b_off, K / 64, flags);
+                                                                    a_off, b_off, K / 64, flags, clear, n_clear);
     return cudaGetLastError();
 }
 

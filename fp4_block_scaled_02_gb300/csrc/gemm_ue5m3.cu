@@ -27,6 +27,17 @@
 //                 (tcgen05.ld both, add with round-to-nearest, tcgen05.st), so no
 //                 accumulator lives in registers, and at the last chunk of a tile
 //                 stores alpha * (sum + chunk).
+// After a rebias pass (fp4_gemm_ws) this kernel computes only the output tiles
+// whose rows did not fit, usually one 128-row tile-row (where the native
+// kernel ran 128 x 256 tiles, a flagged B row tile takes the other half of its
+// pair along: the native kernel skipped both): a warp lists the
+// flagged A and B row tiles in shared memory, the flagged tiles are numbered
+// from those lists and dealt out one per CTA, and when they are fewer than the
+// CTAs, each tile's K is split into S contiguous parts (S = CTAs / tiles, at
+// most one part per 256-value stage). Each part leaves its FP32 sums in the
+// workspace; per 32-row quarter of the tile, the epilogue warp that finishes
+// last (a counter per quarter) adds the S parts in order p = 0 .. S-1, which
+// fixes the result whatever the CTAs' timing, and writes the output.
 #include <cstdint>
 
 #include <cuda.h>
@@ -51,6 +62,11 @@ struct EmuParams {
     int* status;
     const uint8_t* rb_flags;  // nullable: after a rebias pass, compute only the flagged tiles (none set: return)
     int64_t rb_nflags;
+    int use_list;             // number the flagged tiles from shared-memory lists (else scan every tile)
+    int rb_pair;              // 2: the native kernel skipped 128 x 256 tiles, so a flagged B tile takes its pair along
+    uint32_t* split_cnt;      // nullable: 4 counters per split tile, zero on entry, left zero
+    float* split_buf;         // FP32 partial tiles, split_cap of them
+    int64_t split_cap;
 };
 
 struct EmuCfg {
@@ -70,7 +86,11 @@ struct EmuCfg {
     static constexpr int OFF_BAR = OFF_SFB + RAW_STAGES * RAW_SFB;
     static constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * DEC_STAGES + 4 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    // lists of flagged A row tiles, unflagged A row tiles and flagged B row
+    // tiles (16-bit tile indices), and their counts
+    static constexpr int LIST_CAP = 4096;
+    static constexpr int OFF_LIST = OFF_MISC + 32;
+    static constexpr int SMEM_BYTES = OFF_LIST + 2 * LIST_CAP + 1024;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS);
     static constexpr int TMEM_COLS = 512;  // two 128-column chunk accumulators + the running sum
     static constexpr int SUM_COL = 2 * BN;
@@ -129,7 +149,61 @@ __device__ __forceinline__ void decode_half(const uint8_t* raw, const uint8_t* s
     }
 }
 
-template <bool OUT32>
+// One unit of work: output tile (mb, nb), stages [kb0, kb1) of its K, and
+// with split > 1 the partial tile it leaves (slot, part).
+struct EmuItem {
+    int64_t mb, nb;
+    int kb0, kb1;
+    int64_t tile_item;
+    int part;
+};
+
+// The work of a launch. Without a rebias pass: every tile, all of K. After
+// one: with lists, the flagged tiles numbered as all tiles of the flagged A
+// row tiles (A-list order, B fastest) then the flagged B row tiles of the
+// other A row tiles, each split into `split` parts; without lists (shapes too
+// large for them), every tile scanned and the unflagged ones skipped.
+struct EmuWork {
+    int64_t num_m, num_n, count;
+    int num_k, split;
+    int64_t fa, fb;
+    const uint16_t* l_fa;
+    const uint16_t* l_nfa;
+    const uint16_t* l_fb;
+    const uint8_t* flags;
+    int pair;
+
+    template <bool LISTED>
+    __device__ bool item(int64_t j, EmuItem& it) const {
+        if (LISTED) {
+            const int64_t i = j / split;
+            it.part = (int)(j % split);
+            it.tile_item = i;
+            if (i < fa * num_n) {
+                it.mb = l_fa[i / num_n];
+                it.nb = i % num_n;
+            } else {
+                const int64_t i2 = i - fa * num_n;
+                it.mb = l_nfa[i2 / fb];
+                it.nb = l_fb[i2 % fb];
+            }
+            it.kb0 = (int)((int64_t)it.part * num_k / split);
+            it.kb1 = (int)((int64_t)(it.part + 1) * num_k / split);
+            return true;
+        }
+        it.mb = j % num_m;
+        it.nb = j / num_m;
+        it.kb0 = 0;
+        it.kb1 = num_k;
+        it.tile_item = j;
+        it.part = 0;
+        return flags == nullptr || rb_tile_flagged(flags, num_m, it.mb, it.nb / pair, pair);
+    }
+};
+
+// LISTED: the rebias fallback with flagged-tile lists and K split (else the
+// plain tile loop, skipping unflagged tiles when rb_flags is set).
+template <bool OUT32, bool LISTED>
 __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
     gemm_ue5m3_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const EmuParams p) {
@@ -183,20 +257,75 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
         tc::tmem_relinquish();
     }
+    uint16_t* lists = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST);
+    int* counts = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // flagged A, flagged B row tiles
+    if (LISTED && warp == C::FIRST_DEC_WARP) {
+        // lists[0 .. fa): flagged A row tiles; lists[num_m .. 2 num_m - fa):
+        // the others; lists[2 num_m ..): flagged B row tiles (ascending)
+        int fa = 0, nfa = 0, fbn = 0;
+        for (int64_t base = 0; base < num_m; base += 32) {
+            const int64_t mb = base + lane;
+            const bool in = mb < num_m, f = in && p.rb_flags[mb] != 0;
+            const uint32_t bf = __ballot_sync(0xFFFFFFFFu, f), bn = __ballot_sync(0xFFFFFFFFu, in && !f);
+            const uint32_t below = (1u << lane) - 1u;
+            if (f) lists[fa + __popc(bf & below)] = (uint16_t)mb;
+            if (in && !f) lists[num_m + nfa + __popc(bn & below)] = (uint16_t)mb;
+            fa += __popc(bf);
+            nfa += __popc(bn);
+        }
+        for (int64_t base = 0; base < num_n; base += 32) {
+            const int64_t nb = base + lane;
+            const bool f = nb < num_n && (p.rb_flags[num_m + nb] != 0 ||
+                                          (p.rb_pair == 2 && p.rb_flags[num_m + (nb ^ 1)] != 0));
+            const uint32_t bf = __ballot_sync(0xFFFFFFFFu, f);
+            if (f) lists[2 * num_m + fbn + __popc(bf & ((1u << lane) - 1u))] = (uint16_t)nb;
+            fbn += __popc(bf);
+        }
+        if (lane == 0) {
+            counts[0] = fa;
+            counts[1] = fbn;
+        }
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    EmuWork wk;
+    wk.num_m = num_m;
+    wk.num_n = num_n;
+    wk.num_k = num_k;
+    wk.flags = p.rb_flags;
+    wk.pair = p.rb_pair;
+    wk.split = 1;
+    wk.count = tiles;
+    wk.fa = wk.fb = 0;
+    wk.l_fa = lists;
+    wk.l_nfa = lists + num_m;
+    wk.l_fb = lists + 2 * num_m;
+    if (LISTED) {
+        wk.fa = counts[0];
+        wk.fb = counts[1];
+        const int64_t f = wk.fa * num_n + (num_m - wk.fa) * wk.fb;  // >= 1: some flag is set
+        int64_t split = 1;
+        if (p.split_buf != nullptr && f < gridDim.x) {
+            split = gridDim.x / f;
+            if (split > num_k) split = num_k;
+            if (split * f > p.split_cap) split = p.split_cap / f;
+            if (split < 1) split = 1;
+        }
+        wk.split = (int)split;
+        wk.count = f * split;
+    }
 
     if (warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-                if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
-                    continue;
-                const int64_t mb = tile % num_m, nb = tile / num_m;
-                for (int kb = 0; kb < num_k; ++kb, ++it) {
+            for (int64_t j = blockIdx.x; j < wk.count && ok; j += gridDim.x) {
+                EmuItem w;
+                if (!wk.template item<LISTED>(j, w)) continue;
+                const int64_t mb = w.mb, nb = w.nb;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = (int)(it % C::RAW_STAGES);
                     const uint32_t ph = (it / C::RAW_STAGES) & 1u;
                     if (!tc::mbar_wait(raw_empty(s), ph ^ 1u, p.status)) {
@@ -221,10 +350,10 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         const int op = t >> 8, h = (t >> 7) & 1, r = t & 127;  // operand (A/B), raw chunk half, row
         uint32_t it_raw = 0, it_dec = 0;
         bool ok = true;
-        for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-            if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
-                continue;
-            for (int kb = 0; kb < num_k && ok; ++kb, ++it_raw) {
+        for (int64_t j = blockIdx.x; j < wk.count && ok; j += gridDim.x) {
+            EmuItem w;
+            if (!wk.template item<LISTED>(j, w)) continue;
+            for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ++it_raw) {
                 const int rs = (int)(it_raw % C::RAW_STAGES);
                 if (!tc::mbar_wait(raw_full(rs), (it_raw / C::RAW_STAGES) & 1u, p.status)) {
                     ok = false;
@@ -254,10 +383,10 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
             constexpr uint32_t IDESC = tc::idesc_bf16(C::BM, C::BN);
             uint32_t it_dec = 0, chunk = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-                if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
-                    continue;
-                for (int kb = 0; kb < num_k && ok; ++kb, ++chunk) {
+            for (int64_t j = blockIdx.x; j < wk.count && ok; j += gridDim.x) {
+                EmuItem w;
+                if (!wk.template item<LISTED>(j, w)) continue;
+                for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ++chunk) {
                     // one raw stage = one accumulator chunk
                     const int buf = (int)(chunk & 1u);
                     if (!tc::mbar_wait(acce(buf), ((chunk >> 1) & 1u) ^ 1u, p.status)) {
@@ -294,19 +423,57 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t chunk = 0;
         bool ok = true;
-        for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-            if (p.rb_flags != nullptr && !rb_tile_flagged(p.rb_flags, p.M / C::BM, tile % num_m, tile / num_m, 1))
-                continue;
-            const int64_t mb = tile % num_m, nb = tile / num_m;
+        // alpha * the 32 sums of row m, columns n0 .. n0 + 31, to the output
+        auto write_out = [&](const uint32_t (&rs)[32], int64_t m, int64_t n0) {
+            if (OUT32) {
+                float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+#pragma unroll
+                for (int v = 0; v < 32; v += 4) {
+                    float4 o = make_float4(__fmul_rn(__uint_as_float(rs[v]), alpha),
+                                           __fmul_rn(__uint_as_float(rs[v + 1]), alpha),
+                                           __fmul_rn(__uint_as_float(rs[v + 2]), alpha),
+                                           __fmul_rn(__uint_as_float(rs[v + 3]), alpha));
+                    if (p.accumulate) {
+                        const float4 old = *reinterpret_cast<const float4*>(dst + v);
+                        o.x = __fadd_rn(o.x, old.x);
+                        o.y = __fadd_rn(o.y, old.y);
+                        o.z = __fadd_rn(o.z, old.z);
+                        o.w = __fadd_rn(o.w, old.w);
+                    }
+                    *reinterpret_cast<float4*>(dst + v) = o;
+                }
+            } else {
+                uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
+#pragma unroll
+                for (int v = 0; v < 32; v += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 hh =
+                            __floats2bfloat162_rn(__fmul_rn(__uint_as_float(rs[v + 2 * k]), alpha),
+                                                  __fmul_rn(__uint_as_float(rs[v + 2 * k + 1]), alpha));
+                        w[k] = *reinterpret_cast<const uint32_t*>(&hh);
+                    }
+                    *reinterpret_cast<uint4*>(dst + v) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        };
+        const bool split = LISTED && wk.split > 1;
+        for (int64_t j = blockIdx.x; j < wk.count && ok; j += gridDim.x) {
+            EmuItem w;
+            if (!wk.template item<LISTED>(j, w)) continue;
+            const int64_t mb = w.mb, nb = w.nb;
             const int64_t m = mb * C::BM + q * 32 + lane;
-            for (int kb = 0; kb < num_k; ++kb, ++chunk) {
+            // this part's FP32 sums of row m of the tile (split only)
+            float* part_row = split ? p.split_buf + ((size_t)j * C::BM + (size_t)(q * 32 + lane)) * C::BN : nullptr;
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++chunk) {
                 const int buf = (int)(chunk & 1u);
                 if (!tc::mbar_wait(accf(buf), (chunk >> 1) & 1u, p.status)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                const bool first = kb == 0, last = kb == num_k - 1;
+                const bool first = kb == w.kb0, last = kb == w.kb1 - 1;
 #pragma unroll 1
                 for (int c = 0; c < C::BN; c += 32) {
                     uint32_t rc[32], rs[32];
@@ -331,40 +498,15 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
                         tc::tmem_st_32x32b_x32(lane_base + (uint32_t)(C::SUM_COL + c), rs);
                         continue;
                     }
-                    // last chunk of the tile: alpha * sum to the output row m, columns n0 + c ..
-                    const int64_t n0 = nb * C::BN + c;
-                    if (OUT32) {
-                        float* dst = static_cast<float*>(p.d) + m * p.N + n0;
+                    if (split) {
 #pragma unroll
-                        for (int v = 0; v < 32; v += 4) {
-                            float4 o = make_float4(__fmul_rn(__uint_as_float(rs[v]), alpha),
-                                                   __fmul_rn(__uint_as_float(rs[v + 1]), alpha),
-                                                   __fmul_rn(__uint_as_float(rs[v + 2]), alpha),
-                                                   __fmul_rn(__uint_as_float(rs[v + 3]), alpha));
-                            if (p.accumulate) {
-                                const float4 old = *reinterpret_cast<const float4*>(dst + v);
-                                o.x = __fadd_rn(o.x, old.x);
-                                o.y = __fadd_rn(o.y, old.y);
-                                o.z = __fadd_rn(o.z, old.z);
-                                o.w = __fadd_rn(o.w, old.w);
-                            }
-                            *reinterpret_cast<float4*>(dst + v) = o;
-                        }
-                    } else {
-                        uint16_t* dst = static_cast<uint16_t*>(p.d) + m * p.N + n0;
-#pragma unroll
-                        for (int v = 0; v < 32; v += 8) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const __nv_bfloat162 hh =
-                                    __floats2bfloat162_rn(__fmul_rn(__uint_as_float(rs[v + 2 * k]), alpha),
-                                                          __fmul_rn(__uint_as_float(rs[v + 2 * k + 1]), alpha));
-                                w[k] = *reinterpret_cast<const uint32_t*>(&hh);
-                            }
-                            *reinterpret_cast<uint4*>(dst + v) = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int v = 0; v < 32; v += 4)
+                            __stcg(reinterpret_cast<uint4*>(part_row + c + v),
+                                   make_uint4(rs[v], rs[v + 1], rs[v + 2], rs[v + 3]));
+                        continue;
                     }
+                    // last chunk of the tile: alpha * sum to the output row m, columns nb * BN + c ..
+                    write_out(rs, m, nb * C::BN + c);
                 }
                 // the running sum is written before this warp's next loads of it
                 if (!last) tc::tmem_st_wait();
@@ -372,6 +514,44 @@ __global__ void __launch_bounds__(EmuCfg::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(acce(buf));
             }
+            if (!ok || !split) continue;
+            // split: this warp's 32 rows of part w.part are in the workspace;
+            // the warp that counts the last part of this quarter adds the parts
+            // in order p = 0 .. split - 1 and writes the output rows
+            __threadfence();
+            __syncwarp();
+            uint32_t prev = 0;
+            if (lane == 0) prev = atomicAdd(p.split_cnt + 4 * w.tile_item + q, 1u);
+            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+            if (prev != (uint32_t)(wk.split - 1)) continue;
+            __threadfence();
+            const float* row0 =
+                p.split_buf + ((size_t)(w.tile_item * wk.split) * C::BM + (size_t)(q * 32 + lane)) * C::BN;
+#pragma unroll 1
+            for (int c = 0; c < C::BN; c += 32) {
+                uint32_t rs[32];
+#pragma unroll
+                for (int v = 0; v < 32; v += 4) {
+                    const uint4 u = __ldcg(reinterpret_cast<const uint4*>(row0 + c + v));
+                    rs[v] = u.x;
+                    rs[v + 1] = u.y;
+                    rs[v + 2] = u.z;
+                    rs[v + 3] = u.w;
+                }
+                for (int pp = 1; pp < wk.split; ++pp) {
+                    const float* row = row0 + (size_t)pp * C::BM * C::BN;
+#pragma unroll
+                    for (int v = 0; v < 32; v += 4) {
+                        const float4 u = __ldcg(reinterpret_cast<const float4*>(row + c + v));
+                        rs[v] = __float_as_uint(__fadd_rn(__uint_as_float(rs[v]), u.x));
+                        rs[v + 1] = __float_as_uint(__fadd_rn(__uint_as_float(rs[v + 1]), u.y));
+                        rs[v + 2] = __float_as_uint(__fadd_rn(__uint_as_float(rs[v + 2]), u.z));
+                        rs[v + 3] = __float_as_uint(__fadd_rn(__uint_as_float(rs[v + 3]), u.w));
+                    }
+                }
+                write_out(rs, m, nb * C::BN + c);
+            }
+            if (lane == 0) p.split_cnt[4 * w.tile_item + q] = 0u;  // zero again for the next call
         }
     }
     tc::fence_before_sync();
@@ -387,9 +567,15 @@ cudaError_t run_emu(const GemmJob& j, cudaStream_t st) {
     CUtensorMap ta, tb;
     if (!make_tmap_u8_sw128(&ta, j.a_codes, j.M, j.K / 2, EmuCfg::BM)) return cudaErrorInvalidValue;
     if (!make_tmap_u8_sw128(&tb, j.b_codes, j.N, j.K / 2, EmuCfg::BN)) return cudaErrorInvalidValue;
+    const int64_t num_m = j.M / EmuCfg::BM, num_n = j.N / EmuCfg::BN;
+    const bool rb = j.rb_emulated && j.rb_flags != nullptr;
+    // the flagged-tile lists hold 2 num_m + num_n 16-bit entries
+    const int use_list = rb && 2 * num_m + num_n <= EmuCfg::LIST_CAP && num_m < 65536 && num_n < 65536;
     EmuParams p{j.a_scales, j.b_scales, j.a_sdec, j.b_sdec, j.d, j.M, j.N, j.K, j.accumulate, j.status,
-                j.rb_emulated ? j.rb_flags : nullptr, j.rb_nflags};
-    auto kern = gemm_ue5m3_kernel<OUT32>;
+                rb ? j.rb_flags : nullptr, j.rb_nflags, use_list, j.N % 256 == 0 ? 2 : 1,
+                use_list ? j.split_cnt : nullptr,
+                use_list ? j.split_buf : nullptr, use_list ? j.split_cap : 0};
+    auto kern = use_list ? gemm_ue5m3_kernel<OUT32, true> : gemm_ue5m3_kernel<OUT32, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, EmuCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (j.M / EmuCfg::BM) * (j.N / EmuCfg::BN);

@@ -130,7 +130,16 @@ struct GemmJob {
     const uint8_t* rb_flags;
     int64_t rb_nflags;
     int rb_emulated;
+    // emulated fallback after a rebias pass: workspace for splitting the
+    // flagged tiles' K (4 counters per split tile, zero on entry; split_cap
+    // FP32 128 x 128 partial tiles); null: no split
+    uint32_t* split_cnt;
+    float* split_buf;
+    int64_t split_cap;
 };
+// Split tiles of the emulated fallback (bounds the counters and partial
+// tiles the workspace holds; at least the SM count).
+constexpr int64_t kEmuSplitMaxTiles = 256;
 cudaError_t launch_gemm_nvfp4(const GemmJob& job, cudaStream_t stream);
 cudaError_t launch_gemm_ue5m3(const GemmJob& job, cudaStream_t stream);
 // Rewrite the UE5M3 block scales of A (M rows) and B (N rows), tensor-core
@@ -138,9 +147,10 @@ cudaError_t launch_gemm_ue5m3(const GemmJob& job, cudaStream_t stream);
 // two: s = e4m3_out * 2^off[row] exactly. flags[t] (one byte per 128-row tile,
 // A's tiles first, M / 128 + N / 128 in all) is set to 1 if a row of tile t
 // has scales spanning more binades than E4M3 holds, else to 0.
+// It also zeroes n_clear words at `clear` (the emulated fallback's split counters).
 cudaError_t launch_rebias_ue5m3(const uint8_t* a_scales, int64_t M, const uint8_t* b_scales, int64_t N, int64_t K,
                                 uint8_t* a_out, uint8_t* b_out, int8_t* a_off, int8_t* b_off, uint8_t* flags,
-                                cudaStream_t stream);
+                                uint32_t* clear, int64_t n_clear, cudaStream_t stream);
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
 // completes; after limit_ns the wait records FP4_ERR_DEVICE_TIMEOUT in *status
 // and the kernel returns.

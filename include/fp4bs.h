@@ -272,9 +272,13 @@ fp4_status_t fp4_gemm(const fp4_tensor_t* a, const fp4_tensor_t* b, void* d, int
  * span more than E4M3's 15 binades cannot be rebiased: the output tiles its
  * 128-row tile touches are computed by the emulated kernel, all others by the
  * native one; the split is made on the device (no host synchronisation), and
- * the emulated kernel returns at once when no row was flagged. ws: device, 16-byte aligned, at least
- * fp4_gemm_workspace_bytes(a, b) bytes (about (M + N) * K / 16), owned by the
- * caller, overwritten, not to be shared by calls in flight at the same time.
+ * the emulated kernel returns at once when no row was flagged. When the
+ * flagged output tiles are fewer than the SMs, the emulated kernel splits
+ * their K across the idle SMs and adds the FP32 parts in a fixed order (the
+ * result does not depend on timing). ws: device, 16-byte aligned, at least
+ * fp4_gemm_workspace_bytes(a, b) bytes (about (M + N) * K / 16, plus up to
+ * 16 MB of FP32 partial tiles for that split), owned by the caller,
+ * overwritten, not to be shared by calls in flight at the same time.
  * Too small or NULL: FP4_ERR_WORKSPACE. Other scale formats ignore ws and run
  * exactly as fp4_gemm. After the stream has run the call, byte t of ws
  * (t < M / 128 + N / 128, A's 128-row tiles first) is 1 if tile t held a row

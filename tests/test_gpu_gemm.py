@@ -291,7 +291,9 @@ def test_gemm_ue5m3_rebias_edges_and_fallback():
     mantissa <= 6 (exponent 8) with the smallest 14 binades below; UE5M3
     subnormal scales. All fit and run natively. One more binade in a single row
     sends the output tiles of its 128-row tile to the emulated kernel while the
-    native kernel computes the rest. Every output gives the oracle's sums."""
+    native kernel computes the rest; then one more row of B does the same for
+    its tile column (the emulated kernel numbers both kinds of flagged tiles and
+    splits their K over the idle SMs). Every output gives the oracle's sums."""
     M, N, K = 256, 256, 512
     ra, _ = _operand(45, M, K, "normal", fmt=UE)
     rb, _ = _operand(46, N, K, "weight", fmt=UE)
@@ -300,9 +302,11 @@ def test_gemm_ue5m3_rebias_edges_and_fallback():
     _set_row(sa, 130, [0xA6, 0x30, 0x99])              # E 5 (f 6) .. -9
     _set_row(sb, 7, [0x50, 0x01, 0x03, 0x07, 0x0F])    # E -5 .. -17 (subnormals)
     _set_row(sb, 255, [0x00])                          # all-zero row
-    for fallback in (False, True):
+    for fallback in (False, True, "a_and_b"):
         if fallback:
             _set_row(sa, 9, [0xA7, 0x30])              # 14 binades under a mantissa-7 maximum
+        if fallback == "a_and_b":
+            _set_row(sb, 200, [0xA7, 0x30])            # and in B's second 128-row tile
         ra2, rb2 = dict(ra, scales=sa), dict(rb, scales=sb)
         a, b = upload_operand(ra2, M, K, UE), upload_operand(rb2, N, K, UE)
         for out32 in (False, True):
@@ -310,7 +314,7 @@ def test_gemm_ue5m3_rebias_edges_and_fallback():
             ws = _ws_for(a, b)
             fb.fp4_gemm(a, b, d, ws=ws)
             assert fb.fp4_device_status() == 0
-            assert _took_native(ws, a, b) == (not fallback)
+            assert _took_native(ws, a, b) == (fallback is False)
             c_ref, s = oracle.gemm(ra2["codes"], sa, ra2["s_dec"], rb2["codes"], sb, rb2["s_dec"],
                                    scale_fmt=oracle.FMT_UE5M3)
             _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
