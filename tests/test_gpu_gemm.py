@@ -320,6 +320,34 @@ def test_gemm_ue5m3_rebias_edges_and_fallback():
             _check(d.float().cpu().numpy(), c_ref, s, bf16=not out32)
 
 
+def test_gemm_ue5m3_fallback_more_tiles_than_sms_on_narrow_tiles():
+    """A B row that does not fit, with N % 256 != 0 (the native kernel runs
+    128 x 128 tiles, so only that tile column falls back) and 160 A row tiles:
+    160 flagged output tiles, more than the SMs, so the emulated kernel deals
+    them out from its lists without splitting K. Whole 128-row tiles (the
+    first, a middle one and the last; output rows are independent) give the
+    oracle's sums."""
+    M, N, K = 160 * 128, 384, 256
+    ra, a = _operand(61, M, K, "normal", fmt=UE)
+    rb, _ = _operand(62, N, K, "weight", fmt=UE)
+    sb = rb["scales"].copy()
+    _set_row(sb, 140, [0xA7, 0x30])  # 14 binades under a mantissa-7 maximum, B's tile 1
+    rb2 = dict(rb, scales=sb)
+    b = upload_operand(rb2, N, K, UE)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws = _ws_for(a, b)
+    fb.fp4_gemm(a, b, d, ws=ws)
+    assert fb.fp4_device_status() == 0
+    flags = ws[: M // 128 + N // 128].cpu().numpy()
+    assert flags[: M // 128].sum() == 0 and flags[M // 128:].tolist() == [0, 1, 0]
+    out = d.float().cpu().numpy()
+    for t in (0, 79, 159):
+        r = slice(128 * t, 128 * (t + 1))
+        c_ref, s = oracle.gemm(ra["codes"][r], ra["scales"][r], ra["s_dec"], rb2["codes"], sb, rb2["s_dec"],
+                               scale_fmt=oracle.FMT_UE5M3)
+        _check(out[r], c_ref, s, bf16=True)
+
+
 def test_gemm_ue5m3_workspace_checks():
     _, a = _operand(47, 128, 256, "normal", fmt=UE)
     _, b = _operand(48, 128, 256, "normal", fmt=UE)
