@@ -375,9 +375,10 @@ class Fp4Linear:
         _mark(mark, "dy/end")
 
     def _quantize_all_overlapped(self, x, w, dy, step, stream, mark=None):
-        # side stream: the tensor amaxes of W (smallest, first), X and dY; main
-        # stream: W, X and dY quantized with them as each becomes ready, so only
-        # W's amax pass is not hidden behind a conversion pass
+        # side stream: the tensor amaxes of W, X and dY, the smallest tensor
+        # first; main stream: the three quantized in the same order, each as
+        # soon as its amax is ready, so only the smallest tensor's amax pass is
+        # not hidden behind a conversion pass
         b, c, g, rht = self.bufs, self.counters, self.given, self.rht
         main = torch.cuda.current_stream() if stream is None else stream
         side = self.side
@@ -390,29 +391,31 @@ class Fp4Linear:
         dy_r = dict(round=FP4_ROUND_SR)
         dy_c = dict(orient=FP4_ORIENT_COLWISE, rht=rht, round=FP4_ROUND_SR)
         giv = dict(tscale=FP4_TSCALE_GIVEN)
-        fp4_tensor_amax(self._cfg(2, step, **w_cfg), w, g[2], self.ws_side[0], stream=side)
-        self.ev_amax[0].record(side)
-        fp4_tensor_amax_dual(self._cfg(0, step), self._cfg(1, step, **x_c), x, g[0], g[1], self.ws_side[1],
-                             stream=side)
-        self.ev_amax[1].record(side)
-        fp4_tensor_amax_dual(self._cfg(3, step, **dy_r), self._cfg(4, step, **dy_c), dy, g[3], g[4], self.ws_side[2],
-                             stream=side)
-        self.ev_amax[2].record(side)
-        main.wait_event(self.ev_amax[0])
-        _mark(mark, "w")
-        fp4_quantize(self._cfg(2, step, emit_transpose=True, **w_cfg, **giv), w, b["w"], b["wt"], state=g[2],
-                     counters=c[2], stream=main)
-        _mark(mark, "w/end")
-        main.wait_event(self.ev_amax[1])
-        _mark(mark, "x")
-        fp4_quantize_dual(self._cfg(0, step, **giv), self._cfg(1, step, **x_c, **giv), x, b["x"], b["xt"], g[0], g[1],
-                          c[0], c[1], stream=main)
-        _mark(mark, "x/end")
-        main.wait_event(self.ev_amax[2])
-        _mark(mark, "dy")
-        fp4_quantize_dual(self._cfg(3, step, **dy_r, **giv), self._cfg(4, step, **dy_c, **giv), dy, b["dy"], b["dyt"],
-                          g[3], g[4], c[3], c[4], stream=main)
-        _mark(mark, "dy/end")
+        jobs = [
+            ("w", w.numel(),
+             lambda: fp4_tensor_amax(self._cfg(2, step, **w_cfg), w, g[2], self.ws_side[0], stream=side),
+             lambda: fp4_quantize(self._cfg(2, step, emit_transpose=True, **w_cfg, **giv), w, b["w"], b["wt"],
+                                  state=g[2], counters=c[2], stream=main)),
+            ("x", x.numel(),
+             lambda: fp4_tensor_amax_dual(self._cfg(0, step), self._cfg(1, step, **x_c), x, g[0], g[1],
+                                          self.ws_side[1], stream=side),
+             lambda: fp4_quantize_dual(self._cfg(0, step, **giv), self._cfg(1, step, **x_c, **giv), x, b["x"],
+                                       b["xt"], g[0], g[1], c[0], c[1], stream=main)),
+            ("dy", dy.numel(),
+             lambda: fp4_tensor_amax_dual(self._cfg(3, step, **dy_r), self._cfg(4, step, **dy_c), dy, g[3], g[4],
+                                          self.ws_side[2], stream=side),
+             lambda: fp4_quantize_dual(self._cfg(3, step, **dy_r, **giv), self._cfg(4, step, **dy_c, **giv), dy,
+                                       b["dy"], b["dyt"], g[3], g[4], c[3], c[4], stream=main)),
+        ]
+        jobs.sort(key=lambda j: j[1])  # stable: W, X, dY among equal sizes
+        for i, (_, _, amax, _) in enumerate(jobs):
+            amax()
+            self.ev_amax[i].record(side)
+        for i, (name, _, _, quant) in enumerate(jobs):
+            main.wait_event(self.ev_amax[i])
+            _mark(mark, name)
+            quant()
+            _mark(mark, name + "/end")
 
     def gemms(self, y: torch.Tensor, dx: torch.Tensor, dw: torch.Tensor, stream=None, mark=None):
         """Fprop, Dgrad and Wgrad (`mark` as for quantize_all)."""
