@@ -145,6 +145,23 @@ struct Counts {
     uint32_t esat = 0, eunder = 0, ssat = 0, sunder = 0;
 };
 
+// (row, col) of tile t in a row-major grid with `cols` tiles per row. at()
+// divides once; advance() adds another cursor's offset with one carry (both
+// columns are below `cols`), so a grid-stride loop over tiles, whose threads
+// each convert only a few dozen elements per tile, needs no 64-bit division.
+struct TileCursor {
+    int64_t row, col;
+    __device__ __forceinline__ static TileCursor at(int64_t t, int64_t cols) { return TileCursor{t / cols, t % cols}; }
+    __device__ __forceinline__ void advance(const TileCursor& d, int64_t cols) {
+        row += d.row;
+        col += d.col;
+        if (col >= cols) {
+            col -= cols;
+            ++row;
+        }
+    }
+};
+
 // Sign bits of eight values placed at bit 3 of nibble i (the code's sign).
 __device__ __forceinline__ uint32_t sign_nibbles8(const float* v) {
     uint32_t s = 0u;
@@ -1039,25 +1056,29 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Colwise pair: channels c0 + 2 cp + ch, token block t0/16 + jb.
     const int cp = tid & 63, jb = tid >> 6;
     Counts cr, cc;
-    auto issue = [&](int64_t t, int s) {
-        const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
+    auto issue = [&](TileCursor at, int s) {
         const uint32_t bar = tc::smem_u32(&full_bar[s]);
         tc::mbar_arrive_expect_tx(bar, kDualTileBytes);
-        tc::tma_load_2d(tc::smem_u32(ring + s * kDualTileBytes), &tmap_x, (int32_t)c0, (int32_t)t0, bar);
+        tc::tma_load_2d(tc::smem_u32(ring + s * kDualTileBytes), &tmap_x, (int32_t)(at.col * kDualTC),
+                        (int32_t)(at.row * kDualTT), bar);
     };
     if (tid == 0) {
         tc::prefetch_tmap(&tmap_x);
         for (int k = 0; k < kDualStages; ++k) {
             const int64_t tk = blockIdx.x + (int64_t)k * gridDim.x;
-            if (tk < ntiles) issue(tk, k);
+            if (tk < ntiles) issue(TileCursor::at(tk, tiles_c), k);
         }
     }
+    // this tile's and the refill tile's coordinates, advanced without a division
+    TileCursor cur = TileCursor::at(blockIdx.x, tiles_c);
+    TileCursor ahead = TileCursor::at(blockIdx.x + (int64_t)kDualStages * gridDim.x, tiles_c);
+    const TileCursor step = TileCursor::at(gridDim.x, tiles_c);
     uint32_t it = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
         const int s = (int)(it % kDualStages);
         const bool ok = tc::mbar_wait(tc::smem_u32(&full_bar[s]), (it / kDualStages) & 1u, qr.status);
         const uint16_t* tile = reinterpret_cast<const uint16_t*>(ring + s * kDualTileBytes);
-        const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
+        const int64_t t0 = cur.row * kDualTT, c0 = cur.col * kDualTC;
         // rowwise: blocks (r, b) and (r + 32, b) of the tile's 64 x 8 blocks
         const int64_t code_row_tile = 8 * t0 * nb_row + (c0 >> 1);
         const int64_t sc_row_tile = 512 * ((t0 >> 7) * (nb_row >> 2) + (c0 >> 6)) + ((t0 & 64) >> 3);
@@ -1121,8 +1142,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!__syncthreads_and(ok)) break;
         if (tid == 0) {
             const int64_t tn = t + (int64_t)kDualStages * gridDim.x;
-            if (tn < ntiles) issue(tn, s);
+            if (tn < ntiles) issue(ahead, s);
         }
+        cur.advance(step, tiles_c);
+        ahead.advance(step, tiles_c);
     }
     flush_counters(qr.counters, cr.esat, cr.eunder, cr.ssat, cr.sunder);
     flush_counters(qc.counters, cc.esat, cc.eunder, cc.ssat, cc.sunder);
@@ -1151,19 +1174,22 @@ __global__ void __launch_bounds__(kAmaxTileThreads)
     }
     __syncthreads();
     const int64_t tiles_c = C / kDualTC, ntiles = (T / kDualTT) * tiles_c;
-    auto issue = [&](int64_t t, int s) {
-        const int64_t t0 = (t / tiles_c) * kDualTT, c0 = (t % tiles_c) * kDualTC;
+    auto issue = [&](TileCursor at, int s) {
         const uint32_t bar = tc::smem_u32(&full_bar[s]);
         tc::mbar_arrive_expect_tx(bar, kDualTileBytes);
-        tc::tma_load_2d(tc::smem_u32(ring + s * kDualTileBytes), &tmap_x, (int32_t)c0, (int32_t)t0, bar);
+        tc::tma_load_2d(tc::smem_u32(ring + s * kDualTileBytes), &tmap_x, (int32_t)(at.col * kDualTC),
+                        (int32_t)(at.row * kDualTT), bar);
     };
     if (tid == 0) {
         tc::prefetch_tmap(&tmap_x);
         for (int k = 0; k < kDualStages; ++k) {
             const int64_t tk = blockIdx.x + (int64_t)k * gridDim.x;
-            if (tk < ntiles) issue(tk, k);
+            if (tk < ntiles) issue(TileCursor::at(tk, tiles_c), k);
         }
     }
+    // the refill tile's coordinates, advanced without a division
+    TileCursor ahead = TileCursor::at(blockIdx.x + (int64_t)kDualStages * gridDim.x, tiles_c);
+    const TileCursor step = TileCursor::at(gridDim.x, tiles_c);
     uint32_t mp = 0u;   // max |x| as BF16 bit pairs
     float mr = 0.0f;    // max |RHT x| (times 4: the 1/4 is applied once at the end)
     uint32_t it = 0;
@@ -1203,8 +1229,9 @@ __global__ void __launch_bounds__(kAmaxTileThreads)
         if (!__syncthreads_and(ok)) break;
         if (tid == 0) {
             const int64_t tn = t + (int64_t)kDualStages * gridDim.x;
-            if (tn < ntiles) issue(tn, s);
+            if (tn < ntiles) issue(ahead, s);
         }
+        ahead.advance(step, tiles_c);
     }
     float vp = __uint_as_float(max(mp & 0xFFFFu, mp >> 16) << 16), vr = __fmul_rn(mr, 0.25f);
 #pragma unroll
